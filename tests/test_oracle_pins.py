@@ -1,0 +1,300 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each pin is written as a check on a GEMM callable ``gemm(A, B) -> C`` (FP32
+inputs, FP64 result), so the same checks run on the oracle and on planted
+mutants of it (``test_pins_reject_planted_mistakes``): a transposed operand,
+a dropped term, a wrong sign or a shifted index must each fail at least one.
+
+What pins the oracle:
+* all-ones inputs give C[i][j] = K exactly;
+* identity factors give the other factor back exactly;
+* closed forms for A[i][k] = i + k, B[k][j] = k + j (the 16x16x16 size of the
+  worked problem in "GEMM, step by step", section "Concept") and for the
+  asymmetric A[i][k] = i + 2k, B[k][j] = 3k + j on non-square shapes;
+* exact rational sums (Python fractions) on tiny random inputs, against the
+  rounding bound of a K-term double sum;
+* the 4x4, tile-2 worked example of "GEMM" (inference-book), section
+  "Shared memory tiling", read back bit by bit from a power-of-two encoding;
+* numpy's float64 matrix product as an independent library routine.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_07_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- pin checks
+
+def pin_all_ones(gemm):
+    for (M, N, K) in [(1, 1, 1), (5, 7, 3), (16, 16, 16), (33, 17, 64)]:
+        C = gemm(np.ones((M, K), np.float32), np.ones((K, N), np.float32))
+        if C.shape != (M, N) or not np.all(C == K):
+            return False
+    return True
+
+
+def pin_identity(gemm):
+    rng = np.random.default_rng(7)
+    B = rng.standard_normal((6, 9)).astype(np.float32)
+    A = rng.standard_normal((5, 6)).astype(np.float32)
+    ok = np.array_equal(gemm(np.eye(6, dtype=np.float32), B), B.astype(np.float64))
+    ok &= np.array_equal(gemm(A, np.eye(6, dtype=np.float32)), A.astype(np.float64))
+    return bool(ok)
+
+
+def _sums(K):
+    s1 = K * (K - 1) // 2               # sum of k
+    s2 = (K - 1) * K * (2 * K - 1) // 6  # sum of k^2
+    return s1, s2
+
+
+def pin_closed_form_symmetric(gemm, n=16):
+    i = np.arange(n, dtype=np.float32)
+    A = (i[:, None] + i[None, :]).astype(np.float32)    # A[i][k] = i + k
+    B = A.copy()                                          # B[k][j] = k + j
+    s1, s2 = _sums(n)
+    I, J = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    expect = n * I * J + (I + J) * s1 + s2
+    return bool(np.array_equal(gemm(A, B), expect.astype(np.float64)))
+
+
+def pin_closed_form_asymmetric(gemm, M=19, N=23, K=29):
+    A = (np.arange(M)[:, None] + 2 * np.arange(K)[None, :]).astype(np.float32)
+    B = (3 * np.arange(K)[:, None] + np.arange(N)[None, :]).astype(np.float32)
+    s1, s2 = _sums(K)
+    I, J = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    # sum_k (i + 2k)(3k + j) = K*i*j + 3*i*s1 + 2*j*s1 + 6*s2
+    expect = K * I * J + 3 * I * s1 + 2 * J * s1 + 6 * s2
+    return bool(np.array_equal(gemm(A, B), expect.astype(np.float64)))
+
+
+def pin_fractions(gemm, seed=3):
+    rng = np.random.default_rng(seed)
+    for (M, N, K) in [(1, 1, 1), (3, 2, 5), (4, 4, 4), (7, 8, 6), (2, 5, 8)]:
+        A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+        B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+        C = gemm(A, B)
+        for i in range(M):
+            for j in range(N):
+                terms = [Fraction(float(A[i, k])) * Fraction(float(B[k, j]))
+                         for k in range(K)]
+                exact = sum(terms, Fraction(0))
+                scale = sum((abs(t) for t in terms), Fraction(0))
+                # K-term recursive double sum of exact products
+                bound = Fraction(K) * Fraction(1, 2**53) * scale
+                if abs(Fraction(float(C[i, j])) - exact) > bound:
+                    return False
+    return True
+
+
+def pin_fractions_int(gemm, seed=4):
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-4, 5, (6, 9)).astype(np.float32)
+    B = rng.integers(-4, 5, (9, 5)).astype(np.float32)
+    C = gemm(A, B)
+    for i in range(6):
+        for j in range(5):
+            exact = sum(int(A[i, k]) * int(B[k, j]) for k in range(9))
+            if C[i, j] != exact:
+                return False
+    return True
+
+
+def pin_tiled_example(gemm):
+    """The 4x4, tile-2 worked example, decoded from a power-of-two encoding.
+
+    a[i][k] = 2^(4i + k) and b[k][j] = 2^(20 + 5k + j): the product for one k
+    is 2^(20 + 4i + j + 6k), so the set bits of C[0][0] name exactly the k
+    whose term it contains.
+    """
+    with open(os.path.join(GOLDEN, "p3_tiled_4x4.json")) as f:
+        g = json.load(f)
+    M, N, K, T = g["M"], g["N"], g["K"], g["tile"]
+    A = np.array([[2.0 ** (4 * i + k) for k in range(K)] for i in range(M)],
+                 np.float32)
+    B = np.array([[2.0 ** (20 + 5 * k + j) for j in range(N)] for k in range(K)],
+                 np.float32)
+    i0, j0 = g["output"]
+    partial = np.zeros((M, N))
+    for s, want in enumerate(g["terms_after_slice"]):
+        k0 = s * T
+        partial = partial + gemm(A[:, k0:k0 + T], B[k0:k0 + T, :])
+        v = int(partial[i0, j0])
+        got = [k for k in range(K) if v >> (20 + 4 * i0 + j0 + 6 * k) & 1]
+        if got != want or v != sum(1 << (20 + 4 * i0 + j0 + 6 * k) for k in want):
+            return False
+    # and the sliced sum equals the one-shot product everywhere
+    return bool(np.array_equal(partial, gemm(A, B)))
+
+
+def pin_numpy(gemm, seed=5):
+    rng = np.random.default_rng(seed)
+    A = rng.uniform(-1, 1, (37, 53)).astype(np.float32)
+    B = rng.uniform(-1, 1, (53, 29)).astype(np.float32)
+    ref = A.astype(np.float64) @ B.astype(np.float64)
+    S = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))
+    return bool(np.all(np.abs(gemm(A, B) - ref) <= 53 * 2.0**-53 * S))
+
+
+PINS = [pin_all_ones, pin_identity, pin_closed_form_symmetric,
+        pin_closed_form_asymmetric, pin_fractions, pin_fractions_int,
+        pin_tiled_example, pin_numpy]
+
+
+# ------------------------------------------------------------------- tests
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_f32_pins(oracle_mod, pin):
+    assert pin(lambda A, B: oracle_mod.gemm_f32(np.ascontiguousarray(A),
+                                                np.ascontiguousarray(B)))
+
+
+def _bf16_gemm(oracle_mod):
+    """The BF16 oracle driven with FP32 inputs that are exact in BF16."""
+    def gemm(A, B):
+        a = torch.from_numpy(np.ascontiguousarray(A)).to(torch.bfloat16)
+        b = torch.from_numpy(np.ascontiguousarray(B)).to(torch.bfloat16)
+        assert torch.equal(a.float(), torch.from_numpy(np.ascontiguousarray(A)))
+        assert torch.equal(b.float(), torch.from_numpy(np.ascontiguousarray(B)))
+        return oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b))
+    return gemm
+
+
+@pytest.mark.parametrize("pin", [pin_all_ones, pin_closed_form_symmetric,
+                                 pin_fractions_int, pin_tiled_example],
+                         ids=lambda p: p.__name__)
+def test_oracle_bf16_pins(oracle_mod, pin):
+    # these pins use values exactly representable in BF16 (8-bit mantissa)
+    assert pin(_bf16_gemm(oracle_mod))
+
+
+def test_bf16_closed_form_small(oracle_mod):
+    # i + 2k and 3k + j stay below 256, so BF16 holds them exactly
+    assert pin_closed_form_asymmetric(_bf16_gemm(oracle_mod), 19, 23, 29)
+
+
+def test_bf16_widening_known_patterns(oracle_mod):
+    cases = {0x3F80: 1.0, 0xBF80: -1.0, 0xC000: -2.0, 0x3F81: 1.0078125,
+             0x4049: 3.140625, 0x0000: 0.0, 0x0001: 2.0**-133,
+             0x7F7F: 3.3895313892515355e38}
+    for bits, val in cases.items():
+        assert oracle_mod.bf16_to_double(bits) == val
+    assert oracle_mod.bf16_to_double(0x7F80) == float("inf")
+
+
+def test_bf16_widening_matches_torch(oracle_mod):
+    bits = np.arange(0, 1 << 16, 97, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double()
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref.numpy())
+    assert np.array_equal(got[finite], ref.numpy()[finite])
+    assert np.all(np.isnan(got[~finite]) == np.isnan(ref.numpy()[~finite]))
+
+
+def test_abs_scale(oracle_mod):
+    rng = np.random.default_rng(11)
+    A = rng.uniform(0, 1, (9, 14)).astype(np.float32)
+    B = rng.uniform(0, 1, (14, 6)).astype(np.float32)
+    C, S = oracle_mod.gemm_f32(A, B, with_abs=True)
+    assert np.array_equal(C, S)                    # nonnegative: |p| = p
+    C2, S2 = oracle_mod.gemm_f32(-A, B, with_abs=True)
+    assert np.array_equal(C2, -C) and np.array_equal(S2, S)
+    A3 = A.copy()
+    A3[:, ::2] *= -1
+    C3, S3 = oracle_mod.gemm_f32(A3, B, with_abs=True)
+    assert np.array_equal(S3, S)
+    assert np.all(np.abs(C3) <= S3)
+
+
+def test_leading_dimensions(oracle_mod):
+    a, b = inputs.make_pair(13, 11, 17, 0, inputs.UNIFORM)
+    aw = inputs.with_leading_dim(a, 24).numpy()
+    bw = inputs.with_leading_dim(b, 16).numpy()
+    assert aw.strides[0] == 24 * 4 and bw.strides[0] == 16 * 4
+    assert np.array_equal(oracle_mod.gemm_f32(aw, bw),
+                          oracle_mod.gemm_f32(a.numpy(), b.numpy()))
+
+
+def test_empty_and_zero_k(oracle_mod):
+    C = oracle_mod.gemm_f32(np.zeros((3, 0), np.float32),
+                            np.zeros((0, 4), np.float32))
+    assert C.shape == (3, 4) and np.all(C == 0)
+    C = oracle_mod.gemm_f32(np.zeros((0, 5), np.float32),
+                            np.zeros((5, 4), np.float32))
+    assert C.shape == (0, 4)
+
+
+def test_invalid_arguments(oracle_mod):
+    import ctypes
+    lib = oracle_mod._load()
+    buf = (ctypes.c_double * 64)()
+    f = (ctypes.c_float * 64)()
+    assert lib.oracle_gemm_f32(-1, 2, 2, f, 2, f, 2, buf, 2, None) == -1
+    assert lib.oracle_gemm_f32(2, 2, 4, f, 3, f, 2, buf, 2, None) == -1  # lda < K
+    assert lib.oracle_gemm_f32(2, 4, 2, f, 2, f, 3, buf, 4, None) == -1  # ldb < N
+    assert lib.oracle_gemm_f32(2, 4, 2, f, 2, f, 4, buf, 3, None) == -1  # ldc < N
+    assert lib.oracle_gemm_f32(2, 2, 2, None, 2, f, 2, buf, 2, None) == -1
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_f32(np.zeros((2, 3), np.float32),
+                            np.zeros((4, 2), np.float32))
+
+
+def test_flop_count(oracle_mod):
+    assert oracle_mod.gemm_flops(4096, 4096, 4096) == 2 * 4096**3
+    # "about 1.37 x 10^11 FLOPs" for the 4096^3 problem
+    assert round(oracle_mod.gemm_flops(4096, 4096, 4096) / 1e11, 2) == 1.37
+    assert oracle_mod.gemm_flops(3, 5, 7) == 210
+
+
+def test_threads_reported(oracle_mod):
+    assert oracle_mod.max_threads() >= 1
+
+
+# ------------------------------------------------------- planted mistakes
+
+def _np_gemm(A, B):
+    return A.astype(np.float64) @ B.astype(np.float64)
+
+
+MUTANTS = {
+    "transposed_B": lambda A, B: A.astype(np.float64) @ B.T.astype(np.float64)
+    if A.shape[1] == B.shape[1] else _np_gemm(A, B[:, ::-1]),
+    "transposed_A": lambda A, B: A.T.astype(np.float64) @ B.astype(np.float64)
+    if A.shape[0] == A.shape[1] else _np_gemm(A[::-1], B),
+    "dropped_last_k": lambda A, B: _np_gemm(A[:, :-1], B[:-1, :])
+    if A.shape[1] > 1 else 0 * _np_gemm(A, B),
+    "dropped_first_k": lambda A, B: _np_gemm(A[:, 1:], B[1:, :])
+    if A.shape[1] > 1 else 0 * _np_gemm(A, B),
+    "negated": lambda A, B: -_np_gemm(A, B),
+    "k_shift_in_B": lambda A, B: _np_gemm(A, np.roll(B, 1, axis=0)),
+    "column_shift_in_C": lambda A, B: np.roll(_np_gemm(A, B), 1, axis=1),
+    "float32_accumulation": lambda A, B: (A @ B).astype(np.float32).astype(np.float64),
+    "abs_products": lambda A, B: np.abs(A).astype(np.float64) @ np.abs(B).astype(np.float64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_mistakes(name):
+    mutant = MUTANTS[name]
+    failed = []
+    for pin in PINS:
+        try:
+            ok = pin(mutant)
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_pins_accept_exact_numpy():
+    # the plain float64 product (a library routine) passes every pin
+    for pin in PINS:
+        assert pin(_np_gemm), pin.__name__
