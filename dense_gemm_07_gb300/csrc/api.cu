@@ -1,0 +1,456 @@
+// api.cu -- the C ABI declared in include/gemm07.h: argument checking, path
+// selection, tensor-map encoding, per-device state and the kernel launches.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gemm07.h"
+#include "kernels.h"
+#include "tile_order.cuh"
+
+namespace g07 {
+namespace {
+
+// Device-side status word: bit 0 = a bounded wait ran out.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 0x7FFFFFFF;  // M, N, K < 2^31
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned int* status = nullptr;  // address of g_status_word on this device
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType,
+                                   cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
+                         int64_t lda, const void* B, int64_t ldb,
+                         const void* C, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
+  return GEMM_OK;
+}
+
+void plan_clear(gemm_plan_t* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->split_k = 1;
+}
+
+gemm_status_t plan_f32(int64_t M, int64_t N, int64_t K, const void* A,
+                       int64_t lda, const void* B, int64_t ldb, const void* C,
+                       int64_t ldc, gemm_plan_t* p) {
+  plan_clear(p);
+  const gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) {
+    p->path = GEMM_PATH_NONE;
+    return GEMM_OK;
+  }
+  if (K == 0) {
+    p->path = GEMM_PATH_ZERO_FILL;
+    return GEMM_OK;
+  }
+  p->path = GEMM_PATH_F32_SIMT;
+  p->tile_m = kF32TileM;
+  p->tile_n = kF32TileN;
+  p->tile_k = kF32TileK;
+  p->stages = 2;
+  p->tiles = ((M + kF32TileM - 1) / kF32TileM) * ((N + kF32TileN - 1) / kF32TileN);
+  if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  return GEMM_OK;
+}
+
+gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
+                        int64_t lda, const void* B, int64_t ldb, const void* C,
+                        int64_t ldc, gemm_plan_t* p) {
+  plan_clear(p);
+  const gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) {
+    p->path = GEMM_PATH_NONE;
+    return GEMM_OK;
+  }
+  if (K == 0) {
+    p->path = GEMM_PATH_ZERO_FILL;
+    return GEMM_OK;
+  }
+  // The tensor-memory accelerator reads an operand in place when its base is
+  // 16-byte aligned and its row stride is a multiple of 16 bytes (8 BF16).
+  p->pack_a = (aligned16(A) && lda % 8 == 0) ? 0 : 1;
+  p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
+  p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
+  p->tile_m = kTcTileM;
+  p->tile_n = kTcTileN;
+  p->tile_k = kTcTileK;
+  p->stages = kTcStages;
+  p->tiles = ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
+  if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  int64_t ws = 0;
+  if (p->pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
+  if (p->pack_b) ws += round_up(K * round_up(N, 8) * 2, 256);
+  p->workspace_bytes = ws;
+  return GEMM_OK;
+}
+
+gemm_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return GEMM_OK;
+  if (e == cudaErrorMemoryAllocation) return GEMM_ERR_NO_MEMORY;
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ||
+      e == cudaErrorNoKernelImageForDevice)
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  return GEMM_ERR_LAUNCH;
+}
+
+// Per-device set-up, once: capability check, status word, memory pool.
+gemm_status_t device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      d.status = static_cast<unsigned int*>(addr);
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_MEMORY;
+      }
+      uint64_t keep = ~0ull;  // keep freed blocks for the next call
+      cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return GEMM_OK;
+}
+
+gemm_status_t encoder(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = g_encode;
+  return GEMM_OK;
+}
+
+// 2-D BF16 tensor map: dims {inner, outer}, row stride ld elements, box
+// {box_inner, box_outer}, 128-byte swizzle, zero fill out of range.
+gemm_status_t make_map(CUtensorMap* map, const void* base, int64_t inner,
+                       int64_t outer, int64_t ld, uint32_t box_inner,
+                       uint32_t box_outer) {
+  EncodeTiledFn enc = nullptr;
+  gemm_status_t s = encoder(&enc);
+  if (s != GEMM_OK) return s;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner),
+                              static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INTERNAL;
+}
+
+gemm_status_t pool_alloc(DeviceState* d, void** p, int64_t bytes,
+                         cudaStream_t stream) {
+  *p = nullptr;
+  if (bytes <= 0) return GEMM_OK;
+  if (cudaMallocFromPoolAsync(p, static_cast<size_t>(bytes), d->pool, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return GEMM_ERR_NO_MEMORY;
+  }
+  return GEMM_OK;
+}
+
+void pool_free(void* p, cudaStream_t stream) {
+  if (p) cudaFreeAsync(p, stream);
+}
+
+gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
+                      int64_t lda, const float* B, int64_t ldb, float* C,
+                      int64_t ldc, cudaStream_t stream) {
+  gemm_plan_t plan;
+  gemm_status_t s = plan_f32(M, N, K, A, lda, B, ldb, C, ldc, &plan);
+  if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
+  DeviceState* d = nullptr;
+  s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  if (plan.path == GEMM_PATH_ZERO_FILL)
+    return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
+                                          static_cast<int>(N), stream));
+  const bool vec_a = aligned16(A) && lda % 4 == 0;
+  const bool vec_b = aligned16(B) && ldb % 4 == 0;
+  const bool vec_c = aligned16(C) && ldc % 4 == 0;
+  return from_cuda(launch_gemm_f32(static_cast<int>(M), static_cast<int>(N),
+                                   static_cast<int>(K), A, lda, B, ldb, C, ldc,
+                                   vec_a, vec_b, vec_c, stream));
+}
+
+gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                       int64_t lda, const uint16_t* B, int64_t ldb, float* C,
+                       int64_t ldc, cudaStream_t stream) {
+  gemm_plan_t plan;
+  gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan);
+  if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
+  DeviceState* d = nullptr;
+  s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  if (plan.path == GEMM_PATH_ZERO_FILL)
+    return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
+                                          static_cast<int>(N), stream));
+
+  const int m = static_cast<int>(M), n = static_cast<int>(N),
+            k = static_cast<int>(K);
+  void* ws = nullptr;
+  s = pool_alloc(d, &ws, plan.workspace_bytes, stream);
+  if (s != GEMM_OK) return s;
+  const uint16_t* a_op = A;
+  const uint16_t* b_op = B;
+  int64_t lda_op = lda, ldb_op = ldb;
+  uint8_t* cursor = static_cast<uint8_t*>(ws);
+  if (plan.pack_a) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    lda_op = round_up(K, 8);
+    cursor += round_up(M * lda_op * 2, 256);
+    s = from_cuda(launch_copy_rows_u16(A, lda, dst, lda_op, m, k, stream));
+    a_op = dst;
+  }
+  if (s == GEMM_OK && plan.pack_b) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    ldb_op = round_up(N, 8);
+    s = from_cuda(launch_copy_rows_u16(B, ldb, dst, ldb_op, k, n, stream));
+    b_op = dst;
+  }
+  CUtensorMap tmA, tmB;
+  if (s == GEMM_OK)
+    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK, kTcTileM);
+  if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
+  if (s == GEMM_OK) {
+    const int grid = static_cast<int>(plan.tiles < d->sms ? plan.tiles : d->sms);
+    const bool vec_c = aligned16(C) && ldc % 4 == 0;
+    s = from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
+                                      d->status, stream));
+  }
+  pool_free(ws, stream);
+  return s;
+}
+
+// Host-buffer variant: stage through pool memory, run, copy back, sync.
+template <typename T, typename Run>
+gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
+                       int64_t lda, const T* B, int64_t ldb, float* C,
+                       int64_t ldc, cudaStream_t stream, Run run) {
+  gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (s != GEMM_OK || M == 0 || N == 0) return s;
+  DeviceState* d = nullptr;
+  s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  const int64_t eb = static_cast<int64_t>(sizeof(T));
+  s = pool_alloc(d, &dA, M * K * eb, stream);
+  if (s == GEMM_OK) s = pool_alloc(d, &dB, K * N * eb, stream);
+  if (s == GEMM_OK) s = pool_alloc(d, &dC, M * N * 4, stream);
+  if (s == GEMM_OK && K > 0)
+    s = from_cuda(cudaMemcpy2DAsync(dA, K * eb, A, lda * eb, K * eb, M,
+                                    cudaMemcpyHostToDevice, stream));
+  if (s == GEMM_OK && K > 0)
+    s = from_cuda(cudaMemcpy2DAsync(dB, N * eb, B, ldb * eb, N * eb, K,
+                                    cudaMemcpyHostToDevice, stream));
+  if (s == GEMM_OK)
+    s = run(M, N, K, static_cast<const T*>(dA), K > 0 ? K : 1,
+            static_cast<const T*>(dB), N, static_cast<float*>(dC), N, stream);
+  if (s == GEMM_OK)
+    s = from_cuda(cudaMemcpy2DAsync(C, ldc * 4, dC, N * 4, N * 4, M,
+                                    cudaMemcpyDeviceToHost, stream));
+  pool_free(dA, stream);
+  pool_free(dB, stream);
+  pool_free(dC, stream);
+  const cudaError_t e = cudaStreamSynchronize(stream);
+  if (s == GEMM_OK) s = from_cuda(e);
+  return s;
+}
+
+}  // namespace
+}  // namespace g07
+
+using namespace g07;
+
+extern "C" {
+
+gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K, const float* A,
+                       int64_t lda, const float* B, int64_t ldb, float* C,
+                       int64_t ldc, void* stream) {
+  return run_f32(M, N, K, A, lda, B, ldb, C, ldc,
+                 static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
+                               const uint16_t* A, int64_t lda,
+                               const uint16_t* B, int64_t ldb, float* C,
+                               int64_t ldc, void* stream) {
+  return run_bf16(M, N, K, A, lda, B, ldb, C, ldc,
+                  static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
+                            int64_t lda, const float* B, int64_t ldb, float* C,
+                            int64_t ldc, void* stream) {
+  return run_host<float>(M, N, K, A, lda, B, ldb, C, ldc,
+                         static_cast<cudaStream_t>(stream), run_f32);
+}
+
+gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
+                                    const uint16_t* A, int64_t lda,
+                                    const uint16_t* B, int64_t ldb, float* C,
+                                    int64_t ldc, void* stream) {
+  return run_host<uint16_t>(M, N, K, A, lda, B, ldb, C, ldc,
+                            static_cast<cudaStream_t>(stream), run_bf16);
+}
+
+const char* gemm_status_string(gemm_status_t status) {
+  switch (status) {
+    case GEMM_OK: return "success";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument (size, leading dimension or pointer)";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3 (sm_103a) is current";
+    case GEMM_ERR_LAUNCH: return "a CUDA call or kernel launch failed";
+    case GEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out; the output is incomplete";
+    case GEMM_ERR_NO_MEMORY: return "device workspace allocation failed";
+    case GEMM_ERR_INTERNAL: return "internal error (tensor map encoding)";
+  }
+  return "unknown status";
+}
+
+gemm_status_t gemm_get_device_status(void* stream) {
+  DeviceState* d = nullptr;
+  gemm_status_t s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(d->status, 0, sizeof(v));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return (v & 1u) ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+void gemm_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int cur = -1;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (int i = 0; i < kMaxDevices; ++i) {
+    DeviceState& d = g_dev[i];
+    if (d.pool) {
+      if (cudaSetDevice(i) == cudaSuccess) {
+        cudaDeviceSynchronize();
+        cudaMemPoolDestroy(d.pool);
+      }
+    }
+    d = DeviceState();
+  }
+  if (have_cur) cudaSetDevice(cur);
+  cudaGetLastError();
+}
+
+int gemm_abi_version(void) { return 1; }
+
+gemm_status_t gemm_tile_order(int64_t tiles_m, int64_t tiles_n, int64_t group,
+                              int64_t linear, int64_t* tile_m,
+                              int64_t* tile_n) {
+  if (tiles_m <= 0 || tiles_n <= 0 || group <= 0 || tiles_m > kMaxDim ||
+      tiles_n > kMaxDim || group > kMaxDim || tile_m == nullptr ||
+      tile_n == nullptr || linear < 0 || linear >= tiles_m * tiles_n)
+    return GEMM_ERR_INVALID_ARG;
+  const TileCoord t = tile_order(linear, static_cast<int32_t>(tiles_m),
+                                 static_cast<int32_t>(tiles_n),
+                                 static_cast<int32_t>(group));
+  *tile_m = t.m;
+  *tile_n = t.n;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
+                             int64_t lda, const void* B, int64_t ldb,
+                             const void* C, int64_t ldc, gemm_plan_t* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  return plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, plan);
+}
+
+gemm_status_t gemm_plan_f32(int64_t M, int64_t N, int64_t K, const void* A,
+                            int64_t lda, const void* B, int64_t ldb,
+                            const void* C, int64_t ldc, gemm_plan_t* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  return plan_f32(M, N, K, A, lda, B, ldb, C, ldc, plan);
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cu)
+// and the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace g07 {
+
+// ---- FP32 SIMT path (gemm_f32.cu)
+constexpr int kF32TileM = 128;
+constexpr int kF32TileN = 128;
+constexpr int kF32TileK = 16;
+constexpr int kF32Group = 8;
+
+cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
+                            const float* B, int64_t ldb, float* C, int64_t ldc,
+                            bool vec_a, bool vec_b, bool vec_c,
+                            cudaStream_t stream);
+
+// ---- BF16 tensor-core path (gemm_bf16_tc.cu)
+constexpr int kTcTileM = 128;
+constexpr int kTcTileN = 256;
+constexpr int kTcTileK = 64;
+constexpr int kTcStages = 4;
+constexpr int kTcGroup = 8;
+
+size_t tc_smem_bytes();
+
+// A and B described by tensor maps (K-major A box 64 x 128, N-major B box
+// 64 x 64, both 128-byte swizzled).  `grid` persistent CTAs walk the tiles.
+cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                float* C, int64_t ldc, int M, int N, int K,
+                                bool vec_c, int grid, unsigned int* status,
+                                cudaStream_t stream);
+
+// ---- small helpers (gemm_aux.cu)
+cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
+                                 cudaStream_t stream);
+// Copy a rows x cols matrix of 16-bit elements to dst with row stride ld_dst.
+cudaError_t launch_copy_rows_u16(const uint16_t* src, int64_t ld_src,
+                                 uint16_t* dst, int64_t ld_dst, int rows,
+                                 int cols, cudaStream_t stream);
+
+}  // namespace g07

@@ -1,0 +1,195 @@
+/*
+ * gemm07.h -- C ABI of libgemm07.so, dense GEMM C = A * B on one NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The operation (every entry point below computes it):
+ *   C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j],   0 <= i < M, 0 <= j < N,
+ * with A (M x K), B (K x N) and C (M x N) row-major: element (r, c) of a
+ * matrix with leading dimension ld sits at base + r*ld + c.
+ *   - "GEMM" (inference-book, Part 4), opening section: the element formula.
+ *   - "GEMM Optimization" (infra.bea.ai), section 1 "The Problem".
+ *   - "How a Matrix Multiply Runs on a GPU", "Level 0": the row-major
+ *     indexing A[row*K + k], B[k*N + col], C[row*N + col].
+ * C is overwritten (no alpha/beta).  K == 0 writes zeros into C (the empty
+ * sum); M == 0 or N == 0 is a no-op.  Out-of-range rows and columns of a
+ * ragged edge tile contribute zero and are never written ("A06 -- Tiled
+ * Matrix Multiply (GEMM)", section 3, the guarded tiled kernel and ": 0.0f").
+ *
+ * Conventions shared by every entry point:
+ *   - Sizes and leading dimensions are element counts (int64_t).  Required:
+ *     M, N, K >= 0, lda >= max(K, 1), ldb >= max(N, 1), ldc >= max(N, 1),
+ *     and M, N, K < 2^31.
+ *   - Pointers are DEVICE pointers on the calling thread's current device,
+ *     owned by the caller; the library keeps none of them after the call
+ *     returns, and never frees caller memory.  A null pointer is allowed only
+ *     for an operand with no elements.  C must not overlap A or B
+ *     (unchecked).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls only enqueue work and return without synchronising;
+ *     a device-side failure (a bounded wait that ran out) is reported by
+ *     gemm_get_device_status().
+ *   - Results are deterministic: the same inputs, sizes and device give the
+ *     same bits on every call (no atomics in any reduction).
+ *   - Calls are thread-safe.  The library may hold per-device state (a
+ *     status word, a workspace pool) until gemm_shutdown() or process exit.
+ *
+ * Errors: every entry point returns a gemm_status_t.  Argument errors are
+ * detected on the host before anything is enqueued and leave C untouched.
+ */
+#ifndef GEMM07_H
+#define GEMM07_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM07_API __attribute__((visibility("default")))
+#else
+#define GEMM07_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* negative size, short ld, null pointer */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 2, /* no device, or not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = 3,             /* a CUDA call or kernel launch failed */
+    GEMM_ERR_TIMEOUT = 4,            /* a device-side bounded wait ran out */
+    GEMM_ERR_NO_MEMORY = 5,          /* workspace or staging allocation failed */
+    GEMM_ERR_INTERNAL = 6
+} gemm_status_t;
+
+/*
+ * gemm_f32 -- FP32 inputs, FP32 output, FP32 arithmetic on the CUDA cores
+ * (no tensor cores).
+ *   Method: the register-blocked, shared-memory-tiled kernel of "GEMM,
+ *   step by step" (section "Concept", register blocking: each thread owns an
+ *   8 x 8 patch of C, 128 x 128 blocks) and "A06 -- Tiled Matrix Multiply",
+ *   section 3 (transposed A tile with padding, vectorised shared reads,
+ *   double buffering).  Each product is fused into its running FP32 sum
+ *   (FMA); the order of the sum over k is increasing k.
+ *   A: M x K floats, row stride lda.  B: K x N floats, row stride ldb.
+ *   C: M x N floats, row stride ldc; columns N..ldc-1 are not touched.
+ *   Any alignment and any leading dimension are accepted; 16-byte aligned
+ *   bases with ld a multiple of 4 take the vectorised loads.
+ */
+GEMM07_API gemm_status_t gemm_f32(int64_t M, int64_t N, int64_t K,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc, void *stream);
+
+/*
+ * gemm_bf16_f32acc -- BF16 inputs, FP32 accumulation, FP32 output, on the
+ * tensor cores (tcgen05.mma, accumulators in tensor memory).
+ *   Method: the tensor-core rung of "GEMM, step by step" (section
+ *   "Concept": BF16 inputs, FP32 sums, large 128 x 256 tiles, neighbouring
+ *   blocks kept on the same rows and columns so their loads hit L2) and the
+ *   block-order swizzle of "GEMM Optimization", section "L2 Cache and Wave
+ *   Analysis".  Every BF16 x BF16 product is exact in FP32; the sums are
+ *   FP32.
+ *   A, B: arrays of BF16 values, passed as their 16-bit patterns (uint16_t,
+ *   bit-compatible with __nv_bfloat16).  A: M x K, row stride lda.
+ *   B: K x N, row stride ldb.  C: M x N floats, row stride ldc.
+ *   Fast path: A and B 16-byte aligned with lda and ldb multiples of 8 (the
+ *   operands are then read directly by the tensor-memory accelerator).
+ *   Other layouts are first copied on the GPU into an aligned workspace
+ *   taken from a library-owned, stream-ordered memory pool.
+ */
+GEMM07_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
+                               const uint16_t *A, int64_t lda,
+                               const uint16_t *B, int64_t ldb,
+                               float *C, int64_t ldc, void *stream);
+
+/*
+ * Host-buffer variants: the same operations with A, B and C in HOST memory
+ * (pinned memory gives the fastest copies; pageable memory works).  The
+ * call copies A and B to device staging buffers on `stream`, runs the GEMM,
+ * copies C back and synchronises `stream` before it returns.  Staging
+ * buffers come from the library's memory pool on the current device.
+ */
+GEMM07_API gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K,
+                            const float *A, int64_t lda,
+                            const float *B, int64_t ldb,
+                            float *C, int64_t ldc, void *stream);
+GEMM07_API gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
+                                    const uint16_t *A, int64_t lda,
+                                    const uint16_t *B, int64_t ldb,
+                                    float *C, int64_t ldc, void *stream);
+
+/* Static English text for a status code (never NULL). */
+GEMM07_API const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's
+ * device-side status word.  Returns GEMM_ERR_TIMEOUT if any kernel since the
+ * last call gave up on a bounded wait (its output is then incomplete),
+ * GEMM_ERR_LAUNCH if the stream reports a CUDA error, GEMM_OK otherwise.
+ */
+GEMM07_API gemm_status_t gemm_get_device_status(void *stream);
+
+/* Releases per-device state held by the library (pools, status words). */
+GEMM07_API void gemm_shutdown(void);
+
+/* ABI version of this header: 1. */
+GEMM07_API int gemm_abi_version(void);
+
+/*
+ * Host-only helpers (no GPU needed), exported so that the tile scheduling
+ * and the path selection can be checked without a device.
+ *
+ * gemm_tile_order: the block-order swizzle.  Maps the linear tile index
+ * `linear` (0 <= linear < tiles_m * tiles_n) to the tile (*tile_m, *tile_n)
+ * it computes.  Tiles are visited in bands of `group` tile-rows; inside a
+ * band the index runs down a column of tiles before moving to the next
+ * column, so tiles computed at the same time share rows of A and columns of
+ * B ("GEMM Optimization", section "L2 Cache and Wave Analysis").  Returns
+ * GEMM_ERR_INVALID_ARG when an argument is out of range.
+ */
+GEMM07_API gemm_status_t gemm_tile_order(int64_t tiles_m, int64_t tiles_n, int64_t group,
+                              int64_t linear, int64_t *tile_m, int64_t *tile_n);
+
+/* Which kernel path a call with these arguments takes (no GPU needed). */
+typedef enum gemm_path {
+    GEMM_PATH_NONE = 0,         /* M == 0 or N == 0: nothing to do          */
+    GEMM_PATH_ZERO_FILL = 1,    /* K == 0: C := 0                           */
+    GEMM_PATH_F32_SIMT = 2,     /* gemm_f32 register-blocked kernel         */
+    GEMM_PATH_BF16_TMA = 3,     /* tcgen05 kernel reading the operands      */
+    GEMM_PATH_BF16_PACKED = 4,  /* operands copied to aligned workspace first */
+    GEMM_PATH_BF16_SKINNY = 5   /* small M: split-K tcgen05, B streamed once */
+} gemm_path_t;
+
+typedef struct gemm_plan {
+    int32_t path;          /* a gemm_path_t                                  */
+    int32_t tile_m;        /* output tile rows                               */
+    int32_t tile_n;        /* output tile columns                            */
+    int32_t tile_k;        /* k-slice per pipeline stage                     */
+    int32_t stages;        /* shared-memory ring depth                       */
+    int32_t split_k;       /* slices of K reduced afterwards (1 = none)      */
+    int64_t tiles;         /* output tiles (x split_k work units)            */
+    int64_t workspace_bytes; /* device scratch the call takes from the pool */
+    int32_t pack_a;        /* 1 if A is first copied to aligned workspace    */
+    int32_t pack_b;        /* 1 if B is first copied to aligned workspace    */
+} gemm_plan_t;
+
+/*
+ * gemm_plan_bf16 / gemm_plan_f32: fill *plan with the path that the
+ * corresponding entry point takes for these arguments.  Pointers are only
+ * inspected for their alignment, never dereferenced.  Returns the status
+ * the entry point would return from argument checking.
+ */
+GEMM07_API gemm_status_t gemm_plan_bf16(int64_t M, int64_t N, int64_t K,
+                             const void *A, int64_t lda,
+                             const void *B, int64_t ldb,
+                             const void *C, int64_t ldc, gemm_plan_t *plan);
+GEMM07_API gemm_status_t gemm_plan_f32(int64_t M, int64_t N, int64_t K,
+                            const void *A, int64_t lda,
+                            const void *B, int64_t ldb,
+                            const void *C, int64_t ldc, gemm_plan_t *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM07_H */

@@ -1,0 +1,140 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol the
+header declares, and its host-only logic (tile order, path planning,
+argument checks, status strings) behaves as documented.  No GPU work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import _abi, _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "gemm07.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _abi.lib()
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GEMM07_API\s+[\w\s\*]*?\b(gemm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_symbols()
+    for must in ["gemm_f32", "gemm_bf16_f32acc", "gemm_status_string",
+                 "gemm_get_device_status", "gemm_f32_host", "gemm_bf16_f32acc_host"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in {n for n, _, _ in _abi.SIGNATURES}, f"no binding for {name}"
+        assert hasattr(_abi, name), f"no Python function named {name}"
+
+
+def test_library_is_in_tree_and_for_sm103a():
+    assert os.path.dirname(_build.LIB_PATH).startswith(os.path.dirname(g7.__file__))
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.NVCC_FLAGS)
+
+
+def test_abi_version(lib):
+    assert _abi.gemm_abi_version() == 1
+
+
+def test_status_strings(lib):
+    seen = set()
+    for code in range(7):
+        s = _abi.gemm_status_string(code)
+        assert s and s not in seen
+        seen.add(s)
+    assert _abi.gemm_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("tm,tn,group", [(32, 16, 8), (7, 5, 3), (1, 9, 8),
+                                         (24, 1, 8), (13, 17, 4), (32, 32, 1)])
+def test_tile_order_is_a_bijection_in_bands(tm, tn, group):
+    seen = set()
+    for lin in range(tm * tn):
+        s, m, n = _abi.gemm_tile_order(tm, tn, group, lin)
+        assert s == 0 and 0 <= m < tm and 0 <= n < tn
+        # index `lin` lies in band lin // (group*tn): rows [band*group, +group)
+        band = lin // (group * tn)
+        assert band * group <= m < min(tm, (band + 1) * group)
+        seen.add((m, n))
+    assert len(seen) == tm * tn
+
+
+def test_tile_order_runs_down_columns_first():
+    # inside a band, consecutive indices step down the rows of one column
+    coords = [_abi.gemm_tile_order(32, 16, 8, i)[1:] for i in range(16)]
+    assert coords[:8] == [(r, 0) for r in range(8)]
+    assert coords[8:16] == [(r, 1) for r in range(8)]
+
+
+def test_tile_order_rejects_bad_arguments():
+    assert _abi.gemm_tile_order(0, 4, 2, 0)[0] == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_tile_order(4, 4, 0, 0)[0] == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_tile_order(4, 4, 2, 16)[0] == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_tile_order(4, 4, 2, -1)[0] == _abi.GEMM_ERR_INVALID_ARG
+
+
+def _path(kind, *a, **k):
+    s, p = g7.plan(kind, *a, **k)
+    assert s == 0
+    return _abi.PATHS[p.path], p
+
+
+def test_plan_paths():
+    assert _path("bf16", 0, 5, 5)[0] == "none"
+    assert _path("bf16", 5, 0, 5)[0] == "none"
+    assert _path("bf16", 5, 5, 0)[0] == "zero_fill"
+    assert _path("f32", 5, 5, 0)[0] == "zero_fill"
+    path, p = _path("bf16", 4096, 4096, 4096)
+    assert path == "bf16_tma" and p.tiles == 32 * 16 and p.workspace_bytes == 0
+    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
+    path, p = _path("f32", 4096, 4096, 4096)
+    assert path == "f32_simt" and p.tiles == 32 * 32
+    # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
+    path, p = _path("bf16", 127, 1000, 3001)
+    assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
+    assert p.workspace_bytes >= 127 * 3008 * 2
+    # misaligned base address -> packed
+    path, p = _path("bf16", 256, 256, 256, A=16 + 2)
+    assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
+
+
+def test_plan_and_calls_reject_bad_arguments(lib):
+    bad = [(-1, 4, 4, 4, 4, 4), (4, 4, 8, 7, 4, 4), (4, 8, 4, 4, 7, 8),
+           (4, 8, 4, 4, 8, 7), (1 << 31, 4, 4, 4, 4, 4)]
+    for (M, N, K, lda, ldb, ldc) in bad:
+        for kind in ("bf16", "f32"):
+            s, _ = g7.plan(kind, M, N, K, lda=lda, ldb=ldb, ldc=ldc)
+            assert s == _abi.GEMM_ERR_INVALID_ARG, (kind, M, N, K, lda, ldb, ldc)
+        # the entry points check before touching any device
+        for fn in (_abi.gemm_f32, _abi.gemm_bf16_f32acc):
+            assert fn(M, N, K, 16, lda, 16, ldb, 16, ldc, None) == \
+                _abi.GEMM_ERR_INVALID_ARG
+    # null data pointer with a nonzero extent
+    assert _abi.gemm_f32(4, 4, 4, None, 4, 16, 4, 16, 4, None) == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_bf16_f32acc(4, 4, 4, 16, 4, 16, 4, None, 4, None) == \
+        _abi.GEMM_ERR_INVALID_ARG
+    # empty problems are fine without a GPU: nothing is launched
+    assert _abi.gemm_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == _abi.GEMM_OK
+
+
+def test_no_gpu_means_a_loud_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    buf = (ctypes.c_float * 16)()
+    addr = ctypes.addressof(buf)
+    s = _abi.gemm_f32(2, 2, 2, addr, 2, addr, 2, addr, 2, None)
+    assert s == _abi.GEMM_ERR_UNSUPPORTED_DEVICE
+    with pytest.raises(Exception):
+        g7.gemm_f32(torch.ones(2, 2), torch.ones(2, 2))

@@ -1,0 +1,220 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the oracle.
+
+Every case uses the seeded generators of dense_gemm_07_gb300.inputs and the
+bounds stated in tests/gemm_check.py.  Small and medium shapes are compared
+element by element; the full 4096-class shapes (the ones the benchmark times)
+are compared on sampled rows, which still cover every column tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import inputs
+from gemm_check import (assert_guards_intact, assert_within, guarded_output,
+                        oracle_ref)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _dtype(kind):
+    return torch.float32 if kind == "f32" else torch.bfloat16
+
+
+def _run(kind, a, b, out=None):
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
+    c = fn(a_d, b_d, out=out)
+    torch.cuda.synchronize()
+    return c
+
+
+def _check(kind, M, N, K, seed, dist, dist_b=None, exact=False, rows=None):
+    a, b = inputs.make_pair(M, N, K, seed, dist, dist_b, dtype=_dtype(kind))
+    c = _run(kind, a, b).cpu().numpy()
+    if rows is not None:
+        c = c[rows]
+    c_ref, s_ref = oracle_ref(kind, a, b, rows=rows, with_abs=not exact)
+    assert_within(kind, c, c_ref, s_ref, exact=exact, what=f"{kind} {M}x{N}x{K}")
+    assert g7.gemm_get_device_status() == 0
+
+
+def _sample_rows(M, count, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(M, size=min(count, M), replace=False).tolist())
+    rows.update({0, M - 1, min(127, M - 1), min(128, M - 1)})
+    return np.array(sorted(rows))
+
+
+# ------------------------------------------------------------ FP32 (SIMT)
+
+def test_f32_256_uniform():
+    _check("f32", 256, 256, 256, 0, inputs.UNIFORM)
+
+
+def test_f32_256_integers_exact():
+    _check("f32", 256, 256, 256, 0, inputs.INT4, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (1000, 700, 1024),
+                                   (1000, 700, 1000)])
+def test_f32_ragged_lab_shapes(shape):
+    M, N, K = shape
+    _check("f32", M, N, K, 7, inputs.INT4, exact=True)
+
+
+@pytest.mark.parametrize("K", [1, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127])
+def test_f32_small_and_ragged_k(K):
+    _check("f32", 130, 131, K, 11, inputs.UNIFORM)
+
+
+def test_f32_4096_sampled_rows():
+    M = N = K = 4096
+    _check("f32", M, N, K, 1, inputs.UNIFORM, rows=_sample_rows(M, 48, 1))
+
+
+# --------------------------------------------------- BF16 (tensor cores)
+
+def test_bf16_256_normal():
+    _check("bf16", 256, 256, 256, 2, inputs.NORMAL)
+
+
+def test_bf16_integers_exact_tiles():
+    # several 128 x 256 tiles, several 64-deep k slices and ragged tails
+    _check("bf16", 300, 600, 200, 4, inputs.INT3, exact=True)
+
+
+@pytest.mark.parametrize("K", [1, 8, 16, 63, 64, 65, 200])
+def test_bf16_small_and_ragged_k(K):
+    _check("bf16", 130, 260, K, 5, inputs.INT3, exact=True)
+
+
+def test_bf16_4096_sampled_rows():
+    M = N = K = 4096
+    _check("bf16", M, N, K, 2, inputs.NORMAL, rows=_sample_rows(M, 48, 2))
+
+
+@pytest.mark.parametrize("NK", [(4096, 4096), (11008, 4096), (4096, 11008)])
+def test_bf16_linear_layer_shapes_sampled(NK):
+    N, K = NK
+    _check("bf16", 2048, N, K, 3, inputs.NORMAL, inputs.NORMAL_W,
+           rows=_sample_rows(2048, 24, 3))
+
+
+@pytest.mark.parametrize("M", [127, 1000, 3001])
+@pytest.mark.parametrize("N", [127, 1000, 3001])
+@pytest.mark.parametrize("K", [127, 1000, 3001])
+def test_bf16_boundary_sweep_exact(M, N, K):
+    _check("bf16", M, N, K, 4, inputs.INT3, exact=True)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_bf16_skinny_exact(M):
+    _check("bf16", M, 4096, 4096, 4, inputs.INT3, exact=True)
+
+
+# ------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_zero_k_writes_zeros(kind):
+    buf, c = guarded_output(37, 45, 50, DEV)
+    a = torch.empty((37, 0), dtype=_dtype(kind), device=DEV)
+    b = torch.empty((0, 45), dtype=_dtype(kind), device=DEV)
+    (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a, b, out=c)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)
+    assert_guards_intact(buf, 37, 45, 50)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_empty_m_or_n_is_noop(kind):
+    buf, c = guarded_output(0, 5, 8, DEV)
+    a = torch.ones((0, 3), dtype=_dtype(kind), device=DEV)
+    b = torch.ones((3, 5), dtype=_dtype(kind), device=DEV)
+    (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a, b, out=c)
+    torch.cuda.synchronize()
+    assert_guards_intact(buf, 0, 5, 8)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(129, 257, 70), (300, 600, 200)])
+def test_guard_bands_untouched(kind, shape):
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 9, inputs.INT3, dtype=_dtype(kind))
+    ldc = N + 7
+    buf, c = guarded_output(M, N, ldc, DEV)
+    (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a.to(DEV), b.to(DEV), out=c)
+    torch.cuda.synchronize()
+    assert_guards_intact(buf, M, N, ldc)
+    c_ref, s_ref = oracle_ref(kind, a, b)
+    assert_within(kind, c.cpu().numpy(), c_ref, s_ref, exact=True)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_leading_dims_and_misaligned_bases(kind):
+    M, N, K = 150, 270, 90
+    a, b = inputs.make_pair(M, N, K, 12, inputs.INT3, dtype=_dtype(kind))
+    # operands placed at odd element offsets inside wider rows
+    a_buf = torch.zeros((M, K + 11), dtype=a.dtype, device=DEV)
+    b_buf = torch.zeros((K, N + 13), dtype=b.dtype, device=DEV)
+    a_buf[:, 1:K + 1] = a.to(DEV)
+    b_buf[:, 3:N + 3] = b.to(DEV)
+    a_v, b_v = a_buf[:, 1:K + 1], b_buf[:, 3:N + 3]
+    assert a_v.stride(0) == K + 11 and b_v.stride(0) == N + 13
+    c = (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a_v, b_v)
+    torch.cuda.synchronize()
+    c_ref, s_ref = oracle_ref(kind, a, b)
+    assert_within(kind, c.cpu().numpy(), c_ref, s_ref, exact=True)
+    if kind == "bf16":
+        s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
+                       b_v.data_ptr(), b_v.stride(0), c.data_ptr(), N)
+        assert g7.abi.PATHS[p.path] == "bf16_packed" and p.pack_a and p.pack_b
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_deterministic_bits(kind):
+    a, b = inputs.make_pair(512, 768, 1000, 13, inputs.NORMAL, dtype=_dtype(kind))
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
+    first = fn(a_d, b_d).clone()
+    for _ in range(10):
+        again = fn(a_d, b_d)
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_host_buffer_variant_matches_device(kind):
+    a, b = inputs.make_pair(333, 444, 555, 14, inputs.NORMAL, dtype=_dtype(kind))
+    dev_fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
+    host_fn = g7.gemm_f32_host if kind == "f32" else g7.gemm_bf16_f32acc_host
+    c_dev = dev_fn(a.to(DEV), b.to(DEV)).cpu()
+    c_host = host_fn(a.pin_memory(), b.pin_memory())
+    assert c_host.device.type == "cpu"
+    assert torch.equal(c_host.view(torch.int32), c_dev.view(torch.int32))
+
+
+def test_streams_are_respected():
+    a, b = inputs.make_pair(1024, 1024, 1024, 15, inputs.INT3, dtype=torch.bfloat16)
+    s = torch.cuda.Stream()
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        c = g7.gemm_bf16_f32acc(a_d, b_d)
+    s.synchronize()
+    c_ref, s_ref = oracle_ref("bf16", a, b)
+    assert_within("bf16", c.cpu().numpy(), c_ref, s_ref, exact=True)
+
+
+def test_invalid_arguments_rejected_before_launch():
+    a = torch.ones((4, 8), dtype=torch.bfloat16, device=DEV)
+    b = torch.ones((8, 4), dtype=torch.bfloat16, device=DEV)
+    c = torch.zeros((4, 4), dtype=torch.float32, device=DEV)
+    st = torch.cuda.current_stream().cuda_stream
+    assert g7.abi.gemm_bf16_f32acc(4, 4, 8, a.data_ptr(), 7, b.data_ptr(), 4,
+                                   c.data_ptr(), 4, st) == g7.abi.GEMM_ERR_INVALID_ARG
+    assert g7.abi.gemm_f32(-1, 4, 8, a.data_ptr(), 8, b.data_ptr(), 4,
+                           c.data_ptr(), 4, st) == g7.abi.GEMM_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)
