@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark of the dense-GEMM hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. gemm_bf16_f32acc at M = N = K = 4096 (A, B ~ N(0,1) rounded to BF16,
+     seed 2) -- the tensor-core path;
+  2. gemm_f32 at M = N = K = 4096 (A, B ~ U[-1,1) FP32, seed 1) -- the
+     CUDA-core path.
+Both run through the C ABI (libgemm07.so) on inputs already resident in HBM.
+L2 is flushed (a 256 MiB write) before each GEMM, outside the kernel's CUDA
+events.  Each GEMM is timed with CUDA events on the stream it is launched on;
+ms_per_step is the sum of the two kernels' event times, value = FLOPs of the
+step / ms_per_step.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (BF16→FP32 acc, FP32) at 4096³ and % of GB300 roofline"
+UNIT = "TFLOP/s"
+SIZE = 4096
+FLUSH_BYTES = 256 << 20
+GB300_SMS = 152
+# Fallback denominators if the measured-peaks file is absent.
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = d.get(os.path.basename(kernel_file))
+    src = os.path.join(ROOT, "dense_gemm_07_gb300", "csrc", os.path.basename(kernel_file))
+    if not entry or entry.get("source_sha256_16") != kernel_hash(src):
+        return None
+    return entry.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = None
+        self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.monotonic()
+
+    def mark_off(self):
+        self.t_off = time.monotonic()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        rows = [l for (t, l) in self.lines
+                if self.t_on is not None and self.t_on <= t <= (self.t_off or t)]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_sample_baseline(rows_each=1024):
+    """The oracle as it stands, on the first `rows_each` rows of each of the
+    step's two GEMMs (same seeded inputs), on this host's cores."""
+    import oracle
+    from dense_gemm_07_gb300 import inputs
+    import torch
+
+    oracle.build()
+    a16, b16 = inputs.make_pair(SIZE, SIZE, SIZE, 2, inputs.NORMAL, dtype=torch.bfloat16)
+    a32, b32 = inputs.make_pair(SIZE, SIZE, SIZE, 1, inputs.UNIFORM, dtype=torch.float32)
+    a16b, b16b = inputs.bf16_bits(a16[:rows_each].contiguous()), inputs.bf16_bits(b16)
+    a32n, b32n = a32[:rows_each].contiguous().numpy(), b32.numpy()
+    t0 = time.perf_counter()
+    oracle.gemm_bf16(a16b, b16b)
+    oracle.gemm_f32(a32n, b32n)
+    dt = time.perf_counter() - t0
+    flops = 2 * 2.0 * rows_each * SIZE * SIZE
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": (f"first {rows_each} of 4096 rows of both step GEMMs "
+                       f"(BF16 4096^3 and FP32 4096^3), FP64 triple loop, "
+                       f"OpenMP over rows")}
+
+
+# ------------------------------------------------------------- reference
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from dense_gemm_07_gb300 import inputs
+    import torch
+
+    oracle.build()
+    rows = 16
+    a16, b16 = inputs.make_pair(SIZE, SIZE, SIZE, 2, inputs.NORMAL, dtype=torch.bfloat16)
+    a32, b32 = inputs.make_pair(SIZE, SIZE, SIZE, 1, inputs.UNIFORM, dtype=torch.float32)
+    b16b, b32n = inputs.bf16_bits(b16), b32.numpy()
+
+    def step(i):
+        r0 = (i * rows) % SIZE
+        oracle.gemm_bf16(inputs.bf16_bits(a16[r0:r0 + rows].contiguous()), b16b)
+        oracle.gemm_f32(a32[r0:r0 + rows].contiguous().numpy(), b32n)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    flops = args.steps * 2 * 2.0 * rows * SIZE * SIZE
+    value = flops / dt / 1e12
+    cores = oracle.max_threads()
+    sample = (f"{rows} rows of 4096 per GEMM per step, both step GEMMs "
+              f"(BF16 4096^3, FP32 4096^3), FP64 oracle on {cores} host threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gemm 4096^3 bf16->f32acc + gemm 4096^3 f32, "
+                   "oracle sample", "rows_per_gemm_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import dense_gemm_07_gb300 as g7
+    from dense_gemm_07_gb300 import inputs, roofline
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g7.build()
+
+    peaks, peaks_src = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    a16, b16 = inputs.make_pair(SIZE, SIZE, SIZE, 2, inputs.NORMAL, dtype=torch.bfloat16)
+    a32, b32 = inputs.make_pair(SIZE, SIZE, SIZE, 1, inputs.UNIFORM, dtype=torch.float32)
+    A16, B16 = a16.to(dev), b16.to(dev)
+    A32, B32 = a32.to(dev), b32.to(dev)
+    C16 = torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev)
+    C32 = torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # launches per call of each entry point (1 unless operands are packed)
+    launches = 0
+    for kind, A, B, C in (("bf16", A16, B16, C16), ("f32", A32, B32, C32)):
+        s, p = g7.plan(kind, SIZE, SIZE, SIZE, A.data_ptr(), SIZE, B.data_ptr(), SIZE,
+                       C.data_ptr(), SIZE)
+        launches += 1 + p.pack_a + p.pack_b
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        flush.fill_(1.0)
+        if ev:
+            ev[0].record(stream)
+        g7.gemm_bf16_f32acc(A16, B16, out=C16)
+        if ev:
+            ev[1].record(stream)
+        flush.fill_(2.0)
+        if ev:
+            ev[2].record(stream)
+        g7.gemm_f32(A32, B32, out=C32)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if g7.gemm_get_device_status() != 0:
+        raise SystemExit("device status error after warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+              for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_on()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    sampler.mark_off()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = g7.gemm_get_device_status()
+
+    t_bf16 = [e[0].elapsed_time(e[1]) for e in events]   # ms
+    t_f32 = [e[2].elapsed_time(e[3]) for e in events]
+    ms_bf16 = sum(t_bf16) / len(t_bf16)
+    ms_f32 = sum(t_f32) / len(t_f32)
+    ms_step = ms_bf16 + ms_f32
+    if world > 1:
+        t = torch.tensor([ms_step, ms_bf16, ms_f32], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_bf16, ms_f32 = (float(x) for x in t.tolist())
+
+    flops_one = roofline.gemm_flops(SIZE, SIZE, SIZE)
+    value = world * 2 * flops_one / (ms_step * 1e-3) / 1e12
+    tf_bf16 = flops_one / (ms_bf16 * 1e-3) / 1e12
+    tf_f32 = flops_one / (ms_f32 * 1e-3) / 1e12
+
+    # Roofline denominators.
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    fp32_peak = roofline.fp32_simt_peak(sms, sm_max) / 1e12
+    bf16_roof = min(bf16_peak, roofline.intensity(SIZE, SIZE, SIZE, 2, 4) * hbm / 1e3)
+    fp32_roof = min(fp32_peak, roofline.intensity(SIZE, SIZE, SIZE, 4, 4) * hbm / 1e3)
+    csrc = os.path.join(ROOT, "dense_gemm_07_gb300", "csrc")
+    rl_bf16 = {"bound": "tensor", "achieved": tf_bf16, "peak": bf16_roof, "unit": "TFLOP/s",
+               "frac": tf_bf16 / bf16_roof,
+               "traffic": ncu_traffic(os.path.join(csrc, "gemm_bf16_tc.cu")),
+               "peak_source": f"{peaks_src} bf16 burst (cuBLAS 8192^3)"}
+    rl_f32 = {"bound": "alu", "achieved": tf_f32, "peak": fp32_roof, "unit": "TFLOP/s",
+              "frac": tf_f32 / fp32_roof,
+              "traffic": ncu_traffic(os.path.join(csrc, "gemm_f32.cu")),
+              "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz"}
+    dominant = rl_f32 if ms_f32 >= ms_bf16 else rl_bf16
+
+    # End to end through the host-buffer C-ABI entry points.
+    e2e = None
+    if args.e2e_steps > 0:
+        h_a16, h_b16 = a16.pin_memory(), b16.pin_memory()
+        h_a32, h_b32 = a32.pin_memory(), b32.pin_memory()
+        h_c16 = torch.empty((SIZE, SIZE), dtype=torch.float32).pin_memory()
+        h_c32 = torch.empty((SIZE, SIZE), dtype=torch.float32).pin_memory()
+        g7.gemm_bf16_f32acc_host(h_a16, h_b16, out=h_c16)
+        g7.gemm_f32_host(h_a32, h_b32, out=h_c32)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            g7.gemm_bf16_f32acc_host(h_a16, h_b16, out=h_c16)
+            g7.gemm_f32_host(h_a32, h_b32, out=h_c32)
+        torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        h2d = (h_a16.numel() + h_b16.numel()) * 2 + (h_a32.numel() + h_b32.numel()) * 4
+        d2h = (h_c16.numel() + h_c32.numel()) * 4
+        e2e = {"value": world * 2 * flops_one / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3,
+               "api": "gemm_bf16_f32acc_host + gemm_f32_host (C ABI, pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_sample_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16+f32", "data": "synthetic",
+            "config": {"workload": "gemm 4096^3 bf16->f32acc (N(0,1), seed 2) + "
+                                   "gemm 4096^3 f32 (U[-1,1), seed 1)",
+                       "M": SIZE, "N": SIZE, "K": SIZE,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
+                       "l2": "flushed before each GEMM by a 256 MiB write outside "
+                             "the kernel events"},
+            "paths": {
+                "bf16_f32acc": {"ms": ms_bf16, "tflops": tf_bf16, "roofline": rl_bf16},
+                "f32": {"ms": ms_f32, "tflops": tf_f32, "roofline": rl_f32},
+            },
+            "roofline": dominant,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "wall_ms_per_step": wall / args.steps * 1e3,
+            "clocks": clocks,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

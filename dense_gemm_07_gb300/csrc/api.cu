@@ -106,11 +106,14 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->pack_a = (aligned16(A) && lda % 8 == 0) ? 0 : 1;
   p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
   p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
-  p->tile_m = kTcTileM;
-  p->tile_n = kTcTileN;
+  // More than one 128-row tile: 256 x 256 tiles on SM pairs; otherwise one
+  // SM per 128 x 256 tile.
+  const bool pair = M > kTcTileM;
+  p->tile_m = pair ? kPairTileM : kTcTileM;
+  p->tile_n = pair ? kPairTileN : kTcTileN;
   p->tile_k = kTcTileK;
-  p->stages = kTcStages;
-  p->tiles = ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
+  p->stages = pair ? kPairStages : kTcStages;
+  p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
   int64_t ws = 0;
   if (p->pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
@@ -291,10 +294,19 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK, kTcTileM);
   if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
   if (s == GEMM_OK) {
-    const int grid = static_cast<int>(plan.tiles < d->sms ? plan.tiles : d->sms);
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
-    s = from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
-                                      d->status, stream));
+    const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
+    if (max_pairs > 0) {
+      const int pairs = static_cast<int>(plan.tiles < max_pairs ? plan.tiles : max_pairs);
+      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c, pairs,
+                                          d->status, stream));
+    } else {
+      const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
+                            ((N + kTcTileN - 1) / kTcTileN);
+      const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
+      s = from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
+                                        d->status, stream));
+    }
   }
   pool_free(ws, stream);
   return s;

@@ -1,0 +1,355 @@
+// gemm_bf16_tc2.cu -- BF16 x BF16 -> FP32 GEMM on pairs of SMs.
+//
+// Same method as gemm_bf16_tc.cu (the tensor-core rung of "GEMM, step by
+// step", section "Concept": BF16 inputs, FP32 sums, large tiles, neighbouring
+// blocks on the same rows/columns; multi-stage prefetch as in "GEMM
+// Optimization", section 5), with the output tile grown to 256 x 256 and
+// computed by two SMs together ("Production tensor-core kernels use larger
+// tiles", same section of "GEMM, step by step").
+//
+// sm_103a realisation: clusters of two CTAs, one per SM.  CTA r of the pair
+// owns rows [128r, 128r+128) of the 256-row tile and stages only those rows
+// of A (128 x 64 per k-slice) plus columns [128r, 128r+128) of B (64 x 128);
+// one tcgen05.mma.cta_group::2 (M=256, N=256, K=16), issued by the even CTA,
+// reads A and B from both CTAs' shared memory and writes each CTA's 128 rows
+// of D into that CTA's tensor memory.  Per SM this halves the bytes that
+// have to be copied into shared memory per FLOP compared with one SM
+// computing a 128 x 256 tile, which is what lets six 32 KB stages keep the
+// tensor core busy.
+//
+// Roles (192 threads per CTA):
+//   warp 0 (both CTAs)  TMA producer.  Both CTAs' copies count their bytes on
+//                       the even CTA's "full" barrier; the even CTA arms it
+//                       for 64 KB per stage.
+//   warp 1 (even CTA)   MMA issuer: waits on "full", issues 4 pair MMAs per
+//                       stage, commits to "empty" in both CTAs, and after the
+//                       last slice of a tile to "accumulator full" in both.
+//   warps 2-5 (both)    epilogue: TMEM -> registers -> C (guarded 16-byte
+//                       stores), then arrive on the even CTA's
+//                       "accumulator empty" (8 arrivals per tile).
+// Tensor memory: NUM_ACC 256-column FP32 accumulators per CTA; with two, a
+// tile's epilogue overlaps the next tile's MMAs.  Every wait is bounded; on expiry
+// the CTA raises its own and its peer's abort flag and the status word, all
+// roles unwind, copies and MMAs in flight are drained, and both CTAs meet at
+// a final cluster barrier before tensor memory is released.
+#include <cstdint>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+#include "tile_order.cuh"
+
+namespace g07 {
+namespace {
+
+constexpr int PAIR_M = 256;                       // rows per pair tile
+constexpr int CTA_M = 128;                        // rows per CTA
+constexpr int BN = 256;                           // columns per pair tile
+constexpr int CTA_N = 128;                        // B columns staged per CTA
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_STAGE_BYTES = CTA_M * BK * 2;     // 16 KB
+constexpr int B_BOX_COLS = 64;
+constexpr int B_BOX_BYTES = BK * B_BOX_COLS * 2;  // 8 KB
+constexpr int B_STAGE_BYTES = BK * CTA_N * 2;     // 16 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MMA_K = 16;
+constexpr int NUM_ACC = 2;                        // accumulators in TMEM
+constexpr int TMEM_COLS = NUM_ACC * BN;
+constexpr int THREADS = 192;
+constexpr int GROUP = 8;
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn_major=*/false,
+                                          /*b_mn_major=*/true);
+
+struct alignas(8) PairControl {
+  uint64_t full[STAGES];      // used in the even CTA only
+  uint64_t empty[STAGES];
+  uint64_t acc_full[NUM_ACC];
+  uint64_t acc_empty[NUM_ACC];  // used in the even CTA only (8 arrivals)
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort) {
+  return mbar_wait(bar, parity, abort);
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort,
+                                            uint32_t peer_abort_addr,
+                                            unsigned int* status) {
+  *abort = 1;
+  st_cluster_u32(peer_abort_addr, 1u);
+  atomicOr(status, 1u);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      float* __restrict__ C, int64_t ldc, int M, int N, int K,
+                      int tiles_m, int tiles_n, int vec_c,
+                      unsigned int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  PairControl* ctl = reinterpret_cast<PairControl*>(smem + STAGES * STAGE_BYTES);
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int num_tiles = tiles_m * tiles_n;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(&ctl->acc_full[a], 1);
+      mbar_init(&ctl->acc_empty[a], 8);  // 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&ctl->tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anyone signals them
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const uint32_t peer_abort = map_to_rank(smem_u32(&ctl->abort), rank ^ 1u);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
+        const int a_row = tc.m * PAIR_M + static_cast<int>(rank) * CTA_M;
+        const int b_col = tc.n * BN + static_cast<int>(rank) * CTA_N;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!pair_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          if (even) {
+            mbar_arrive_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
+            last_phase[stage] = static_cast<int>(phase);
+          }
+          const uint32_t full0 = map_to_rank(smem_u32(&ctl->full[stage]), 0);
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          tma_load_2d_pair(sa, &tmA, full0, kb * BK, a_row);
+#pragma unroll
+          for (int j = 0; j < CTA_N / B_BOX_COLS; ++j)
+            tma_load_2d_pair(sb + j * B_BOX_BYTES, &tmB, full0,
+                             b_col + j * B_BOX_COLS, kb * BK);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, peer_abort, status);
+      // The even CTA's "full" barriers count both CTAs' copies: every phase
+      // it armed must complete before the pair may exit.
+      volatile int never = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (last_phase[s] >= 0 &&
+            !mbar_wait(&ctl->full[s], static_cast<uint32_t>(last_phase[s]),
+                       &never))
+          raise_abort(abort, peer_abort, status);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (even && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool issued = false;
+      int t = 0;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs, ++t) {
+        const int acc = t % NUM_ACC;
+        const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
+        if (!pair_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!pair_wait(&ctl->full[stage], phase, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / MMA_K; ++kk) {
+            const uint64_t adesc =
+                sdesc_sw128(a_addr + kk * MMA_K * 2, 16, 1024);
+            const uint64_t bdesc =
+                sdesc_sw128(b_addr + kk * MMA_K * 128, B_BOX_BYTES, 1024);
+            mma_f16_ss_pair(d_tmem, adesc, bdesc, IDESC,
+                            (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(&ctl->empty[stage], 0x3);
+          issued = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&ctl->acc_full[acc], 0x3);
+      }
+      if (!ok) raise_abort(abort, peer_abort, status);
+      if (issued) {
+        mma_commit_pair(&ctl->drain, 0x1);
+        volatile int never = 0;
+        if (!mbar_wait(&ctl->drain, 0u, &never))
+          raise_abort(abort, peer_abort, status);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int t = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++t) {
+      const int acc = t % NUM_ACC;
+      const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) raise_abort(abort, peer_abort, status);
+        break;
+      }
+      tc_fence_after_sync();
+      const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
+      const int row = tc.m * PAIR_M + static_cast<int>(rank) * CTA_M + q * 32 + lane;
+      float* crow = C + static_cast<int64_t>(row) * ldc;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int gn = tc.n * BN + c * 32;
+        if (row < M) {
+          if (vec_c && gn + 31 < N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(crow + gn + j) =
+                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                              __uint_as_float(r[j + 2]),
+                              __uint_as_float(r[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) crow[gn + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_cluster(map_to_rank(smem_u32(&ctl->acc_empty[acc]), 0));
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+struct LaunchInfo {
+  int ready = 0;
+  int max_pairs = 0;
+};
+LaunchInfo g_info[64];
+
+}  // namespace
+
+size_t pair_smem_bytes() {
+  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(PairControl);
+}
+
+int pair_max_active(cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  LaunchInfo& li = g_info[dev];
+  if (!li.ready) {
+    const size_t smem = pair_smem_bytes();
+    if (cudaFuncSetAttribute(gemm_bf16_pair_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_pair_kernel, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    li.max_pairs = clusters;
+    li.ready = 1;
+  }
+  return li.max_pairs;
+}
+
+cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  float* C, int64_t ldc, int M, int N, int K,
+                                  bool vec_c, int pairs, unsigned int* status,
+                                  cudaStream_t stream) {
+  const int tiles_m = (M + PAIR_M - 1) / PAIR_M;
+  const int tiles_n = (N + BN - 1) / BN;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes();
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel, tmA, tmB, C, ldc, M, N,
+                            K, tiles_m, tiles_n, vec_c ? 1 : 0, status);
+}
+
+}  // namespace g07

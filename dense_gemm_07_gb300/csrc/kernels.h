@@ -35,6 +35,20 @@ cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 bool vec_c, int grid, unsigned int* status,
                                 cudaStream_t stream);
 
+// ---- BF16 tensor-core path on SM pairs (gemm_bf16_tc2.cu): 256 x 256 tiles
+constexpr int kPairTileM = 256;
+constexpr int kPairTileN = 256;
+constexpr int kPairStages = 6;
+
+size_t pair_smem_bytes();
+// Clusters of two CTAs that can be resident at once (0 if the pair kernel
+// cannot run on this device).
+int pair_max_active(cudaStream_t stream);
+cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  float* C, int64_t ldc, int M, int N, int K,
+                                  bool vec_c, int pairs, unsigned int* status,
+                                  cudaStream_t stream);
+
 // ---- small helpers (gemm_aux.cu)
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
                                  cudaStream_t stream);

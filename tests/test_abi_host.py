@@ -96,8 +96,11 @@ def test_plan_paths():
     assert _path("bf16", 5, 5, 0)[0] == "zero_fill"
     assert _path("f32", 5, 5, 0)[0] == "zero_fill"
     path, p = _path("bf16", 4096, 4096, 4096)
-    assert path == "bf16_tma" and p.tiles == 32 * 16 and p.workspace_bytes == 0
-    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
+    assert path == "bf16_tma" and p.tiles == 16 * 16 and p.workspace_bytes == 0
+    assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
+    path, p = _path("bf16", 128, 4096, 4096)
+    assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (128, 256, 4)
+    assert p.tiles == 16
     path, p = _path("f32", 4096, 4096, 4096)
     assert path == "f32_simt" and p.tiles == 32 * 32
     # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
