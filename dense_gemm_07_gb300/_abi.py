@@ -22,6 +22,8 @@ GEMM_ERR_LAUNCH = 3
 GEMM_ERR_TIMEOUT = 4
 GEMM_ERR_NO_MEMORY = 5
 GEMM_ERR_INTERNAL = 6
+GEMM_ERR_SCRATCH_TOO_SMALL = 7
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 PATHS = {0: "none", 1: "zero_fill", 2: "f32_simt", 3: "bf16_tma",
          4: "bf16_packed", 5: "bf16_skinny"}
@@ -41,6 +43,7 @@ _GEMM_ARGS = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
 SIGNATURES = [
     ("gemm_f32", _i32, _GEMM_ARGS),
     ("gemm_bf16_f32acc", _i32, _GEMM_ARGS),
+    ("gemm_bf16_f32acc_noalloc", _i32, _GEMM_ARGS),
     ("gemm_f32_host", _i32, _GEMM_ARGS),
     ("gemm_bf16_f32acc_host", _i32, _GEMM_ARGS),
     ("gemm_status_string", ctypes.c_char_p, [_i32]),
@@ -88,6 +91,11 @@ def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream):
 
 def gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream):
     return lib().gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream):
+    """gemm_bf16_f32acc without any device allocation (fixed scratch)."""
+    return lib().gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, stream):

@@ -347,6 +347,117 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   return s;
 }
 
+// ----------------------------------------------------------------------
+// No-allocation variant of the BF16 entry point.  Its operand copies go into
+// a fixed array in device memory instead of the memory pool.
+
+constexpr int64_t kNoallocScratchBytes =
+    static_cast<int64_t>(GEMM07_NOALLOC_SCRATCH_BYTES);
+static __device__ __align__(256) uint8_t g_noalloc_scratch[GEMM07_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocState {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned int* status = nullptr;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch
+};
+NoallocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: capability check and the device
+// addresses of the status word and of the scratch array.  Allocates nothing.
+gemm_status_t noalloc_device(NoallocState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  NoallocState& d = g_noalloc[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* status = nullptr;
+      void* scratch = nullptr;
+      if (cudaGetSymbolAddress(&status, g_status_word) != cudaSuccess ||
+          cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      d.status = static_cast<unsigned int*>(status);
+      d.scratch = static_cast<uint8_t*>(scratch);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return GEMM_OK;
+}
+
+gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
+                               const uint16_t* A, int64_t lda,
+                               const uint16_t* B, int64_t ldb, float* C,
+                               int64_t ldc, cudaStream_t stream) {
+  gemm_plan_t plan;
+  gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan);
+  if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
+  if (plan.workspace_bytes > kNoallocScratchBytes)
+    return GEMM_ERR_SCRATCH_TOO_SMALL;
+  NoallocState* d = nullptr;
+  s = noalloc_device(&d);
+  if (s != GEMM_OK) return s;
+  if (plan.path == GEMM_PATH_ZERO_FILL)
+    return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
+                                          static_cast<int>(N), stream));
+  const int m = static_cast<int>(M), n = static_cast<int>(N),
+            k = static_cast<int>(K);
+  // Same layout as the pooled path: packed A first, then packed B, each
+  // starting on a 256-byte boundary.  Only the copied extent is ever read.
+  const uint16_t* a_op = A;
+  const uint16_t* b_op = B;
+  int64_t lda_op = lda, ldb_op = ldb;
+  uint8_t* cursor = d->scratch;
+  if (plan.pack_a) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    lda_op = round_up(K, 8);
+    cursor += round_up(M * lda_op * 2, 256);
+    s = from_cuda(launch_copy_rows_u16(A, lda, dst, lda_op, m, k, stream));
+    a_op = dst;
+  }
+  if (s == GEMM_OK && plan.pack_b) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    ldb_op = round_up(N, 8);
+    s = from_cuda(launch_copy_rows_u16(B, ldb, dst, ldb_op, k, n, stream));
+    b_op = dst;
+  }
+  CUtensorMap tmA, tmB;
+  if (s == GEMM_OK) s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK, kTcTileM);
+  if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
+  if (s != GEMM_OK) return s;
+  const bool vec_c = aligned16(C) && ldc % 4 == 0;
+  const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
+  if (max_pairs > 0) {
+    const int pairs = static_cast<int>(plan.tiles < max_pairs ? plan.tiles : max_pairs);
+    return from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c,
+                                           pairs, d->status, stream));
+  }
+  const int64_t tiles =
+      ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
+  const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
+  return from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
+                                       d->status, stream));
+}
+
 }  // namespace
 }  // namespace g07
 
@@ -367,6 +478,14 @@ gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
                                int64_t ldc, void* stream) {
   return run_bf16(M, N, K, A, lda, B, ldb, C, ldc,
                   static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K,
+                                        const uint16_t* A, int64_t lda,
+                                        const uint16_t* B, int64_t ldb,
+                                        float* C, int64_t ldc, void* stream) {
+  return run_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc,
+                          static_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
@@ -393,6 +512,7 @@ const char* gemm_status_string(gemm_status_t status) {
     case GEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out; the output is incomplete";
     case GEMM_ERR_NO_MEMORY: return "device workspace allocation failed";
     case GEMM_ERR_INTERNAL: return "internal error (tensor map encoding)";
+    case GEMM_ERR_SCRATCH_TOO_SMALL: return "the operand copies need more than the fixed no-allocation scratch";
   }
   return "unknown status";
 }

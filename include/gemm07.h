@@ -58,7 +58,8 @@ typedef enum gemm_status {
     GEMM_ERR_LAUNCH = 3,             /* a CUDA call or kernel launch failed */
     GEMM_ERR_TIMEOUT = 4,            /* a device-side bounded wait ran out */
     GEMM_ERR_NO_MEMORY = 5,          /* workspace or staging allocation failed */
-    GEMM_ERR_INTERNAL = 6
+    GEMM_ERR_INTERNAL = 6,
+    GEMM_ERR_SCRATCH_TOO_SMALL = 7   /* gemm_bf16_f32acc_noalloc: request exceeds its fixed scratch */
 } gemm_status_t;
 
 /*
@@ -101,6 +102,35 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
                                const uint16_t *A, int64_t lda,
                                const uint16_t *B, int64_t ldb,
                                float *C, int64_t ldc, void *stream);
+
+/*
+ * gemm_bf16_f32acc_noalloc -- the same operation, arguments and results as
+ * gemm_bf16_f32acc, for callers that must not allocate device memory.
+ *   The pages describe no such entry point; it has no counterpart there.
+ *   Who needs it: code that runs inside a host application which owns every
+ *   byte of device memory through its own allocator and forbids plug-ins
+ *   from calling cudaMalloc, and latency-critical loops where an allocation
+ *   could synchronise the device or wait on the allocator.  This call never
+ *   calls cudaMalloc, cudaFree, a pool or any other allocating routine.
+ *   Scratch: when A or B has to be copied to an aligned layout first (base
+ *   not 16-byte aligned, or lda/ldb not a multiple of 8), the copies go into
+ *   one fixed array of GEMM07_NOALLOC_SCRATCH_BYTES that the library
+ *   declares in device memory; every device that loads the library holds it
+ *   until the process exits.  A request whose copies need more than that
+ *   returns GEMM_ERR_SCRATCH_TOO_SMALL before anything is enqueued (aligned
+ *   operands need no scratch and have no such limit).
+ *   Sharing: every call on a device uses the same array and it keeps the
+ *   last call's contents.  Calls whose kernels may overlap on the GPU (on
+ *   different streams without ordering between them) race on it: order them
+ *   on one stream or with events.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (with that device current); later calls reuse it.
+ */
+#define GEMM07_NOALLOC_SCRATCH_BYTES (64ull << 20)
+GEMM07_API gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K,
+                                        const uint16_t *A, int64_t lda,
+                                        const uint16_t *B, int64_t ldb,
+                                        float *C, int64_t ldc, void *stream);
 
 /*
  * Host-buffer variants: the same operations with A, B and C in HOST memory

@@ -49,7 +49,7 @@ def test_abi_version(lib):
 
 def test_status_strings(lib):
     seen = set()
-    for code in range(7):
+    for code in range(8):
         s = _abi.gemm_status_string(code)
         assert s and s not in seen
         seen.add(s)

@@ -1,0 +1,90 @@
+"""gemm_bf16_f32acc_noalloc: the BF16 GEMM for callers that may not allocate
+device memory.
+
+Some callers cannot call cudaMalloc: a plug-in running inside a host
+application that owns all device memory through its own allocator and
+forbids others from allocating, or a latency-critical loop in which an
+allocation could synchronise the device.  For them the library offers one
+entry point whose operand copies go into a fixed scratch array declared in
+device memory instead of a memory pool.
+
+These tests call it through the C ABI and compare it with the ordinary
+(pool-using) entry point on shapes that need the copies, twice in a row, so
+that the second call runs on scratch left over from the first.  The file is
+named so that pytest collects it last.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import _abi, inputs
+from gemm_check import assert_within, oracle_ref
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _noalloc(a, b, out):
+    """Call the no-allocation entry point on (possibly strided) CUDA tensors."""
+    M, K = a.shape
+    N = b.shape[1]
+    st = torch.cuda.current_stream().cuda_stream
+    return _abi.gemm_bf16_f32acc_noalloc(M, N, K, a.data_ptr(), a.stride(0),
+                                         b.data_ptr(), b.stride(0),
+                                         out.data_ptr(), out.stride(0), st)
+
+
+def _misaligned(t, extra_cols, offset):
+    """Copy of t placed `offset` elements into rows `extra_cols` wider."""
+    rows, cols = t.shape
+    buf = torch.zeros((rows, cols + extra_cols), dtype=t.dtype, device=DEV)
+    buf[:, offset:offset + cols] = t.to(DEV)
+    return buf[:, offset:offset + cols]
+
+
+# (M, N, K, seed, distribution, exact): K = 333 makes A's rows a
+# non-multiple of 16 bytes; the second case offsets both operands by odd
+# element counts, so both copies land in the scratch array.
+CASES = [(300, 520, 333, 21, inputs.INT3, True),
+         (257, 300, 200, 22, inputs.NORMAL, False)]
+
+
+def test_noalloc_matches_pooled_entry_point_two_calls_in_a_row():
+    for (M, N, K, seed, dist, exact) in CASES:
+        a, b = inputs.make_pair(M, N, K, seed, dist, dtype=torch.bfloat16)
+        if exact:
+            a_d, b_d = a.to(DEV), b.to(DEV)
+        else:
+            a_d, b_d = _misaligned(a, 9, 3), _misaligned(b, 11, 1)
+        s, plan = g7.plan("bf16", M, N, K, a_d.data_ptr(), a_d.stride(0),
+                          b_d.data_ptr(), b_d.stride(0), 16, N)
+        assert s == 0 and plan.pack_a == 1, "case must exercise the scratch copies"
+        ref = g7.gemm_bf16_f32acc(a_d, b_d)
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
+        torch.cuda.synchronize()
+        assert g7.gemm_get_device_status() == 0
+        got, want = out.cpu().numpy(), ref.cpu().numpy()
+        if exact:
+            assert np.array_equal(got, want)
+        else:
+            _, s_ref = oracle_ref("bf16", a, b)
+            # same bound as the parity tests, measured against the pooled
+            # entry point's output
+            assert_within("bf16", got, want.astype(np.float64), s_ref,
+                          what="noalloc vs pooled entry point")
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    # A needs a copy (lda odd); 4096 rows of 8200 BF16 exceed the 64 MiB scratch
+    M, K, N = 4096, 8199, 64
+    a = torch.zeros((M, K), dtype=torch.bfloat16, device=DEV)
+    b = torch.zeros((K, N), dtype=torch.bfloat16, device=DEV)
+    c = torch.full((M, N), 7.0, dtype=torch.float32, device=DEV)
+    s, plan = g7.plan("bf16", M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N)
+    assert plan.workspace_bytes > _abi.NOALLOC_SCRATCH_BYTES
+    assert _noalloc(a, b, c) == _abi.GEMM_ERR_SCRATCH_TOO_SMALL
+    torch.cuda.synchronize()
+    assert torch.all(c == 7.0)   # nothing was enqueued
