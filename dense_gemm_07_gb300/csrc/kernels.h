@@ -13,6 +13,7 @@ constexpr int kF32TileM = 128;
 constexpr int kF32TileN = 128;
 constexpr int kF32TileK = 16;
 constexpr int kF32Group = 8;
+constexpr int kF32Stages = 3;
 
 cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             const float* B, int64_t ldb, float* C, int64_t ldc,

@@ -70,6 +70,15 @@ def test_f32_small_and_ragged_k(K):
     _check("f32", 130, 131, K, 11, inputs.UNIFORM)
 
 
+@pytest.mark.parametrize("shape", [(2560, 2048, 136), (2432, 2055, 77),
+                                   (4096, 1024, 40)])
+def test_f32_full_and_split_waves_exact(shape):
+    # more tiles than resident blocks: whole waves of 128 x 128 tiles plus a
+    # last wave of half-width tiles, with ragged N and K in the second case
+    M, N, K = shape
+    _check("f32", M, N, K, 16, inputs.INT4, exact=True)
+
+
 def test_f32_4096_sampled_rows():
     M = N = K = 4096
     _check("f32", M, N, K, 1, inputs.UNIFORM, rows=_sample_rows(M, 48, 1))
