@@ -297,9 +297,8 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
     const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
     if (max_pairs > 0) {
-      const int pairs = static_cast<int>(plan.tiles < max_pairs ? plan.tiles : max_pairs);
-      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c, pairs,
-                                          d->status, stream));
+      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c,
+                                          max_pairs, d->status, stream));
     } else {
       const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
                             ((N + kTcTileN - 1) / kTcTileN);
@@ -447,9 +446,8 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (max_pairs > 0) {
-    const int pairs = static_cast<int>(plan.tiles < max_pairs ? plan.tiles : max_pairs);
     return from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c,
-                                           pairs, d->status, stream));
+                                           max_pairs, d->status, stream));
   }
   const int64_t tiles =
       ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);

@@ -7,6 +7,11 @@
 // computed by two SMs together ("Production tensor-core kernels use larger
 // tiles", same section of "GEMM, step by step").
 //
+// Wave tail: when the tiles left for the last wave fill at most half of the
+// resident pairs, each of them is computed as two 256 x 128 units (an N=128
+// pair MMA, one 64-column box of B per CTA), so that wave takes half as long.
+// Every output element is still one tile's k-sum in one accumulator.
+//
 // sm_103a realisation: clusters of two CTAs, one per SM.  CTA r of the pair
 // owns rows [128r, 128r+128) of the 256-row tile and stages only those rows
 // of A (128 x 64 per k-slice) plus columns [128r, 128r+128) of B (64 x 128);
@@ -57,8 +62,6 @@ constexpr int NUM_ACC = 2;                        // accumulators in TMEM
 constexpr int TMEM_COLS = NUM_ACC * BN;
 constexpr int THREADS = 192;
 constexpr int GROUP = 8;
-constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn_major=*/false,
-                                          /*b_mn_major=*/true);
 
 struct alignas(8) PairControl {
   uint64_t full[STAGES];      // used in the even CTA only
@@ -69,6 +72,29 @@ struct alignas(8) PairControl {
   uint32_t tmem_base;
   int abort;
 };
+
+// One unit of work: a 256-row tile of C, columns [n0, n0 + width).
+struct Unit {
+  int m0;
+  int n0;
+  int width;
+};
+
+__device__ __forceinline__ Unit unit_of(int unit, int num_full, int split,
+                                        int tiles_m, int tiles_n) {
+  int tile = unit, piece = 0, width = BN;
+  if (unit >= num_full) {
+    tile = num_full + (unit - num_full) / split;
+    piece = (unit - num_full) % split;
+    width = BN / split;
+  }
+  const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
+  Unit u;
+  u.m0 = tc.m * PAIR_M;
+  u.n0 = tc.n * BN + piece * width;
+  u.width = width;
+  return u;
+}
 
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort) {
@@ -83,12 +109,115 @@ __device__ __forceinline__ void raise_abort(volatile int* abort,
   atomicOr(status, 1u);
 }
 
+// Position in the shared-memory ring (stage, and the parity of its uses).
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance() {
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Producer for one unit of width W: per k-slice, wait for the stage to be
+// free, arm the even CTA's "full" barrier (even CTA only), copy this CTA's
+// 128 rows of A and W/2 columns of B.
+template <int W>
+__device__ __forceinline__ bool produce_unit(const Unit& u, Ring& ring,
+                                             int num_kb, uint8_t* smem,
+                                             PairControl* ctl,
+                                             const CUtensorMap* tmA,
+                                             const CUtensorMap* tmB,
+                                             uint32_t rank, int* last_phase,
+                                             volatile int* abort) {
+  constexpr int BOXES = W / 2 / B_BOX_COLS;
+  constexpr uint32_t TX = 2u * (A_STAGE_BYTES + BOXES * B_BOX_BYTES);
+  const int a_row = u.m0 + static_cast<int>(rank) * CTA_M;
+  const int b_col = u.n0 + static_cast<int>(rank) * (W / 2);
+  for (int kb = 0; kb < num_kb; ++kb) {
+    if (!mbar_wait(&ctl->empty[ring.stage], ring.phase ^ 1u, abort)) return false;
+    if (rank == 0) {
+      mbar_arrive_expect_tx(&ctl->full[ring.stage], TX);
+      last_phase[ring.stage] = static_cast<int>(ring.phase);
+    }
+    const uint32_t full0 = map_to_rank(smem_u32(&ctl->full[ring.stage]), 0);
+    uint8_t* sa = smem + ring.stage * STAGE_BYTES;
+    uint8_t* sb = sa + A_STAGE_BYTES;
+    tma_load_2d_pair(sa, tmA, full0, kb * BK, a_row);
+#pragma unroll
+    for (int j = 0; j < BOXES; ++j)
+      tma_load_2d_pair(sb + j * B_BOX_BYTES, tmB, full0, b_col + j * B_BOX_COLS,
+                       kb * BK);
+    ring.advance();
+  }
+  return true;
+}
+
+// MMA issue for one unit of width W into the accumulator at d_tmem.
+template <int W>
+__device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
+                                         int num_kb, uint8_t* smem,
+                                         PairControl* ctl,
+                                         volatile int* abort) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, W, /*a_mn_major=*/false,
+                                            /*b_mn_major=*/true);
+  for (int kb = 0; kb < num_kb; ++kb) {
+    if (!mbar_wait(&ctl->full[ring.stage], ring.phase, abort)) return false;
+    tc_fence_after_sync();
+    const uint32_t a_addr = smem_u32(smem + ring.stage * STAGE_BYTES);
+    const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < BK / MMA_K; ++kk) {
+      // A: K-major rows of 128 bytes; a 16-deep k step is 32 bytes in.
+      const uint64_t adesc = sdesc_sw128(a_addr + kk * MMA_K * 2, 16, 1024);
+      // B: N-major; 64-column boxes 8 KB apart (LBO), 8-row k groups 1 KB
+      // apart (SBO); a 16-deep k step is 16 rows = 2 KB in.
+      const uint64_t bdesc =
+          sdesc_sw128(b_addr + kk * MMA_K * 128, B_BOX_BYTES, 1024);
+      mma_f16_ss_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+    }
+    mma_commit_pair(&ctl->empty[ring.stage], 0x3);
+    ring.advance();
+  }
+  return true;
+}
+
+// Epilogue of one unit: this thread's row, W columns from TMEM to C.
+template <int W>
+__device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
+                                           int64_t ldc, int row, int n0, int M,
+                                           int N, int vec_c) {
+  float* crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll 1
+  for (int c = 0; c < W / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    tmem_ld_wait();
+    const int gn = n0 + c * 32;
+    if (row < M) {
+      if (vec_c && gn + 31 < N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(crow + gn + j) =
+              make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (gn + j < N) crow[gn + j] = __uint_as_float(r[j]);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       float* __restrict__ C, int64_t ldc, int M, int N, int K,
-                      int tiles_m, int tiles_n, int vec_c,
-                      unsigned int* __restrict__ status) {
+                      int tiles_m, int tiles_n, int num_full, int split,
+                      int vec_c, unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   PairControl* ctl = reinterpret_cast<PairControl*>(smem + STAGES * STAGE_BYTES);
@@ -101,6 +230,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int num_tiles = tiles_m * tiles_n;
+  // Work units: tiles [0, num_full) at full width, then every remaining tile
+  // as `split` column pieces of BN / split (the last, partial wave).
+  const int num_units = num_full + (num_tiles - num_full) * split;
   const int num_kb = (K + BK - 1) / BK;
 
   if (warp == 0 && lane == 0) {
@@ -132,37 +264,17 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      Ring ring;
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-        const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
-        const int a_row = tc.m * PAIR_M + static_cast<int>(rank) * CTA_M;
-        const int b_col = tc.n * BN + static_cast<int>(rank) * CTA_N;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!pair_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
-            ok = false;
-            break;
-          }
-          if (even) {
-            mbar_arrive_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
-            last_phase[stage] = static_cast<int>(phase);
-          }
-          const uint32_t full0 = map_to_rank(smem_u32(&ctl->full[stage]), 0);
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_STAGE_BYTES;
-          tma_load_2d_pair(sa, &tmA, full0, kb * BK, a_row);
-#pragma unroll
-          for (int j = 0; j < CTA_N / B_BOX_COLS; ++j)
-            tma_load_2d_pair(sb + j * B_BOX_BYTES, &tmB, full0,
-                             b_col + j * B_BOX_COLS, kb * BK);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+      for (int unit = pair; ok && unit < num_units; unit += num_pairs) {
+        const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
+        ok = u.width == BN
+                 ? produce_unit<BN>(u, ring, num_kb, smem, ctl, &tmA, &tmB, rank,
+                                    last_phase, abort)
+                 : produce_unit<BN / 2>(u, ring, num_kb, smem, ctl, &tmA, &tmB,
+                                        rank, last_phase, abort);
       }
       if (!ok) raise_abort(abort, peer_abort, status);
       // The even CTA's "full" barriers count both CTAs' copies: every phase
@@ -177,12 +289,12 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (even && lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      Ring ring;
       bool ok = true;
       bool issued = false;
       int t = 0;
-      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs, ++t) {
+      for (int unit = pair; ok && unit < num_units; unit += num_pairs, ++t) {
+        const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
         const int acc = t % NUM_ACC;
         const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
         if (!pair_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort)) {
@@ -191,30 +303,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!pair_wait(&ctl->full[stage], phase, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b_addr = a_addr + A_STAGE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / MMA_K; ++kk) {
-            const uint64_t adesc =
-                sdesc_sw128(a_addr + kk * MMA_K * 2, 16, 1024);
-            const uint64_t bdesc =
-                sdesc_sw128(b_addr + kk * MMA_K * 128, B_BOX_BYTES, 1024);
-            mma_f16_ss_pair(d_tmem, adesc, bdesc, IDESC,
-                            (kb | kk) != 0 ? 1u : 0u);
-          }
-          mma_commit_pair(&ctl->empty[stage], 0x3);
-          issued = true;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        issued |= num_kb > 0;
+        ok = u.width == BN ? mma_unit<BN>(d_tmem, ring, num_kb, smem, ctl, abort)
+                           : mma_unit<BN / 2>(d_tmem, ring, num_kb, smem, ctl, abort);
         if (!ok) break;
         mma_commit_pair(&ctl->acc_full[acc], 0x3);
       }
@@ -230,7 +321,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     int t = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++t) {
+    for (int unit = pair; unit < num_units; unit += num_pairs, ++t) {
       const int acc = t % NUM_ACC;
       const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
       int ok = 0;
@@ -241,32 +332,14 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       }
       tc_fence_after_sync();
-      const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
-      const int row = tc.m * PAIR_M + static_cast<int>(rank) * CTA_M + q * 32 + lane;
-      float* crow = C + static_cast<int64_t>(row) * ldc;
+      const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
+      const int row = u.m0 + static_cast<int>(rank) * CTA_M + q * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_ld_wait();
-        const int gn = tc.n * BN + c * 32;
-        if (row < M) {
-          if (vec_c && gn + 31 < N) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(crow + gn + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]),
-                              __uint_as_float(r[j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gn + j < N) crow[gn + j] = __uint_as_float(r[j]);
-          }
-        }
-      }
+      if (u.width == BN)
+        store_unit<BN>(taddr, C, ldc, row, u.n0, M, N, vec_c);
+      else
+        store_unit<BN / 2>(taddr, C, ldc, row, u.n0, M, N, vec_c);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0)
@@ -332,10 +405,18 @@ int pair_max_active(cudaStream_t stream) {
 
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   float* C, int64_t ldc, int M, int N, int K,
-                                  bool vec_c, int pairs, unsigned int* status,
+                                  bool vec_c, int max_pairs, unsigned int* status,
                                   cudaStream_t stream) {
   const int tiles_m = (M + PAIR_M - 1) / PAIR_M;
   const int tiles_n = (N + BN - 1) / BN;
+  const int tiles = tiles_m * tiles_n;
+  // A last wave that fills at most half of the pairs runs as half-width
+  // units instead, so it takes half as long.
+  const int tail = tiles % max_pairs;
+  const int split = (tail > 0 && 2 * tail <= max_pairs) ? 2 : 1;
+  const int num_full = split == 2 ? tiles - tail : tiles;
+  const int units = num_full + (tiles - num_full) * split;
+  const int pairs = units < max_pairs ? units : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -349,7 +430,8 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel, tmA, tmB, C, ldc, M, N,
-                            K, tiles_m, tiles_n, vec_c ? 1 : 0, status);
+                            K, tiles_m, tiles_n, num_full, split,
+                            vec_c ? 1 : 0, status);
 }
 
 }  // namespace g07

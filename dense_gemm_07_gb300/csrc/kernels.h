@@ -45,9 +45,10 @@ size_t pair_smem_bytes();
 // Clusters of two CTAs that can be resident at once (0 if the pair kernel
 // cannot run on this device).
 int pair_max_active(cudaStream_t stream);
+// `max_pairs` clusters at most (persistent); the last wave may be split.
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   float* C, int64_t ldc, int M, int N, int K,
-                                  bool vec_c, int pairs, unsigned int* status,
+                                  bool vec_c, int max_pairs, unsigned int* status,
                                   cudaStream_t stream);
 
 // ---- small helpers (gemm_aux.cu)

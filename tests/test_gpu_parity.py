@@ -100,6 +100,15 @@ def test_bf16_small_and_ragged_k(K):
     _check("bf16", 130, 260, K, 5, inputs.INT3, exact=True)
 
 
+def test_bf16_full_and_split_waves_exact():
+    # 256 pair tiles: whole waves of 256 x 256 tiles, then the last wave as
+    # 256 x 128 units (rows 3072..4095 hold some of them)
+    M, N, K = 4096, 4096, 136
+    rows = np.unique(np.concatenate([_sample_rows(M, 40, 17),
+                                     [3072, 3300, 3839, 3840, 3999, 4095]]))
+    _check("bf16", M, N, K, 17, inputs.INT3, exact=True, rows=rows)
+
+
 def test_bf16_4096_sampled_rows():
     M = N = K = 4096
     _check("bf16", M, N, K, 2, inputs.NORMAL, rows=_sample_rows(M, 48, 2))
