@@ -197,24 +197,47 @@ gemm_status_t encoder(EncodeTiledFn* fn) {
 
 // 2-D BF16 tensor map: dims {inner, outer}, row stride ld elements, box
 // {box_inner, box_outer}, 128-byte swizzle, zero fill out of range.
-gemm_status_t make_map(CUtensorMap* map, const void* base, int64_t inner,
-                       int64_t outer, int64_t ld, uint32_t box_inner,
-                       uint32_t box_outer) {
+gemm_status_t make_map_typed(CUtensorMap* map, CUtensorMapDataType type,
+                             int64_t elem_bytes, const void* base, int64_t inner,
+                             int64_t outer, int64_t ld, uint32_t box_inner,
+                             uint32_t box_outer) {
   EncodeTiledFn enc = nullptr;
   gemm_status_t s = encoder(&enc);
   if (s != GEMM_OK) return s;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner),
                               static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * elem_bytes)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  const CUresult r = enc(map, type, 2,
                          const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INTERNAL;
+}
+
+gemm_status_t make_map(CUtensorMap* map, const void* base, int64_t inner,
+                       int64_t outer, int64_t ld, uint32_t box_inner,
+                       uint32_t box_outer) {
+  return make_map_typed(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner,
+                        outer, ld, box_inner, box_outer);
+}
+
+// The TMA-store epilogue needs C 16-byte aligned with rows a multiple of 16
+// bytes apart, and N a multiple of 4: the copy engine clips the inner
+// dimension of a store in 16-byte units, so a row that ends mid-unit would
+// be written past column N-1.
+bool tma_store_ok(const float* C, int64_t N, int64_t ldc) {
+  return aligned16(C) && ldc % 4 == 0 && N % 4 == 0;
+}
+
+// FP32 map of C for the TMA-store epilogue: 32 x 32 boxes, 128-byte swizzle.
+gemm_status_t make_map_c(CUtensorMap* map, const float* C, int64_t M,
+                         int64_t N, int64_t ldc) {
+  return make_map_typed(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, ldc,
+                        32, 32);
 }
 
 gemm_status_t pool_alloc(DeviceState* d, void** p, int64_t bytes,
@@ -297,8 +320,11 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
     const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
     if (max_pairs > 0) {
-      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c,
-                                          max_pairs, d->status, stream));
+      CUtensorMap tmC;
+      const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
+      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
+                                          ldc, m, n, k, vec_c, max_pairs,
+                                          d->status, stream));
     } else {
       const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
                             ((N + kTcTileN - 1) / kTcTileN);
@@ -446,8 +472,11 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (max_pairs > 0) {
-    return from_cuda(launch_gemm_bf16_pair(tmA, tmB, C, ldc, m, n, k, vec_c,
-                                           max_pairs, d->status, stream));
+    CUtensorMap tmC;
+    const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
+    return from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
+                                           ldc, m, n, k, vec_c, max_pairs,
+                                           d->status, stream));
   }
   const int64_t tiles =
       ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);

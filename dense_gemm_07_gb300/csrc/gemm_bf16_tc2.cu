@@ -29,15 +29,19 @@
 //   warp 1 (even CTA)   MMA issuer: waits on "full", issues 4 pair MMAs per
 //                       stage, commits to "empty" in both CTAs, and after the
 //                       last slice of a tile to "accumulator full" in both.
-//   warps 2-5 (both)    epilogue: TMEM -> registers -> C (guarded 16-byte
-//                       stores), then arrive on the even CTA's
-//                       "accumulator empty" (8 arrivals per tile).
+//   warps 2-5 (both)    epilogue: TMEM -> registers -> swizzled shared
+//                       staging box -> TMA tensor store of C (whole lines;
+//                       rows/columns outside C are clipped), or guarded
+//                       direct stores when C's layout does not allow TMA;
+//                       then arrive on the even CTA's "accumulator empty"
+//                       (8 arrivals per tile).
 // Tensor memory: NUM_ACC 256-column FP32 accumulators per CTA; with two, a
 // tile's epilogue overlaps the next tile's MMAs.  Every wait is bounded; on expiry
 // the CTA raises its own and its peer's abort flag and the status word, all
 // roles unwind, copies and MMAs in flight are drained, and both CTAs meet at
 // a final cluster barrier before tensor memory is released.
 #include <cstdint>
+#include <cstring>
 
 #include "kernels.h"
 #include "sm103_ptx.cuh"
@@ -61,6 +65,9 @@ constexpr int MMA_K = 16;
 constexpr int NUM_ACC = 2;                        // accumulators in TMEM
 constexpr int TMEM_COLS = NUM_ACC * BN;
 constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BOX_BYTES = 32 * 32 * 4;            // one 32 x 32 FP32 box
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BOX_BYTES;  // double-buffered
 constexpr int GROUP = 8;
 
 struct alignas(8) PairControl {
@@ -212,15 +219,56 @@ __device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
   }
 }
 
+// Epilogue of one unit through shared memory and TMA stores: per 32-column
+// chunk the warp writes its 32 x 32 block into a 128-byte-swizzled staging
+// box (each lane one row, conflict-free 16-byte stores) and one lane stores
+// the box with the copy engine, which writes whole lines and clips rows and
+// columns outside C.  Two staging boxes per warp alternate.
+template <int W>
+__device__ __forceinline__ void store_unit_tma(uint32_t taddr,
+                                               const CUtensorMap* tmC,
+                                               uint8_t* ebuf, int row0, int n0,
+                                               int M, int N, int lane,
+                                               int& chunk) {
+#pragma unroll 1
+  for (int c = 0; c < W / 32; ++c) {
+    // Boxes wholly outside C are skipped (warp-uniform test); every other
+    // chunk issues exactly one store group, which the buffer alternation
+    // below relies on.
+    if (row0 >= M || n0 + c * 32 >= N) continue;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    uint8_t* buf = ebuf + (chunk++ & 1) * EPI_BOX_BYTES;
+    if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
+    __syncwarp();
+    tmem_ld_wait();
+    uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+          make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    // partial boxes are clipped by the copy engine
+    if (lane == 0) {
+      tma_store_2d(tmC, buf, n0 + c * 32, row0);
+      bulk_commit();
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC,
                       float* __restrict__ C, int64_t ldc, int M, int N, int K,
                       int tiles_m, int tiles_n, int num_full, int split,
-                      int vec_c, unsigned int* __restrict__ status) {
+                      int vec_c, int tma_c, unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  PairControl* ctl = reinterpret_cast<PairControl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
+  PairControl* ctl =
+      reinterpret_cast<PairControl*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
   volatile int* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -320,6 +368,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    uint8_t* ebuf = epi_smem + (warp - 2) * 2 * EPI_BOX_BYTES;
+    int chunk = 0;
     int t = 0;
     for (int unit = pair; unit < num_units; unit += num_pairs, ++t) {
       const int acc = t % NUM_ACC;
@@ -336,15 +386,25 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const int row = u.m0 + static_cast<int>(rank) * CTA_M + q * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      if (u.width == BN)
+      const int row0 = row - lane;
+      if (tma_c) {
+        if (u.width == BN)
+          store_unit_tma<BN>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane, chunk);
+        else
+          store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane,
+                                 chunk);
+      } else if (u.width == BN) {
         store_unit<BN>(taddr, C, ldc, row, u.n0, M, N, vec_c);
-      else
+      } else {
         store_unit<BN / 2>(taddr, C, ldc, row, u.n0, M, N, vec_c);
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0)
         mbar_arrive_cluster(map_to_rank(smem_u32(&ctl->acc_empty[acc]), 0));
     }
+    // Every store issued must have completed before the CTA exits.
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before_sync();
@@ -366,7 +426,8 @@ LaunchInfo g_info[64];
 }  // namespace
 
 size_t pair_smem_bytes() {
-  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(PairControl);
+  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + EPI_BYTES +
+         sizeof(PairControl);
 }
 
 int pair_max_active(cudaStream_t stream) {
@@ -404,9 +465,9 @@ int pair_max_active(cudaStream_t stream) {
 }
 
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                  float* C, int64_t ldc, int M, int N, int K,
-                                  bool vec_c, int max_pairs, unsigned int* status,
-                                  cudaStream_t stream) {
+                                  const CUtensorMap* tmC, float* C, int64_t ldc,
+                                  int M, int N, int K, bool vec_c, int max_pairs,
+                                  unsigned int* status, cudaStream_t stream) {
   const int tiles_m = (M + PAIR_M - 1) / PAIR_M;
   const int tiles_n = (N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n;
@@ -429,9 +490,12 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel, tmA, tmB, C, ldc, M, N,
-                            K, tiles_m, tiles_n, num_full, split,
-                            vec_c ? 1 : 0, status);
+  CUtensorMap unused;
+  if (tmC == nullptr) std::memset(&unused, 0, sizeof(unused));
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel, tmA, tmB,
+                            tmC ? *tmC : unused, C, ldc, M, N, K, tiles_m,
+                            tiles_n, num_full, split, vec_c ? 1 : 0,
+                            tmC ? 1 : 0, status);
 }
 
 }  // namespace g07

@@ -46,10 +46,12 @@ size_t pair_smem_bytes();
 // cannot run on this device).
 int pair_max_active(cudaStream_t stream);
 // `max_pairs` clusters at most (persistent); the last wave may be split.
+// tmC: FP32 tensor map of C (box 32 x 32, 128-byte swizzle) for TMA stores,
+// or nullptr to store directly from registers.
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                  float* C, int64_t ldc, int M, int N, int K,
-                                  bool vec_c, int max_pairs, unsigned int* status,
-                                  cudaStream_t stream);
+                                  const CUtensorMap* tmC, float* C, int64_t ldc,
+                                  int M, int N, int K, bool vec_c, int max_pairs,
+                                  unsigned int* status, cudaStream_t stream);
 
 // ---- small helpers (gemm_aux.cu)
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
