@@ -50,6 +50,7 @@ SIGNATURES = [
     ("gemm_get_device_status", _i32, [_vp]),
     ("gemm_shutdown", None, []),
     ("gemm_abi_version", _i32, []),
+    ("gemm_launch_count", ctypes.c_uint64, []),
     ("gemm_tile_order", _i32, [_i64, _i64, _i64, _i64,
                                ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     ("gemm_plan_bf16", _i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
@@ -120,6 +121,10 @@ def gemm_shutdown() -> None:
 
 def gemm_abi_version() -> int:
     return lib().gemm_abi_version()
+
+
+def gemm_launch_count() -> int:
+    return int(lib().gemm_launch_count())
 
 
 def gemm_tile_order(tiles_m, tiles_n, group, linear):

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/gemm07.h: argument checking, path
 // selection, tensor-map encoding, per-device state and the kernel launches.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -12,6 +13,11 @@
 #include "tile_order.cuh"
 
 namespace g07 {
+
+std::atomic<uint64_t> g_launches{0};
+
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
 namespace {
 
 // Device-side status word: bit 0 = a bounded wait ran out.
@@ -582,6 +588,8 @@ void gemm_shutdown(void) {
 }
 
 int gemm_abi_version(void) { return 1; }
+
+uint64_t gemm_launch_count(void) { return g_launches.load(); }
 
 gemm_status_t gemm_tile_order(int64_t tiles_m, int64_t tiles_n, int64_t group,
                               int64_t linear, int64_t* tile_m,

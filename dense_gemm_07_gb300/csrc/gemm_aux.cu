@@ -51,6 +51,7 @@ cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
   const int threads = 256;
   zero_fill_f32_kernel<<<grid_for(static_cast<int64_t>(M) * N, threads),
                          threads, 0, stream>>>(C, ldc, M, N);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -61,6 +62,7 @@ cudaError_t launch_copy_rows_u16(const uint16_t* src, int64_t ld_src,
   copy_rows_u16_kernel<<<grid_for(static_cast<int64_t>(rows) * cols, threads),
                          threads, 0, stream>>>(src, ld_src, dst, ld_dst, rows,
                                                cols);
+  note_launches(1);
   return cudaGetLastError();
 }
 

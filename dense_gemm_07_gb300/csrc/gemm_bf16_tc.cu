@@ -288,6 +288,7 @@ cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const int tiles_n = (N + BN - 1) / BN;
   gemm_bf16_tc_kernel<<<grid, THREADS, smem, stream>>>(
       tmA, tmB, C, ldc, M, N, K, tiles_m, tiles_n, vec_c ? 1 : 0, status);
+  note_launches(1);
   return cudaGetLastError();
 }
 

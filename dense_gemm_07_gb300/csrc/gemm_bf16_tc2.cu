@@ -492,10 +492,11 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   cfg.numAttrs = 1;
   CUtensorMap unused;
   if (tmC == nullptr) std::memset(&unused, 0, sizeof(unused));
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel, tmA, tmB,
-                            tmC ? *tmC : unused, C, ldc, M, N, K, tiles_m,
-                            tiles_n, num_full, split, vec_c ? 1 : 0,
-                            tmC ? 1 : 0, status);
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused, C, ldc, M, N,
+      K, tiles_m, tiles_n, num_full, split, vec_c ? 1 : 0, tmC ? 1 : 0, status);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 }  // namespace g07

@@ -255,6 +255,7 @@ cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
   const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<TN>);
   gemm_f32_regblock_kernel<TN, VEC_B><<<blocks, THREADS, smem, stream>>>(
       M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, vec_c);
+  note_launches(1);
   return cudaGetLastError();
 }
 

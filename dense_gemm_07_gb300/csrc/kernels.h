@@ -8,6 +8,10 @@
 
 namespace g07 {
 
+// Records `n` kernel launches by this library (defined in api.cu); the total
+// is exported through gemm_launch_count().
+void note_launches(int n);
+
 // ---- FP32 SIMT path (gemm_f32.cu)
 constexpr int kF32TileM = 128;
 constexpr int kF32TileN = 128;

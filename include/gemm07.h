@@ -166,6 +166,12 @@ GEMM07_API void gemm_shutdown(void);
 GEMM07_API int gemm_abi_version(void);
 
 /*
+ * Number of CUDA kernels this library has launched in this process, across
+ * all entry points and devices (for accounting, e.g. kernels per step).
+ */
+GEMM07_API uint64_t gemm_launch_count(void);
+
+/*
  * Host-only helpers (no GPU needed), exported so that the tile scheduling
  * and the path selection can be checked without a device.
  *
