@@ -112,8 +112,23 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->pack_a = (aligned16(A) && lda % 8 == 0) ? 0 : 1;
   p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
   p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
-  // More than one 128-row tile: 256 x 256 tiles on SM pairs; otherwise one
-  // SM per 128 x 256 tile.
+  int64_t ws = 0;
+  if (p->pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
+  if (p->pack_b) ws += round_up(K * round_up(N, 8) * 2, 256);
+  p->workspace_bytes = ws;
+  if (M <= kSkinnyMaxM) {
+    // Small M: 128-column tiles of C, K split over a cluster (the split is
+    // reported for the 152 SMs of a GB300; launches use the device's count).
+    p->path = GEMM_PATH_BF16_SKINNY;
+    p->tile_m = skinny_rows(static_cast<int>(M));
+    p->tile_n = kSkinnyTileN;
+    p->tile_k = kTcTileK;
+    p->stages = 0;
+    p->split_k = skinny_split(static_cast<int>(N), static_cast<int>(K), 152);
+    p->tiles = ((N + kSkinnyTileN - 1) / kSkinnyTileN) * p->split_k;
+    return GEMM_OK;
+  }
+  // 256 x 256 tiles on SM pairs.
   const bool pair = M > kTcTileM;
   p->tile_m = pair ? kPairTileM : kTcTileM;
   p->tile_n = pair ? kPairTileN : kTcTileN;
@@ -121,10 +136,6 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->stages = pair ? kPairStages : kTcStages;
   p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
-  int64_t ws = 0;
-  if (p->pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
-  if (p->pack_b) ws += round_up(K * round_up(N, 8) * 2, 256);
-  p->workspace_bytes = ws;
   return GEMM_OK;
 }
 
@@ -319,10 +330,16 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     b_op = dst;
   }
   CUtensorMap tmA, tmB;
+  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
   if (s == GEMM_OK)
-    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK, kTcTileM);
+    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK,
+                 skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
   if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
-  if (s == GEMM_OK) {
+  if (s == GEMM_OK && skinny) {
+    s = from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
+                                          skinny_split(n, k, d->sms), d->status,
+                                          stream));
+  } else if (s == GEMM_OK) {
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
     const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
     if (max_pairs > 0) {
@@ -472,9 +489,16 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
     b_op = dst;
   }
   CUtensorMap tmA, tmB;
-  if (s == GEMM_OK) s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK, kTcTileM);
+  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
+  if (s == GEMM_OK)
+    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK,
+                 skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
   if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
   if (s != GEMM_OK) return s;
+  if (skinny)
+    return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
+                                             skinny_split(n, k, d->sms),
+                                             d->status, stream));
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (max_pairs > 0) {

@@ -57,6 +57,20 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
                                   int M, int N, int K, bool vec_c, int max_pairs,
                                   unsigned int* status, cudaStream_t stream);
 
+// ---- BF16 small-M path (gemm_bf16_skinny.cu): swap-AB, split-K over a
+// cluster, partial sums reduced through distributed shared memory.
+constexpr int kSkinnyMaxM = 128;
+constexpr int kSkinnyTileN = 128;
+// MMA N used for M rows (16, 32, 64 or 128).
+int skinny_rows(int M);
+// CTAs per cluster (k split) for an N x K problem on `sms` SMs (1..8).
+int skinny_split(int N, int K, int sms);
+// tmA: box {64, skinny_rows(M)}; tmB: the usual box {64, 64}.
+cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,
+                                    const CUtensorMap& tmB, float* C,
+                                    int64_t ldc, int M, int N, int K, int cs,
+                                    unsigned int* status, cudaStream_t stream);
+
 // ---- small helpers (gemm_aux.cu)
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
                                  cudaStream_t stream);

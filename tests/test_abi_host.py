@@ -98,13 +98,22 @@ def test_plan_paths():
     path, p = _path("bf16", 4096, 4096, 4096)
     assert path == "bf16_tma" and p.tiles == 16 * 16 and p.workspace_bytes == 0
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
-    path, p = _path("bf16", 128, 4096, 4096)
-    assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (128, 256, 4)
-    assert p.tiles == 16
+    path, p = _path("bf16", 129, 4096, 4096)
+    assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (256, 256, 6)
+    # M <= 128: small-M path, 128-column tiles, K split 4 ways over 32 tiles
+    path, p = _path("bf16", 16, 4096, 4096)
+    assert path == "bf16_skinny" and (p.tile_m, p.tile_n, p.split_k) == (16, 128, 4)
+    assert p.tiles == 32 * 4
+    assert _path("bf16", 1, 4096, 4096)[1].tile_m == 16
+    assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
+    assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
+    assert _path("bf16", 16, 100, 64)[1].split_k == 1      # one k slice only
     path, p = _path("f32", 4096, 4096, 4096)
     assert path == "f32_simt" and p.tiles == 32 * 32
     # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
     path, p = _path("bf16", 127, 1000, 3001)
+    assert path == "bf16_skinny" and p.pack_a == 1 and p.pack_b == 0
+    path, p = _path("bf16", 300, 1000, 3001)
     assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
     assert p.workspace_bytes >= 127 * 3008 * 2
     # misaligned base address -> packed

@@ -133,6 +133,19 @@ def test_bf16_skinny_exact(M):
     _check("bf16", M, 4096, 4096, 4, inputs.INT3, exact=True)
 
 
+@pytest.mark.parametrize("shape", [(2, 300, 1000), (17, 1000, 777), (33, 257, 4096),
+                                   (64, 4096, 64), (65, 999, 130), (100, 128, 3001),
+                                   (128, 2048, 2048), (5, 50, 1)])
+def test_bf16_small_m_paths_exact(shape):
+    # every MMA width (16/32/64/128), ragged N and K, K below the split count
+    M, N, K = shape
+    _check("bf16", M, N, K, 18, inputs.INT3, exact=True)
+
+
+def test_bf16_small_m_normal_values():
+    _check("bf16", 24, 3000, 4096, 19, inputs.NORMAL, inputs.NORMAL_W)
+
+
 # ------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("kind", ["f32", "bf16"])
