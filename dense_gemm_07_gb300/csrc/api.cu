@@ -286,12 +286,29 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   if (plan.path == GEMM_PATH_ZERO_FILL)
     return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
                                           static_cast<int>(N), stream));
-  const bool vec_a = aligned16(A) && lda % 4 == 0;
   const bool vec_b = aligned16(B) && ldb % 4 == 0;
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
-  return from_cuda(launch_gemm_f32(static_cast<int>(M), static_cast<int>(N),
-                                   static_cast<int>(K), A, lda, B, ldb, C, ldc,
-                                   vec_a, vec_b, vec_c, stream));
+  const int m = static_cast<int>(M), n = static_cast<int>(N),
+            k = static_cast<int>(K);
+  const int64_t slots = f32_slots();
+  if (slots <= 0) return GEMM_ERR_LAUNCH;
+  const F32Plan fp = f32_plan(m, n, k, slots);
+  void* ws = nullptr;
+  const int64_t ws_bytes = round_up(fp.workspace_bytes, 256) + fp.counter_bytes;
+  s = pool_alloc(d, &ws, ws_bytes, stream);
+  if (s != GEMM_OK) return s;
+  float* partials = static_cast<float*>(ws);
+  unsigned int* counters = nullptr;
+  if (fp.split > 1) {
+    counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) +
+                                               round_up(fp.workspace_bytes, 256));
+    s = from_cuda(cudaMemsetAsync(counters, 0, fp.counter_bytes, stream));
+  }
+  if (s == GEMM_OK)
+    s = from_cuda(launch_gemm_f32(m, n, k, A, lda, B, ldb, C, ldc, vec_b, vec_c,
+                                  fp, partials, counters, stream));
+  pool_free(ws, stream);
+  return s;
 }
 
 gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,

@@ -19,7 +19,12 @@
 //     copies global -> shared without passing through registers and zero-fills
 //     out-of-range elements (the ": 0.0f" of the guarded tiled kernel); one
 //     barrier per slice;
-//   * stores are guarded on both row < M and col < N.
+//   * stores are guarded on both row < M and col < N;
+//   * wave tail: tiles are launched in whole waves of resident blocks; the
+//     tiles of a last, partial wave are split along K (split-K, "A06",
+//     section 3) into ranges computed by separate blocks, whose partial sums
+//     are added in a fixed order by the last block to finish, so the tail
+//     keeps every SM busy and results stay deterministic.
 //
 // Thread layout: 8 warps as 4 (M) x 2 (N), each warp a 32 x 64 sub-tile;
 // lane (ly = lane/8, lx = lane%8) owns rows {4ly..4ly+3, 16+4ly..16+4ly+3}
@@ -39,6 +44,8 @@ constexpr int BK = kF32TileK;
 constexpr int THREADS = 256;
 constexpr int STAGES = kF32Stages;
 constexpr int A_STRIDE = BM + 4;  // transposed A rows, padded
+static_assert(THREADS % BK == 0 && BM % (THREADS / BK) == 0 && BM / (THREADS / BK) <= 32,
+              "copy plan covers the A slice in whole passes");
 
 template <int TN>
 struct F32Stage {
@@ -82,13 +89,15 @@ template <int TN, bool VEC_B>
 struct SliceLoader {
   static constexpr int B_ITERS = VEC_B ? BK * TN / 4 / THREADS : BK * TN / THREADS;
   static constexpr int B_ROW_STEP = VEC_B ? THREADS / (TN / 4) : THREADS / TN;
+  static constexpr int A_ROW_STEP = THREADS / BK;     // rows per pass over A
+  static constexpr int A_ITERS = BM / A_ROW_STEP;     // passes per slice
   const float* a_ptr;  // A[m0 + r0][k], advanced by BK per slice
   const float* b_ptr;  // B[kr0][n0 + nc], advanced by BK rows per slice
   const float* a_base;
   const float* b_base;
   int64_t a_step;      // 16 rows of A
   int64_t b_step;      // B_ROW_STEP rows of B
-  uint32_t a_rows_ok;  // bit i: row m0 + r0 + 16 i < M
+  uint32_t a_rows_ok;  // bit i: row m0 + r0 + A_ROW_STEP * i < M
   uint32_t b_bytes;    // bytes of this thread's B group inside [0, N)
   uint32_t a_dst, b_dst;  // offsets of this thread's first element in a stage
   int k_a, k_b;        // k of this thread's A element / first B row, slice 0
@@ -97,17 +106,17 @@ struct SliceLoader {
   __device__ __forceinline__ SliceLoader(const float* A, int64_t lda,
                                          const float* B, int64_t ldb, int M,
                                          int N, int K_, int m0, int n0,
-                                         int tid) {
+                                         int kt_start, int tid) {
     K = K_;
-    const int r0 = tid >> 4;
-    k_a = tid & 15;
+    const int r0 = tid / BK;
+    k_a = tid % BK;
     a_base = A;
     a_ptr = A + static_cast<int64_t>(m0 + r0) * lda + k_a;
-    a_step = 16 * lda;
+    a_step = A_ROW_STEP * lda;
     a_rows_ok = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (m0 + r0 + 16 * i < M) a_rows_ok |= 1u << i;
+    for (int i = 0; i < A_ITERS; ++i)
+      if (m0 + r0 + A_ROW_STEP * i < M) a_rows_ok |= 1u << i;
     a_dst = static_cast<uint32_t>((k_a * A_STRIDE + r0) * sizeof(float));
     b_base = B;
     int nc;
@@ -123,19 +132,23 @@ struct SliceLoader {
     }
     b_ptr = B + static_cast<int64_t>(k_b) * ldb + n0 + nc;
     b_step = B_ROW_STEP * ldb;
+    // start at k-slice kt_start
+    a_ptr += static_cast<int64_t>(kt_start) * BK;
+    b_ptr += static_cast<int64_t>(kt_start) * BK * ldb;
     b_dst = static_cast<uint32_t>(
         (offsetof(F32Stage<TN>, b) / sizeof(float) + k_b * TN + nc) * sizeof(float));
     (void)ldb;
   }
 
-  // Issue the copies of slice kt into the stage at shared address `stage`.
+  // Issue the copies of slice kt into the stage at shared address `stage`
+  // (slices must be requested in consecutive order from kt_start).
   __device__ __forceinline__ void load(uint32_t stage, int kt) {
     const int k0 = kt * BK;
     const bool ka = k0 + k_a < K;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < A_ITERS; ++i) {
       const bool ok = ka && ((a_rows_ok >> i) & 1u);
-      cp_async4(stage + a_dst + i * 16 * sizeof(float),
+      cp_async4(stage + a_dst + i * A_ROW_STEP * sizeof(float),
                 ok ? a_ptr + i * a_step : a_base, ok ? 4u : 0u);
     }
     a_ptr += BK;
@@ -153,30 +166,77 @@ struct SliceLoader {
   }
 };
 
-// TN = 128: full 128 x 128 tiles, thread patch 8 x 8.  TN = 64: half-width
-// 128 x 64 tiles (thread patch 8 x 4) for the last, partial wave of a grid.
-// Tile `first + blockIdx.x / SPLIT` of the grouped order is computed; with
-// SPLIT = 2 each block takes column half blockIdx.x % 2 of it.
-template <int TN, bool VEC_B>
+// Guarded store of one 4-wide group of row `crow` at column gn.
+__device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
+                                       float4 v) {
+  if (vec_c && gn + 3 < N) {
+    *reinterpret_cast<float4*>(crow + gn) = v;
+  } else {
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (gn + j < N) crow[gn + j] = e[j];
+  }
+}
+
+// Last block of a split tile: add the `split` parked partial tiles in range
+// order 0, 1, ..., split-1 and write this thread's 8 x 8 patch of C.
+__device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
+                                           float* C, int64_t ldc, int M, int N,
+                                           int m0, int n0, int row_a, int col_b,
+                                           int vec_c) {
+#pragma unroll 1
+  for (int i = 0; i < 8; ++i) {
+    const int r = row_a + (i < 4 ? i : 12 + i);
+    const int gm = m0 + r;
+    if (gm >= M) continue;
+    float* crow = C + static_cast<int64_t>(gm) * ldc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float* src = tile_ws + r * BN + col_b + 32 * h;
+      float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
+      for (int q = 1; q < split; ++q) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + q * (BM * BN)));
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+      store4(crow, n0 + col_b + 32 * h, N, vec_c, sum);
+    }
+  }
+}
+
+// One launch computes tiles first .. first + gridDim.x / split - 1 of the
+// grouped order; with split > 1 each tile's k-slices are cut into `split`
+// contiguous ranges, one per block (split-K), block b taking range b % split
+// of tile first + b / split.  A split tile's partial sums go to `ws`
+// (split x 128 x 128 floats per tile); the last of its blocks to finish (per
+// `counters`, zero at launch) adds the partials in range order 0, 1, ... and
+// writes C, so the result does not depend on which block finishes last.
+template <bool VEC_B>
 __global__ void __launch_bounds__(THREADS, 2)
 gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
                          int64_t lda, const float* __restrict__ B, int64_t ldb,
                          float* __restrict__ C, int64_t ldc, int tiles_m,
-                         int tiles_n, int first, int vec_c) {
-  constexpr int SPLIT = BN / TN;   // column pieces per 128 x 128 tile
-  constexpr int JP = TN / 32;      // float2 accumulators per row (4 or 2)
+                         int tiles_n, int first, int split, int vec_c,
+                         float* __restrict__ ws, unsigned int* __restrict__ counters) {
+  constexpr int TN = BN;
+  constexpr int JP = TN / 32;      // float2 accumulators per row
   extern __shared__ __align__(16) uint8_t smem_raw[];
   F32Stage<TN>* stage = reinterpret_cast<F32Stage<TN>*>(smem_raw);
+  __shared__ int last_block;
 
-  const TileCoord tc =
-      tile_order(first + blockIdx.x / SPLIT, tiles_m, tiles_n, kF32Group);
+  const int local_tile = blockIdx.x / split;
+  const int piece = blockIdx.x % split;
+  const TileCoord tc = tile_order(first + local_tile, tiles_m, tiles_n, kF32Group);
   const int m0 = tc.m * BM;
-  const int n0 = tc.n * BN + (blockIdx.x % SPLIT) * TN;
+  const int n0 = tc.n * BN;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int row_a = (warp >> 1) * 32 + (lane >> 3) * 4;      // + {0..3, 16..19}
-  const int col_b = (warp & 1) * (TN / 2) + (lane & 7) * 4;  // + {0..3[, 32..35]}
+  const int col_b = (warp & 1) * (TN / 2) + (lane & 7) * 4;  // + {0..3, 32..35}
 
   // acc[i][jp]: columns 2jp, 2jp+1 (then 32 + ...) of row i of the patch.
   float2 acc[8][JP];
@@ -185,12 +245,15 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
 #pragma unroll
     for (int j = 0; j < JP; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
-  const int nk = (K + BK - 1) / BK;
-  SliceLoader<TN, VEC_B> loader(A, lda, B, ldb, M, N, K, m0, n0, tid);
+  const int nk_all = (K + BK - 1) / BK;
+  const int kt_begin = static_cast<int>(static_cast<int64_t>(nk_all) * piece / split);
+  const int kt_end = static_cast<int>(static_cast<int64_t>(nk_all) * (piece + 1) / split);
+  const int nk = kt_end - kt_begin;
+  SliceLoader<TN, VEC_B> loader(A, lda, B, ldb, M, N, K, m0, n0, kt_begin, tid);
   const uint32_t stage0 = smem_addr(stage);
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nk) loader.load(stage0 + s * sizeof(F32Stage<TN>), s);
+    if (s < nk) loader.load(stage0 + s * sizeof(F32Stage<TN>), kt_begin + s);
     cp_async_commit();
   }
 
@@ -199,7 +262,8 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     __syncthreads();              // everyone's landed; slice kt-1 consumed
     {
       const int nxt = kt + STAGES - 1;
-      if (nxt < nk) loader.load(stage0 + (nxt % STAGES) * sizeof(F32Stage<TN>), nxt);
+      if (nxt < nk)
+        loader.load(stage0 + (nxt % STAGES) * sizeof(F32Stage<TN>), kt_begin + nxt);
       cp_async_commit();
     }
     const F32Stage<TN>& st = stage[kt % STAGES];
@@ -225,6 +289,32 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   }
   cp_async_wait<0>();
 
+  if (split > 1) {
+    // Park this range's partial tile, then count the tile's finished ranges.
+    float* tile_ws = ws + static_cast<int64_t>(local_tile) * split * (BM * BN);
+    float* mine = tile_ws + piece * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = row_a + (i < 4 ? i : 12 + i);
+#pragma unroll
+      for (int h = 0; h < JP / 2; ++h)
+        __stcg(reinterpret_cast<float4*>(mine + r * BN + col_b + 32 * h),
+               make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                           acc[i][2 * h + 1].y));
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+      last_block = atomicAdd(&counters[local_tile], 1u) == static_cast<unsigned>(split - 1);
+    __syncthreads();
+    if (last_block) {
+      __threadfence();
+      reduce_ranges(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c);
+      if (tid == 0) counters[local_tile] = 0;  // leave the counter as found
+    }
+    return;
+  }
+
   // Epilogue: guarded stores, 16-byte vectors where the layout allows.
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -247,23 +337,25 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   }
 }
 
-template <int TN, bool VEC_B>
+template <bool VEC_B>
 cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int64_t lda, const float* B, int64_t ldb, float* C,
                         int64_t ldc, int tiles_m, int tiles_n, int first,
-                        int vec_c, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<TN>);
-  gemm_f32_regblock_kernel<TN, VEC_B><<<blocks, THREADS, smem, stream>>>(
-      M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, vec_c);
+                        int split, int vec_c, float* ws, unsigned int* counters,
+                        cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<BN>);
+  gemm_f32_regblock_kernel<VEC_B><<<blocks, THREADS, smem, stream>>>(
+      M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
+      counters);
   note_launches(1);
   return cudaGetLastError();
 }
 
-template <int TN, bool VEC_B>
+template <bool VEC_B>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_f32_regblock_kernel<TN, VEC_B>,
+  return cudaFuncSetAttribute(gemm_f32_regblock_kernel<VEC_B>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(STAGES * sizeof(F32Stage<TN>)));
+                              static_cast<int>(STAGES * sizeof(F32Stage<BN>)));
 }
 
 int g_attr_set[64];
@@ -271,61 +363,84 @@ int64_t g_slots[64];
 
 }  // namespace
 
-int f32_blocks_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, gemm_f32_regblock_kernel<BN, true>, THREADS,
-          STAGES * sizeof(F32Stage<BN>)) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-// Whole waves of full tiles first; the tiles of a last, partial wave are
-// split into two half-width tiles when that keeps them within one wave
-// (the grid is then two launches on the stream).
-cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
-                            const float* B, int64_t ldb, float* C, int64_t ldc,
-                            bool /*vec_a*/, bool vec_b, bool vec_c,
-                            cudaStream_t stream) {
-  const int tiles_m = (M + BM - 1) / BM;
-  const int tiles_n = (N + BN - 1) / BN;
-  const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-  if (tiles > 0x3FFFFFFF) return cudaErrorInvalidConfiguration;
+// Resident blocks of the FP32 kernel on the current device (cached).
+int64_t f32_slots() {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!g_attr_set[dev]) {
-    e = set_smem_attr<BN, true>();
-    if (e == cudaSuccess) e = set_smem_attr<BN, false>();
-    if (e == cudaSuccess) e = set_smem_attr<BN / 2, true>();
-    if (e == cudaSuccess) e = set_smem_attr<BN / 2, false>();
-    if (e != cudaSuccess) return e;
-    int sms = 0;
+    if (set_smem_attr<true>() != cudaSuccess || set_smem_attr<false>() != cudaSuccess)
+      return 0;
+    int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    g_slots[dev] = sms * f32_blocks_per_sm();
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, gemm_f32_regblock_kernel<true>, THREADS,
+            STAGES * sizeof(F32Stage<BN>)) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    g_slots[dev] = static_cast<int64_t>(sms) * per_sm;
     g_attr_set[dev] = 1;
   }
-  const int64_t slots = g_slots[dev];
-  const int64_t tail = slots > 0 ? tiles % slots : 0;
-  const int64_t split = (tail > 0 && 2 * tail <= slots) ? tail : 0;
-  const int full = static_cast<int>(tiles - split);
+  return g_slots[dev];
+}
+
+F32Plan f32_plan(int M, int N, int K, int64_t slots) {
+  F32Plan p;
+  p.tiles_m = (M + BM - 1) / BM;
+  p.tiles_n = (N + BN - 1) / BN;
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  const int nk = (K + BK - 1) / BK;
+  p.tail = slots > 0 ? static_cast<int>(tiles % slots) : 0;
+  p.full = static_cast<int>(tiles - p.tail);
+  p.split = 1;
+  if (p.tail > 0) {
+    // Split the tiles of the last, partial wave along K so that its blocks
+    // fill the resident slots: choose the split with the lowest estimated
+    // time, rounds x (1/split + a per-round overhead for pipeline fill and
+    // the reduction), keeping at least 4 k-slices per range.
+    double best = 1e30;
+    const int max_split = nk / 4 < 16 ? nk / 4 : 16;
+    for (int s = 1; s <= (max_split > 1 ? max_split : 1); ++s) {
+      const int64_t rounds = (static_cast<int64_t>(p.tail) * s + slots - 1) / slots;
+      const double cost = static_cast<double>(rounds) * (1.0 / s + 0.04);
+      if (cost < best - 1e-9) {
+        best = cost;
+        p.split = s;
+      }
+    }
+  }
+  p.workspace_bytes =
+      p.split > 1 ? static_cast<int64_t>(p.tail) * p.split * BM * BN * 4 : 0;
+  p.counter_bytes = p.split > 1 ? static_cast<int64_t>(p.tail) * 4 : 0;
+  return p;
+}
+
+// Whole waves of tiles first; then the tiles of the last, partial wave,
+// split along K as planned (two launches on the stream).
+cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
+                            const float* B, int64_t ldb, float* C, int64_t ldc,
+                            bool vec_b, bool vec_c, const F32Plan& p, float* ws,
+                            unsigned int* counters, cudaStream_t stream) {
+  if (f32_slots() <= 0) return cudaErrorInvalidDeviceFunction;
   const int vc = vec_c ? 1 : 0;
-  if (full > 0) {
-    e = vec_b ? launch_part<BN, true>(full, M, N, K, A, lda, B, ldb, C, ldc,
-                                      tiles_m, tiles_n, 0, vc, stream)
-              : launch_part<BN, false>(full, M, N, K, A, lda, B, ldb, C, ldc,
-                                       tiles_m, tiles_n, 0, vc, stream);
+  cudaError_t e = cudaSuccess;
+  if (p.full > 0) {
+    e = vec_b ? launch_part<true>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
+                                  p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
+                                  nullptr, stream)
+              : launch_part<false>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
+                                   p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
+                                   nullptr, stream);
     if (e != cudaSuccess) return e;
   }
-  if (split > 0) {
-    const int blocks = static_cast<int>(2 * split);
-    e = vec_b ? launch_part<BN / 2, true>(blocks, M, N, K, A, lda, B, ldb, C,
-                                          ldc, tiles_m, tiles_n, full, vc, stream)
-              : launch_part<BN / 2, false>(blocks, M, N, K, A, lda, B, ldb, C,
-                                           ldc, tiles_m, tiles_n, full, vc, stream);
+  if (p.tail > 0) {
+    const int blocks = p.tail * p.split;
+    e = vec_b ? launch_part<true>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
+                                  p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
+                                  counters, stream)
+              : launch_part<false>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
+                                   p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
+                                   counters, stream);
   }
   return e;
 }

@@ -15,13 +15,25 @@ void note_launches(int n);
 // ---- FP32 SIMT path (gemm_f32.cu)
 constexpr int kF32TileM = 128;
 constexpr int kF32TileN = 128;
-constexpr int kF32TileK = 16;
+constexpr int kF32TileK = 32;
 constexpr int kF32Group = 8;
-constexpr int kF32Stages = 3;
+constexpr int kF32Stages = 2;
 
+// Launch plan: `full` tiles in whole waves, then `tail` tiles split into
+// `split` k-ranges each (split-K; needs workspace_bytes of partials and
+// counter_bytes of zeroed counters).
+struct F32Plan {
+  int tiles_m = 0, tiles_n = 0;
+  int full = 0, tail = 0, split = 1;
+  int64_t workspace_bytes = 0, counter_bytes = 0;
+};
+// Resident blocks of the FP32 kernel on the current device (0: cannot run).
+int64_t f32_slots();
+F32Plan f32_plan(int M, int N, int K, int64_t slots);
 cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             const float* B, int64_t ldb, float* C, int64_t ldc,
-                            bool vec_a, bool vec_b, bool vec_c,
+                            bool vec_b, bool vec_c, const F32Plan& plan,
+                            float* ws, unsigned int* counters,
                             cudaStream_t stream);
 
 // ---- BF16 tensor-core path (gemm_bf16_tc.cu)
