@@ -51,6 +51,7 @@ SIGNATURES = [
     ("gemm_shutdown", None, []),
     ("gemm_abi_version", _i32, []),
     ("gemm_launch_count", ctypes.c_uint64, []),
+    ("gemm_debug_inject", _i32, [_i32, ctypes.c_uint64]),
     ("gemm_tile_order", _i32, [_i64, _i64, _i64, _i64,
                                ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     ("gemm_plan_bf16", _i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
@@ -121,6 +122,11 @@ def gemm_shutdown() -> None:
 
 def gemm_abi_version() -> int:
     return lib().gemm_abi_version()
+
+
+def gemm_debug_inject(mode: int, wait_ns: int) -> int:
+    """Test hook: bounded-wait limit and fault mode (see include/gemm07.h)."""
+    return lib().gemm_debug_inject(mode, wait_ns)
 
 
 def gemm_launch_count() -> int:

@@ -20,8 +20,9 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
 namespace {
 
-// Device-side status word: bit 0 = a bounded wait ran out.
-__device__ unsigned int g_status_word;
+// Device status block: [0] status bits (bit 0: a bounded wait ran out),
+// [1] test fault mode, [2..3] bounded-wait limit in ns (0: default 2 s).
+__device__ unsigned int g_status_word[4];
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 0x7FFFFFFF;  // M, N, K < 2^31
@@ -629,6 +630,23 @@ void gemm_shutdown(void) {
 }
 
 int gemm_abi_version(void) { return 1; }
+
+gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns) {
+  if (mode < 0 || mode > 1) return GEMM_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const gemm_status_t s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  const unsigned int words[3] = {static_cast<unsigned int>(mode),
+                                 static_cast<unsigned int>(wait_ns & 0xFFFFFFFFull),
+                                 static_cast<unsigned int>(wait_ns >> 32)};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(d->status + 1, words, sizeof(words), cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
 
 uint64_t gemm_launch_count(void) { return g_launches.load(); }
 

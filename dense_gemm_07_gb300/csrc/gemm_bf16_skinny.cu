@@ -109,6 +109,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  const uint64_t tmo = wait_limit_ns(status);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -118,7 +119,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
+        if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort, tmo)) {
           raise_abort(abort, status);
           break;
         }
@@ -137,7 +138,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
       volatile int never = 0;
       for (int s = 0; s < STAGES; ++s)
         if (last_phase[s] >= 0 &&
-            !mbar_wait(&ctl->full[s], static_cast<uint32_t>(last_phase[s]), &never))
+            !mbar_wait(&ctl->full[s], static_cast<uint32_t>(last_phase[s]), &never, tmo))
           raise_abort(abort, status);
     }
   } else if (warp == 1) {
@@ -147,7 +148,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t phase = 0;
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+        if (!mbar_wait(&ctl->full[stage], phase, abort, tmo)) {
           ok = false;
           break;
         }
@@ -176,14 +177,14 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
       mma_commit(&ctl->acc_full);
       volatile int never = 0;
       mma_commit(&ctl->drain);
-      if (!mbar_wait(&ctl->drain, 0u, &never)) raise_abort(abort, status);
+      if (!mbar_wait(&ctl->drain, 0u, &never, tmo)) raise_abort(abort, status);
     }
   } else {
     // ------------------------------------------- epilogue: park the partial
     const int q = warp & 3;
     const int n_local = q * 32 + lane;  // TMEM lane = column of the tile
     int ok = 0;
-    if (lane == 0) ok = mbar_wait(&ctl->acc_full, 0u, abort) ? 1 : 0;
+    if (lane == 0) ok = mbar_wait(&ctl->acc_full, 0u, abort, tmo) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok && lane == 0) raise_abort(abort, status);
     tc_fence_after_sync();

@@ -112,6 +112,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  const uint64_t tmo = wait_limit_ns(status);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -124,7 +125,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileCoord tc = tile_order(tile, tiles_m, tiles_n, kTcGroup);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort, tmo)) {
             ok = false;
             break;
           }
@@ -149,7 +150,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int s = 0; s < STAGES; ++s)
         if (last_phase[s] >= 0 &&
             !mbar_wait(&ctl->full[s], static_cast<uint32_t>(last_phase[s]),
-                       &never))
+                       &never, tmo))
           raise_abort(abort, status);
     }
   } else if (warp == 1) {
@@ -163,14 +164,14 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
         const int acc = t & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(t >> 1) & 1u;
-        if (!mbar_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort)) {
+        if (!mbar_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+          if (!mbar_wait(&ctl->full[stage], phase, abort, tmo)) {
             ok = false;
             break;
           }
@@ -203,7 +204,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       if (issued) {
         mma_commit(&ctl->drain);
         volatile int never = 0;
-        if (!mbar_wait(&ctl->drain, 0u, &never)) raise_abort(abort, status);
+        if (!mbar_wait(&ctl->drain, 0u, &never, tmo)) raise_abort(abort, status);
       }
     }
   } else {
@@ -214,7 +215,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const int acc = t & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(t >> 1) & 1u;
       int ok = 0;
-      if (lane == 0) ok = mbar_wait(&ctl->acc_full[acc], acc_phase, abort) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&ctl->acc_full[acc], acc_phase, abort, tmo) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) raise_abort(abort, status);

@@ -104,8 +104,8 @@ __device__ __forceinline__ Unit unit_of(int unit, int num_full, int split,
 }
 
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
-  return mbar_wait(bar, parity, abort);
+                                          volatile int* abort, uint64_t tmo) {
+  return mbar_wait(bar, parity, abort, tmo);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort,
@@ -138,13 +138,20 @@ __device__ __forceinline__ bool produce_unit(const Unit& u, Ring& ring,
                                              const CUtensorMap* tmA,
                                              const CUtensorMap* tmB,
                                              uint32_t rank, int* last_phase,
-                                             volatile int* abort) {
+                                             volatile int* abort, uint64_t tmo,
+                                             bool skip_first) {
   constexpr int BOXES = W / 2 / B_BOX_COLS;
   constexpr uint32_t TX = 2u * (A_STAGE_BYTES + BOXES * B_BOX_BYTES);
   const int a_row = u.m0 + static_cast<int>(rank) * CTA_M;
   const int b_col = u.n0 + static_cast<int>(rank) * (W / 2);
   for (int kb = 0; kb < num_kb; ++kb) {
-    if (!mbar_wait(&ctl->empty[ring.stage], ring.phase ^ 1u, abort)) return false;
+    if (!mbar_wait(&ctl->empty[ring.stage], ring.phase ^ 1u, abort, tmo)) return false;
+    if (skip_first && kb == 0) {
+      // Test fault: this k-slice is never copied, so the MMA's wait for it
+      // runs out and the kernel unwinds with a timeout status.
+      ring.advance();
+      continue;
+    }
     if (rank == 0) {
       mbar_arrive_expect_tx(&ctl->full[ring.stage], TX);
       last_phase[ring.stage] = static_cast<int>(ring.phase);
@@ -167,11 +174,11 @@ template <int W>
 __device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
                                          int num_kb, uint8_t* smem,
                                          PairControl* ctl,
-                                         volatile int* abort) {
+                                         volatile int* abort, uint64_t tmo) {
   constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, W, /*a_mn_major=*/false,
                                             /*b_mn_major=*/true);
   for (int kb = 0; kb < num_kb; ++kb) {
-    if (!mbar_wait(&ctl->full[ring.stage], ring.phase, abort)) return false;
+    if (!mbar_wait(&ctl->full[ring.stage], ring.phase, abort, tmo)) return false;
     tc_fence_after_sync();
     const uint32_t a_addr = smem_u32(smem + ring.stage * STAGE_BYTES);
     const uint32_t b_addr = a_addr + A_STAGE_BYTES;
@@ -307,6 +314,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  const uint64_t tmo = wait_limit_ns(status);
+  const unsigned int fault = status[1];
   const uint32_t peer_abort = map_to_rank(smem_u32(&ctl->abort), rank ^ 1u);
 
   if (warp == 0) {
@@ -318,11 +327,12 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       for (int unit = pair; ok && unit < num_units; unit += num_pairs) {
         const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
+        const bool skip = fault == 1 && unit == pair;
         ok = u.width == BN
                  ? produce_unit<BN>(u, ring, num_kb, smem, ctl, &tmA, &tmB, rank,
-                                    last_phase, abort)
+                                    last_phase, abort, tmo, skip)
                  : produce_unit<BN / 2>(u, ring, num_kb, smem, ctl, &tmA, &tmB,
-                                        rank, last_phase, abort);
+                                        rank, last_phase, abort, tmo, skip);
       }
       if (!ok) raise_abort(abort, peer_abort, status);
       // The even CTA's "full" barriers count both CTAs' copies: every phase
@@ -331,7 +341,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int s = 0; s < STAGES; ++s)
         if (last_phase[s] >= 0 &&
             !mbar_wait(&ctl->full[s], static_cast<uint32_t>(last_phase[s]),
-                       &never))
+                       &never, tmo))
           raise_abort(abort, peer_abort, status);
     }
   } else if (warp == 1) {
@@ -345,15 +355,15 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
         const int acc = t % NUM_ACC;
         const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
-        if (!pair_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort)) {
+        if (!pair_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         issued |= num_kb > 0;
-        ok = u.width == BN ? mma_unit<BN>(d_tmem, ring, num_kb, smem, ctl, abort)
-                           : mma_unit<BN / 2>(d_tmem, ring, num_kb, smem, ctl, abort);
+        ok = u.width == BN ? mma_unit<BN>(d_tmem, ring, num_kb, smem, ctl, abort, tmo)
+                           : mma_unit<BN / 2>(d_tmem, ring, num_kb, smem, ctl, abort, tmo);
         if (!ok) break;
         mma_commit_pair(&ctl->acc_full[acc], 0x3);
       }
@@ -361,7 +371,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       if (issued) {
         mma_commit_pair(&ctl->drain, 0x1);
         volatile int never = 0;
-        if (!mbar_wait(&ctl->drain, 0u, &never))
+        if (!mbar_wait(&ctl->drain, 0u, &never, tmo))
           raise_abort(abort, peer_abort, status);
       }
     }
@@ -375,7 +385,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const int acc = t % NUM_ACC;
       const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
       int ok = 0;
-      if (lane == 0) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort) ? 1 : 0;
+      if (lane == 0) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort, tmo) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) raise_abort(abort, peer_abort, status);

@@ -64,10 +64,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Device status block shared by the kernels (one per device):
+//   [0] status bits (bit 0: a bounded wait ran out), [1] test fault mode,
+//   [2], [3] low / high 32 bits of the bounded-wait limit in ns (0: default).
+__device__ __forceinline__ uint64_t wait_limit_ns(const unsigned int* status) {
+  const uint64_t v = (static_cast<uint64_t>(status[3]) << 32) | status[2];
+  return v ? v : kWaitTimeoutNs;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up (and
-// returns false) when *abort becomes nonzero or after kWaitTimeoutNs.
+// returns false) when *abort becomes nonzero or after limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -75,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 15u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -140,6 +140,11 @@ def test_plan_and_calls_reject_bad_arguments(lib):
     assert _abi.gemm_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == _abi.GEMM_OK
 
 
+def test_debug_hook_rejects_unknown_modes(lib):
+    assert _abi.gemm_debug_inject(7, 0) == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_debug_inject(-1, 0) == _abi.GEMM_ERR_INVALID_ARG
+
+
 def test_no_gpu_means_a_loud_error(lib):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():

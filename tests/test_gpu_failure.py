@@ -1,0 +1,35 @@
+"""Failure detection on the GPU without a fault: every mbarrier wait in the
+tensor-core kernels is bounded.  The test hook makes the paired-SM kernel
+withhold the copy of its first k-slice, so the MMA issuer's wait runs out
+(after a 20 ms limit); the kernel must unwind and return, the host must read
+GEMM_ERR_TIMEOUT from the device status word, and the context must stay
+usable: the next GEMM is correct and the status is clean again."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import _abi, inputs
+from gemm_check import assert_within, oracle_ref
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_runs_out_and_gpu_stays_usable():
+    M, N, K = 512, 768, 640           # paired-SM path, several tiles per pair
+    a, b = inputs.make_pair(M, N, K, 31, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.cuda(), b.cuda()
+    assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    assert _abi.gemm_debug_inject(1, 20_000_000) == _abi.GEMM_OK
+    try:
+        g7.gemm_bf16_f32acc(a_d, b_d)
+        assert g7.gemm_get_device_status() == _abi.GEMM_ERR_TIMEOUT
+        # the status word is cleared by reading it
+        assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    finally:
+        assert _abi.gemm_debug_inject(0, 0) == _abi.GEMM_OK
+    c = g7.gemm_bf16_f32acc(a_d, b_d)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
