@@ -238,7 +238,7 @@ def main():
     import torch.distributed as dist
 
     import dense_gemm_07_gb300 as g7
-    from dense_gemm_07_gb300 import inputs, roofline
+    from dense_gemm_07_gb300 import inputs, replicas, roofline
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -310,13 +310,10 @@ def main():
     ms_bf16 = sum(t_bf16) / len(t_bf16)
     ms_f32 = sum(t_f32) / len(t_f32)
     ms_step = ms_bf16 + ms_f32
-    if world > 1:
-        t = torch.tensor([ms_step, ms_bf16, ms_f32], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_bf16, ms_f32 = (float(x) for x in t.tolist())
+    ms_step, ms_bf16, ms_f32 = replicas.max_over_ranks([ms_step, ms_bf16, ms_f32], dev)
 
     flops_one = roofline.gemm_flops(SIZE, SIZE, SIZE)
-    value = world * 2 * flops_one / (ms_step * 1e-3) / 1e12
+    value = replicas.whole_job_rate(world, 2 * flops_one, ms_step * 1e-3) / 1e12
     tf_bf16 = flops_one / (ms_bf16 * 1e-3) / 1e12
     tf_f32 = flops_one / (ms_f32 * 1e-3) / 1e12
 
@@ -356,13 +353,11 @@ def main():
             g7.gemm_f32_host(h_a32, h_b32, out=h_c32)
         torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = replicas.max_over_ranks([e2e_s], dev)[0]
         h2d = (h_a16.numel() + h_b16.numel()) * 2 + (h_a32.numel() + h_b32.numel()) * 4
         d2h = (h_c16.numel() + h_c32.numel()) * 4
-        e2e = {"value": world * 2 * flops_one / e2e_s / 1e12, "unit": UNIT,
+        e2e = {"value": replicas.whole_job_rate(world, 2 * flops_one, e2e_s) / 1e12,
+               "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3,
                "api": "gemm_bf16_f32acc_host + gemm_f32_host (C ABI, pinned host buffers)"}
