@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-ladder", action="store_true")
     return p.parse_args()
 
 
@@ -178,6 +179,52 @@ def cpu_sample_baseline(rows_each=4096):
             "sample": (f"first {rows_each} of 4096 rows of both step GEMMs "
                        f"(BF16 4096^3 and FP32 4096^3), FP64 triple loop, "
                        f"OpenMP over rows")}
+
+
+def ladder_context(g7, roofline, A32, B32, C32, flush, stream, sms, sm_mhz, hbm_gbs):
+    """The pages' FP32 ladder on this GPU at 4096^3: measured TFLOP/s of each
+    rung beside the per-k-tile model of "GEMM, step by step" (section "Code")
+    evaluated with GB300 rates, and the reconciliation ratio of "A06", section
+    5 (achieved / (intensity x measured HBM bandwidth)) for the naive rung."""
+    import torch
+
+    fp32_peak = roofline.fp32_simt_peak(sms, sm_mhz)
+    smem_bw = roofline.smem_bandwidth(sms, sm_mhz)
+    hbm = hbm_gbs * 1e9
+    models = [
+        ("naive", roofline.TileModel(False, 1, 1, 1, 1, 1, 4)),
+        ("smem_tiled_32", roofline.TileModel(True, 32, 32, 32, 1, 1, 4)),
+        ("register_1d_64x64_8", roofline.TileModel(True, 64, 64, 8, 8, 1, 4)),
+        ("register_2d_128x128_8x8 (gemm_f32)", roofline.TileModel(True, 128, 128, 32, 8, 8, 4)),
+    ]
+    out = []
+    flops = roofline.gemm_flops(SIZE, SIZE, SIZE)
+    for rung, (name, model) in enumerate(models):
+        def call():
+            if rung < 3:
+                g7.gemm_f32_ladder(rung, A32, B32, out=C32)
+            else:
+                g7.gemm_f32(A32, B32, out=C32)
+        call()
+        times = []
+        for _ in range(2):
+            flush.fill_(3.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e-3)
+        t = min(times)
+        glob, _ = roofline.tile_model_bytes(model, SIZE, SIZE, SIZE)
+        mt, bound = roofline.tile_model_time(model, SIZE, SIZE, SIZE, fp32_peak, hbm, smem_bw)
+        entry = {"rung": name, "ms": t * 1e3, "tflops": flops / t / 1e12,
+                 "model_tflops": flops / mt / 1e12, "model_bound": bound,
+                 "flop_per_byte_global": flops / glob}
+        if rung == 0:
+            entry["achieved_over_intensity_x_hbm"] = (flops / t) / (flops / glob * hbm)
+        out.append(entry)
+    return out
 
 
 # ------------------------------------------------------------- reference
@@ -362,6 +409,11 @@ def main():
                "ms_per_step": e2e_s * 1e3,
                "api": "gemm_bf16_f32acc_host + gemm_f32_host (C ABI, pinned host buffers)"}
 
+    ladder = None
+    if rank == 0 and not args.no_ladder:
+        ladder = ladder_context(g7, roofline, A32, B32, C32, flush, stream, sms,
+                                sm_max, hbm)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_sample_baseline()
@@ -384,6 +436,7 @@ def main():
             },
             "roofline": dominant,
             "cpu_baseline": cpu,
+            "ladder_fp32_4096": ladder,
             "e2e": e2e,
             "gpu_launches": launches,
             "wall_ms_per_step": wall / args.steps * 1e3,

@@ -18,7 +18,7 @@ from __future__ import annotations
 from . import _abi as abi
 from ._build import build
 
-__all__ = ["abi", "build", "GemmError", "gemm_f32", "gemm_bf16_f32acc",
+__all__ = ["abi", "build", "GemmError", "gemm_f32", "gemm_bf16_f32acc", "gemm_f32_ladder",
            "gemm_f32_host", "gemm_bf16_f32acc_host", "gemm_get_device_status",
            "gemm_status_string", "plan"]
 
@@ -105,6 +105,19 @@ def gemm_f32(A, B, out=None, stream=None):
 def gemm_bf16_f32acc(A, B, out=None, stream=None):
     """C = A @ B for bfloat16 CUDA tensors; FP32 accumulation and output."""
     return _call("gemm_bf16_f32acc", _torch().bfloat16, A, B, out, stream, "cuda")
+
+
+def gemm_f32_ladder(rung, A, B, out=None, stream=None):
+    """C = A @ B with teaching rung 0, 1 or 2 (FP32, for measurement)."""
+    torch = _torch()
+    M, N, K, out = _operands(A, B, torch.float32, out, "cuda")
+    with torch.cuda.device(A.device):
+        s = abi.gemm_f32_ladder(int(rung), M, N, K, _ptr(A), _ld(A, "A"), _ptr(B),
+                                _ld(B, "B"), _ptr(out), _ld(out, "out"),
+                                _stream_handle(stream, A.device))
+    if s != abi.GEMM_OK:
+        raise GemmError(s, "gemm_f32_ladder")
+    return out
 
 
 def gemm_f32_host(A, B, out=None, stream=None):

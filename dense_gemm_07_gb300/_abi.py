@@ -45,6 +45,7 @@ SIGNATURES = [
     ("gemm_bf16_f32acc", _i32, _GEMM_ARGS),
     ("gemm_bf16_f32acc_noalloc", _i32, _GEMM_ARGS),
     ("gemm_f32_host", _i32, _GEMM_ARGS),
+    ("gemm_f32_ladder", _i32, [_i32] + _GEMM_ARGS),
     ("gemm_bf16_f32acc_host", _i32, _GEMM_ARGS),
     ("gemm_status_string", ctypes.c_char_p, [_i32]),
     ("gemm_get_device_status", _i32, [_vp]),
@@ -98,6 +99,11 @@ def gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream):
 def gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream):
     """gemm_bf16_f32acc without any device allocation (fixed scratch)."""
     return lib().gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f32_ladder(rung, M, N, K, A, lda, B, ldb, C, ldc, stream):
+    """Teaching rung 0 (naive), 1 (smem-tiled) or 2 (1-D register tiles)."""
+    return lib().gemm_f32_ladder(rung, M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, stream):

@@ -563,6 +563,26 @@ gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K,
                           static_cast<cudaStream_t>(stream));
 }
 
+gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
+                              const float* A, int64_t lda, const float* B,
+                              int64_t ldb, float* C, int64_t ldc, void* stream) {
+  if (rung < 0 || rung > 2) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (s != GEMM_OK || M == 0 || N == 0) return s;
+  // grid.y of the rungs is M / 8 at most rows per block: keep it in range
+  if (M > 65535LL * 8) return GEMM_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  s = device_state(&d);
+  if (s != GEMM_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0)
+    return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
+                                          static_cast<int>(N), st));
+  return from_cuda(launch_gemm_f32_ladder(rung, static_cast<int>(M),
+                                          static_cast<int>(N), static_cast<int>(K),
+                                          A, lda, B, ldb, C, ldc, st));
+}
+
 gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
                             int64_t lda, const float* B, int64_t ldb, float* C,
                             int64_t ldc, void* stream) {

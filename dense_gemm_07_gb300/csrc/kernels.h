@@ -83,6 +83,12 @@ cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,
                                     int64_t ldc, int M, int N, int K, int cs,
                                     unsigned int* status, cudaStream_t stream);
 
+// ---- FP32 teaching rungs (gemm_f32_ladder.cu): 0 naive, 1 smem-tiled,
+// 2 one-dimensional register tiling.
+cudaError_t launch_gemm_f32_ladder(int rung, int M, int N, int K, const float* A,
+                                   int64_t lda, const float* B, int64_t ldb,
+                                   float* C, int64_t ldc, cudaStream_t stream);
+
 // ---- small helpers (gemm_aux.cu)
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
                                  cudaStream_t stream);

@@ -133,6 +133,23 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t 
                                         float *C, int64_t ldc, void *stream);
 
 /*
+ * gemm_f32_ladder -- the teaching rungs that lead up to gemm_f32, for
+ * measuring the ladder of the pages on this GPU (not a production path):
+ *   rung 0: one thread per output, coalesced mapping ("How a Matrix Multiply
+ *           Runs on a GPU", "Level 0"), 0.25 FLOP/byte;
+ *   rung 1: 32 x 32 shared-memory tiles, two barriers per tile, zero-filled
+ *           edges ("Level 1"; "A06", section 3), 8 FLOP/byte;
+ *   rung 2: one-dimensional register tiling, 8 outputs per thread in one
+ *           column ("GEMM" (inference-book), 1D register tiling).
+ * Same operands, conventions and errors as gemm_f32; rung outside 0..2 or
+ * M > 524280 returns GEMM_ERR_INVALID_ARG.
+ */
+GEMM07_API gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
+                              const float *A, int64_t lda,
+                              const float *B, int64_t ldb,
+                              float *C, int64_t ldc, void *stream);
+
+/*
  * Host-buffer variants: the same operations with A, B and C in HOST memory
  * (pinned memory gives the fastest copies; pageable memory works).  The
  * call copies A and B to device staging buffers on `stream`, runs the GEMM,

@@ -140,6 +140,13 @@ def test_plan_and_calls_reject_bad_arguments(lib):
     assert _abi.gemm_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == _abi.GEMM_OK
 
 
+def test_ladder_rejects_bad_rungs(lib):
+    assert _abi.gemm_f32_ladder(3, 4, 4, 4, 16, 4, 16, 4, 16, 4, None) == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_f32_ladder(-1, 4, 4, 4, 16, 4, 16, 4, 16, 4, None) == _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_f32_ladder(0, 600000, 4, 4, 16, 4, 16, 4, 16, 4, None) == \
+        _abi.GEMM_ERR_INVALID_ARG
+
+
 def test_debug_hook_rejects_unknown_modes(lib):
     assert _abi.gemm_debug_inject(7, 0) == _abi.GEMM_ERR_INVALID_ARG
     assert _abi.gemm_debug_inject(-1, 0) == _abi.GEMM_ERR_INVALID_ARG

@@ -84,6 +84,26 @@ def test_f32_4096_sampled_rows():
     _check("f32", M, N, K, 1, inputs.UNIFORM, rows=_sample_rows(M, 48, 1))
 
 
+@pytest.mark.parametrize("rung", [0, 1, 2])
+@pytest.mark.parametrize("shape", [(256, 256, 256), (1000, 700, 1000), (65, 129, 33)])
+def test_f32_ladder_rungs_exact(rung, shape):
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 20, inputs.INT4, dtype=torch.float32)
+    c = g7.gemm_f32_ladder(rung, a.to(DEV), b.to(DEV))
+    torch.cuda.synchronize()
+    c_ref, _ = oracle_ref("f32", a, b, with_abs=False)
+    assert_within("f32", c.cpu().numpy(), c_ref, None, exact=True, what=f"rung {rung}")
+
+
+def test_f32_ladder_rung_uniform():
+    a, b = inputs.make_pair(300, 200, 500, 21, inputs.UNIFORM, dtype=torch.float32)
+    for rung in range(3):
+        c = g7.gemm_f32_ladder(rung, a.to(DEV), b.to(DEV))
+        torch.cuda.synchronize()
+        c_ref, s_ref = oracle_ref("f32", a, b)
+        assert_within("f32", c.cpu().numpy(), c_ref, s_ref, what=f"rung {rung}")
+
+
 # --------------------------------------------------- BF16 (tensor cores)
 
 def test_bf16_256_normal():
