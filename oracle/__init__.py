@@ -73,6 +73,10 @@ def _load():
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_gemm_flops.restype = ctypes.c_double
             lib.oracle_gemm_flops.argtypes = [i64, i64, i64]
+            lib.oracle_gemm_epilogue.restype = ctypes.c_int
+            lib.oracle_gemm_epilogue.argtypes = [i64, i64, vp, i64, ctypes.c_double,
+                                                 ctypes.c_double, vp, i64, vp,
+                                                 ctypes.c_int, vp, i64]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -124,6 +128,32 @@ def gemm_bf16(A_bits: np.ndarray, B_bits: np.ndarray, with_abs: bool = False):
     if A_bits.dtype != np.uint16 or B_bits.dtype != np.uint16:
         raise TypeError("oracle.gemm_bf16 takes uint16 (BF16 bit) arrays")
     return _gemm("oracle_gemm_bf16", A_bits, B_bits, with_abs)
+
+
+def gemm_epilogue(AB: np.ndarray, alpha: float = 1.0, beta: float = 0.0,
+                  C0: np.ndarray | None = None, bias: np.ndarray | None = None,
+                  act: int = 0) -> np.ndarray:
+    """act(alpha * AB + beta * C0 + bias) in double; AB from gemm_f32/gemm_bf16.
+
+    C0 (FP32, M x N) None means C is not read; bias (FP32, N) None means no
+    bias; act 0 = identity, 1 = ReLU.
+    """
+    lib = _load()
+    AB = np.ascontiguousarray(AB, dtype=np.float64)
+    M, N = AB.shape
+    c0 = None if C0 is None else np.ascontiguousarray(C0, dtype=np.float32)
+    bs = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if c0 is not None and c0.shape != (M, N):
+        raise ValueError("oracle: C0 must be M x N")
+    if bs is not None and bs.shape != (N,):
+        raise ValueError("oracle: bias must have N elements")
+    out = np.zeros((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_epilogue(M, N, _ptr(AB), max(N, 1), float(alpha), float(beta),
+                                  _ptr(c0), max(N, 1), _ptr(bs), int(act), _ptr(out),
+                                  max(N, 1))
+    if rc != 0:
+        raise ValueError("oracle: gemm_epilogue rejected its arguments")
+    return out
 
 
 def bf16_to_double(bits: int) -> float:

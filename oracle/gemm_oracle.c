@@ -112,6 +112,36 @@ int oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
     return 0;
 }
 
+/*
+ * The epilogue step of the register-tiled kernel's pseudocode ("How a Matrix
+ * Multiply Runs on a GPU", "Level 2": the output is alpha * acc + beta * C,
+ * plus a bias and an activation) applied to an exact product:
+ *   out[i][j] = act(alpha * AB[i][j] + beta * C0[i][j] + bias[j])
+ * in double.  AB is the oracle's product (ld_ab), C0 the prior contents of
+ * C as FP32 (NULL: treated as zero, i.e. not read), bias N floats or NULL,
+ * act 0 = identity, 1 = max(x, 0).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemm_epilogue(int64_t M, int64_t N, const double *AB, int64_t ld_ab,
+                         double alpha, double beta, const float *C0,
+                         int64_t ld_c0, const float *bias, int act, double *out,
+                         int64_t ld_out)
+{
+    if (M < 0 || N < 0 || act < 0 || act > 1) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (AB == NULL || out == NULL || ld_ab < N || ld_out < N) return -1;
+    if (C0 != NULL && ld_c0 < N) return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double v = alpha * AB[i * ld_ab + j];
+            if (C0 != NULL) v += beta * (double)C0[i * ld_c0 + j];
+            if (bias != NULL) v += (double)bias[j];
+            if (act == 1 && v < 0.0) v = 0.0;
+            out[i * ld_out + j] = v;
+        }
+    }
+    return 0;
+}
+
 /* Floating-point operation count of one GEMM: one multiply and one add per
  * (i, j, k), i.e. 2*M*N*K ("A06 -- Tiled Matrix Multiply (GEMM)", section 6,
  * Pitfall 4; "How a Matrix Multiply Runs on a GPU", "The problem and the

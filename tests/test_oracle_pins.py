@@ -298,3 +298,51 @@ def test_pins_accept_exact_numpy():
     # the plain float64 product (a library routine) passes every pin
     for pin in PINS:
         assert pin(_np_gemm), pin.__name__
+
+
+# ------------------------------------------------------------ epilogue pins
+
+def _ab_int(oracle_mod, seed=40, M=7, N=9, K=5):
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    return A, B, oracle_mod.gemm_f32(A, B)
+
+
+def test_epilogue_identity_is_the_product(oracle_mod):
+    _, _, AB = _ab_int(oracle_mod)
+    assert np.array_equal(oracle_mod.gemm_epilogue(AB), AB)
+
+
+def test_epilogue_closed_form_by_hand(oracle_mod):
+    A, B, AB = _ab_int(oracle_mod)
+    rng = np.random.default_rng(41)
+    C0 = rng.integers(-5, 6, AB.shape).astype(np.float32)
+    bias = rng.integers(-4, 5, AB.shape[1]).astype(np.float32)
+    out = oracle_mod.gemm_epilogue(AB, alpha=2.0, beta=-3.0, C0=C0, bias=bias)
+    for i in range(AB.shape[0]):
+        for j in range(AB.shape[1]):
+            # alpha * sum_k a_ik b_kj + beta * c_ij + bias_j, exact in integers
+            want = 2 * sum(int(A[i, k]) * int(B[k, j]) for k in range(A.shape[1])) \
+                - 3 * int(C0[i, j]) + int(bias[j])
+            assert out[i, j] == want
+    relu = oracle_mod.gemm_epilogue(AB, alpha=2.0, beta=-3.0, C0=C0, bias=bias, act=1)
+    assert np.array_equal(relu, np.maximum(out, 0.0))
+    assert np.any(out < 0) and np.all(relu >= 0)
+
+
+def test_epilogue_beta_without_c_and_zero_product(oracle_mod):
+    AB = np.zeros((3, 4))
+    C0 = np.arange(12, dtype=np.float32).reshape(3, 4)
+    assert np.array_equal(oracle_mod.gemm_epilogue(AB, beta=0.5, C0=C0), 0.5 * C0)
+    # C0 None: C is not read, whatever beta is
+    assert np.array_equal(oracle_mod.gemm_epilogue(AB, beta=7.0), AB)
+    bias = np.array([1, -2, 3, -4], dtype=np.float32)
+    assert np.array_equal(oracle_mod.gemm_epilogue(AB, bias=bias), np.tile(bias, (3, 1)))
+
+
+def test_epilogue_rejects_bad_arguments(oracle_mod):
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_epilogue(np.zeros((2, 3)), act=2)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_epilogue(np.zeros((2, 3)), bias=np.zeros(2, np.float32))
