@@ -19,6 +19,7 @@ from . import _abi as abi
 from ._build import build
 
 __all__ = ["abi", "build", "GemmError", "gemm_f32", "gemm_bf16_f32acc", "gemm_f32_ladder",
+           "gemm_f32_ex", "gemm_bf16_f32acc_ex",
            "gemm_f32_host", "gemm_bf16_f32acc_host", "gemm_get_device_status",
            "gemm_status_string", "plan"]
 
@@ -105,6 +106,45 @@ def gemm_f32(A, B, out=None, stream=None):
 def gemm_bf16_f32acc(A, B, out=None, stream=None):
     """C = A @ B for bfloat16 CUDA tensors; FP32 accumulation and output."""
     return _call("gemm_bf16_f32acc", _torch().bfloat16, A, B, out, stream, "cuda")
+
+
+def _gemm_ex(fn_name, dtype, A, B, out, alpha, beta, bias, activation, stream):
+    torch = _torch()
+    if beta != 0.0 and out is None:
+        raise ValueError("beta != 0 reads C: pass its prior contents as `out`")
+    M, N, K, out = _operands(A, B, dtype, out, "cuda")
+    acts = {"none": abi.ACT_NONE, "relu": abi.ACT_RELU}
+    if activation not in acts:
+        raise ValueError(f"activation must be one of {sorted(acts)}")
+    if bias is not None:
+        if bias.shape != (N,) or bias.dtype != torch.float32 or bias.device != A.device \
+                or (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous float32 vector of N elements "
+                             "on A's device")
+    epi = abi.GemmEpilogue(float(alpha), float(beta),
+                           bias.data_ptr() if bias is not None and bias.numel() else None,
+                           acts[activation])
+    with torch.cuda.device(A.device):
+        s = getattr(abi, fn_name)(M, N, K, _ptr(A), _ld(A, "A"), _ptr(B), _ld(B, "B"),
+                                  _ptr(out), _ld(out, "out"), epi,
+                                  _stream_handle(stream, A.device))
+    if s != abi.GEMM_OK:
+        raise GemmError(s, fn_name)
+    return out
+
+
+def gemm_f32_ex(A, B, out=None, alpha=1.0, beta=0.0, bias=None, activation="none",
+                stream=None):
+    """C = act(alpha * A @ B + beta * C + bias) for float32 CUDA tensors."""
+    return _gemm_ex("gemm_f32_ex", _torch().float32, A, B, out, alpha, beta, bias,
+                    activation, stream)
+
+
+def gemm_bf16_f32acc_ex(A, B, out=None, alpha=1.0, beta=0.0, bias=None,
+                        activation="none", stream=None):
+    """C = act(alpha * A @ B + beta * C + bias) for bfloat16 A, B; FP32 C."""
+    return _gemm_ex("gemm_bf16_f32acc_ex", _torch().bfloat16, A, B, out, alpha, beta,
+                    bias, activation, stream)
 
 
 def gemm_f32_ladder(rung, A, B, out=None, stream=None):

@@ -37,6 +37,15 @@ class GemmPlan(ctypes.Structure):
                 ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32)]
 
 
+class GemmEpilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("bias", ctypes.c_void_p), ("activation", ctypes.c_int32)]
+
+
+ACT_NONE = 0
+ACT_RELU = 1
+
+
 # (name, restype, argtypes)
 _i64, _vp, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 _GEMM_ARGS = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -44,6 +53,8 @@ SIGNATURES = [
     ("gemm_f32", _i32, _GEMM_ARGS),
     ("gemm_bf16_f32acc", _i32, _GEMM_ARGS),
     ("gemm_bf16_f32acc_noalloc", _i32, _GEMM_ARGS),
+    ("gemm_f32_ex", _i32, _GEMM_ARGS[:-1] + [ctypes.POINTER(GemmEpilogue), _vp]),
+    ("gemm_bf16_f32acc_ex", _i32, _GEMM_ARGS[:-1] + [ctypes.POINTER(GemmEpilogue), _vp]),
     ("gemm_f32_host", _i32, _GEMM_ARGS),
     ("gemm_f32_ladder", _i32, [_i32] + _GEMM_ARGS),
     ("gemm_bf16_f32acc_host", _i32, _GEMM_ARGS),
@@ -94,6 +105,21 @@ def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream):
 
 def gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream):
     return lib().gemm_bf16_f32acc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def _epi(epilogue):
+    return None if epilogue is None else ctypes.byref(epilogue)
+
+
+def gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, epilogue, stream):
+    """gemm_f32 with a fused epilogue (GemmEpilogue or None)."""
+    return lib().gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, _epi(epilogue), stream)
+
+
+def gemm_bf16_f32acc_ex(M, N, K, A, lda, B, ldb, C, ldc, epilogue, stream):
+    """gemm_bf16_f32acc with a fused epilogue (GemmEpilogue or None)."""
+    return lib().gemm_bf16_f32acc_ex(M, N, K, A, lda, B, ldb, C, ldc, _epi(epilogue),
+                                     stream)
 
 
 def gemm_bf16_f32acc_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream):

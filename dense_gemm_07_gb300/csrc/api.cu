@@ -140,6 +140,19 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   return GEMM_OK;
 }
 
+// The caller's epilogue description as kernel parameters (NULL: identity).
+gemm_status_t to_epi(const gemm_epilogue_t* e, EpiParams* out) {
+  *out = epi_identity();
+  if (e == nullptr) return GEMM_OK;
+  if (e->activation != GEMM_ACT_NONE && e->activation != GEMM_ACT_RELU)
+    return GEMM_ERR_INVALID_ARG;
+  out->alpha = e->alpha;
+  out->beta = e->beta;
+  out->bias = e->bias;
+  out->act = e->activation;
+  return GEMM_OK;
+}
+
 gemm_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return GEMM_OK;
   if (e == cudaErrorMemoryAllocation) return GEMM_ERR_NO_MEMORY;
@@ -277,7 +290,8 @@ void pool_free(void* p, cudaStream_t stream) {
 
 gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
                       int64_t lda, const float* B, int64_t ldb, float* C,
-                      int64_t ldc, cudaStream_t stream) {
+                      int64_t ldc, cudaStream_t stream,
+                      const EpiParams& epi = epi_identity()) {
   gemm_plan_t plan;
   gemm_status_t s = plan_f32(M, N, K, A, lda, B, ldb, C, ldc, &plan);
   if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
@@ -286,7 +300,7 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   if (s != GEMM_OK) return s;
   if (plan.path == GEMM_PATH_ZERO_FILL)
     return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
-                                          static_cast<int>(N), stream));
+                                          static_cast<int>(N), epi, stream));
   const bool vec_b = aligned16(B) && ldb % 4 == 0;
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   const int m = static_cast<int>(M), n = static_cast<int>(N),
@@ -307,14 +321,15 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   }
   if (s == GEMM_OK)
     s = from_cuda(launch_gemm_f32(m, n, k, A, lda, B, ldb, C, ldc, vec_b, vec_c,
-                                  fp, partials, counters, stream));
+                                  fp, partials, counters, epi, stream));
   pool_free(ws, stream);
   return s;
 }
 
 gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                        int64_t lda, const uint16_t* B, int64_t ldb, float* C,
-                       int64_t ldc, cudaStream_t stream) {
+                       int64_t ldc, cudaStream_t stream,
+                       const EpiParams& epi = epi_identity()) {
   gemm_plan_t plan;
   gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan);
   if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
@@ -323,7 +338,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (s != GEMM_OK) return s;
   if (plan.path == GEMM_PATH_ZERO_FILL)
     return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
-                                          static_cast<int>(N), stream));
+                                          static_cast<int>(N), epi, stream));
 
   const int m = static_cast<int>(M), n = static_cast<int>(N),
             k = static_cast<int>(K);
@@ -356,7 +371,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (s == GEMM_OK && skinny) {
     s = from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                           skinny_split(n, k, d->sms), d->status,
-                                          stream));
+                                          epi, stream));
   } else if (s == GEMM_OK) {
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
     const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
@@ -365,13 +380,13 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
       const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
       s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
                                           ldc, m, n, k, vec_c, max_pairs,
-                                          d->status, stream));
+                                          d->status, epi, stream));
     } else {
       const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
                             ((N + kTcTileN - 1) / kTcTileN);
       const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
       s = from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
-                                        d->status, stream));
+                                        d->status, epi, stream));
     }
   }
   pool_free(ws, stream);
@@ -484,7 +499,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   if (s != GEMM_OK) return s;
   if (plan.path == GEMM_PATH_ZERO_FILL)
     return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
-                                          static_cast<int>(N), stream));
+                                          static_cast<int>(N), epi_identity(), stream));
   const int m = static_cast<int>(M), n = static_cast<int>(N),
             k = static_cast<int>(K);
   // Same layout as the pooled path: packed A first, then packed B, each
@@ -516,7 +531,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   if (skinny)
     return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                              skinny_split(n, k, d->sms),
-                                             d->status, stream));
+                                             d->status, epi_identity(), stream));
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (max_pairs > 0) {
@@ -524,13 +539,13 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
     const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
     return from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
                                            ldc, m, n, k, vec_c, max_pairs,
-                                           d->status, stream));
+                                           d->status, epi_identity(), stream));
   }
   const int64_t tiles =
       ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
   const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
   return from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
-                                       d->status, stream));
+                                       d->status, epi_identity(), stream));
 }
 
 }  // namespace
@@ -555,6 +570,29 @@ gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
                   static_cast<cudaStream_t>(stream));
 }
 
+gemm_status_t gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float* C,
+                          int64_t ldc, const gemm_epilogue_t* epilogue,
+                          void* stream) {
+  EpiParams epi;
+  const gemm_status_t s = to_epi(epilogue, &epi);
+  if (s != GEMM_OK) return s;
+  return run_f32(M, N, K, A, lda, B, ldb, C, ldc,
+                 static_cast<cudaStream_t>(stream), epi);
+}
+
+gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K,
+                                  const uint16_t* A, int64_t lda,
+                                  const uint16_t* B, int64_t ldb, float* C,
+                                  int64_t ldc, const gemm_epilogue_t* epilogue,
+                                  void* stream) {
+  EpiParams epi;
+  const gemm_status_t s = to_epi(epilogue, &epi);
+  if (s != GEMM_OK) return s;
+  return run_bf16(M, N, K, A, lda, B, ldb, C, ldc,
+                  static_cast<cudaStream_t>(stream), epi);
+}
+
 gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t K,
                                         const uint16_t* A, int64_t lda,
                                         const uint16_t* B, int64_t ldb,
@@ -577,7 +615,7 @@ gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0)
     return from_cuda(launch_zero_fill_f32(C, ldc, static_cast<int>(M),
-                                          static_cast<int>(N), st));
+                                          static_cast<int>(N), epi_identity(), st));
   return from_cuda(launch_gemm_f32_ladder(rung, static_cast<int>(M),
                                           static_cast<int>(N), static_cast<int>(K),
                                           A, lda, B, ldb, C, ldc, st));
@@ -586,16 +624,24 @@ gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
 gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
                             int64_t lda, const float* B, int64_t ldb, float* C,
                             int64_t ldc, void* stream) {
-  return run_host<float>(M, N, K, A, lda, B, ldb, C, ldc,
-                         static_cast<cudaStream_t>(stream), run_f32);
+  return run_host<float>(
+      M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
+      [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la,
+         const float* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
+        return run_f32(m, n, k, a, la, b, lb, c, lc, st);
+      });
 }
 
 gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
                                     const uint16_t* A, int64_t lda,
                                     const uint16_t* B, int64_t ldb, float* C,
                                     int64_t ldc, void* stream) {
-  return run_host<uint16_t>(M, N, K, A, lda, B, ldb, C, ldc,
-                            static_cast<cudaStream_t>(stream), run_bf16);
+  return run_host<uint16_t>(
+      M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
+      [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
+         const uint16_t* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
+        return run_bf16(m, n, k, a, la, b, lb, c, lc, st);
+      });
 }
 
 const char* gemm_status_string(gemm_status_t status) {

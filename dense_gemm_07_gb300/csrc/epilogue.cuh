@@ -1,0 +1,32 @@
+// epilogue.cuh -- the fused output step of every kernel:
+//   C := act(alpha * (A*B) + beta * C + bias[col])
+// ("How a Matrix Multiply Runs on a GPU", "Level 2" pseudocode: the output is
+// alpha * acc + beta * C, plus a bias and an activation, applied while the
+// accumulators are still in registers).  With alpha = 1, beta = 0, no bias
+// and no activation the value is the accumulator itself, bit for bit, and C
+// is not read.
+#pragma once
+
+#include <cstdint>
+
+namespace g07 {
+
+struct EpiParams {
+  float alpha;
+  float beta;          // 0: the prior contents of C are not read
+  const float* bias;   // N floats (device) or nullptr
+  int act;             // 0 identity, 1 ReLU
+};
+
+inline EpiParams epi_identity() { return EpiParams{1.0f, 0.0f, nullptr, 0}; }
+
+__device__ __forceinline__ float epi_apply(const EpiParams& e, float acc,
+                                           float c_old, float bias) {
+  float v = e.alpha * acc;
+  if (e.beta != 0.0f) v = fmaf(e.beta, c_old, v);
+  if (e.bias != nullptr) v += bias;
+  if (e.act == 1) v = fmaxf(v, 0.0f);
+  return v;
+}
+
+}  // namespace g07

@@ -1,5 +1,6 @@
 // gemm_aux.cu -- the small memory-bound kernels around the GEMMs:
-//   * zero fill of C for K == 0 (the empty sum);
+//   * C for K == 0 (the empty sum): zeros, or act(beta * C + bias) when an
+//     epilogue is given;
 //   * a row copy of a 16-bit matrix into a buffer with a different row
 //     stride, used to give the tensor-memory accelerator an operand whose
 //     base is 16-byte aligned and whose row stride is a multiple of 16 bytes.
@@ -13,13 +14,15 @@ namespace g07 {
 namespace {
 
 __global__ void zero_fill_f32_kernel(float* __restrict__ C, int64_t ldc, int M,
-                                     int N) {
+                                     int N, EpiParams epi) {
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
        i < total; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / N;
     const int64_t c = i - r * N;
-    C[r * ldc + c] = 0.0f;
+    float* p = C + r * ldc + c;
+    *p = epi_apply(epi, 0.0f, epi.beta != 0.0f ? *p : 0.0f,
+                   epi.bias ? epi.bias[c] : 0.0f);
   }
 }
 
@@ -47,10 +50,10 @@ int grid_for(int64_t total, int threads) {
 }  // namespace
 
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
-                                 cudaStream_t stream) {
+                                 const EpiParams& epi, cudaStream_t stream) {
   const int threads = 256;
   zero_fill_f32_kernel<<<grid_for(static_cast<int64_t>(M) * N, threads),
-                         threads, 0, stream>>>(C, ldc, M, N);
+                         threads, 0, stream>>>(C, ldc, M, N, epi);
   note_launches(1);
   return cudaGetLastError();
 }

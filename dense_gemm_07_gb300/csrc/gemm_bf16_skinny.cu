@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         float* __restrict__ C, int64_t ldc, int M, int N,
-                        int K, int cs, unsigned int* __restrict__ status) {
+                        int K, int cs, unsigned int* __restrict__ status,
+                        EpiParams epi) {
   using S = SkinnyShape<NM>;
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC =
@@ -234,7 +235,11 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
         for (int q = 1; q < 8; ++q)
           if (q < cs) sum += v[i][q];
-        if (m < rows && n < N) C[static_cast<int64_t>(m) * ldc + n] = sum;
+        if (m < rows && n < N) {
+          float* p = C + static_cast<int64_t>(m) * ldc + n;
+          *p = epi_apply(epi, sum, epi.beta != 0.0f ? *p : 0.0f,
+                         epi.bias ? epi.bias[n] : 0.0f);
+        }
       }
     }
   }
@@ -254,8 +259,8 @@ int g_attr_done[64][4];
 template <int NM>
 cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
                       int64_t ldc, int M, int N, int K, int cs,
-                      unsigned int* status, cudaStream_t stream, int dev,
-                      int slot) {
+                      unsigned int* status, const EpiParams& epi,
+                      cudaStream_t stream, int dev, int slot) {
   using S = SkinnyShape<NM>;
   const size_t smem = 1024 + static_cast<size_t>(S::STAGES) * S::STAGE_BYTES +
                       sizeof(SkinnyControl<S::STAGES>);
@@ -283,7 +288,7 @@ cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel<NM>, tmA,
-                                           tmB, C, ldc, M, N, K, cs, status);
+                                           tmB, C, ldc, M, N, K, cs, status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
@@ -304,20 +309,21 @@ int skinny_split(int N, int K, int sms) {
 cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,
                                     const CUtensorMap& tmB, float* C,
                                     int64_t ldc, int M, int N, int K, int cs,
-                                    unsigned int* status, cudaStream_t stream) {
+                                    unsigned int* status, const EpiParams& epi,
+                                    cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   switch (skinny_rows(M)) {
     case 16:
-      return launch_nm<16>(tmA, tmB, C, ldc, M, N, K, cs, status, stream, dev, 0);
+      return launch_nm<16>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 0);
     case 32:
-      return launch_nm<32>(tmA, tmB, C, ldc, M, N, K, cs, status, stream, dev, 1);
+      return launch_nm<32>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 1);
     case 64:
-      return launch_nm<64>(tmA, tmB, C, ldc, M, N, K, cs, status, stream, dev, 2);
+      return launch_nm<64>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 2);
     default:
-      return launch_nm<128>(tmA, tmB, C, ldc, M, N, K, cs, status, stream, dev, 3);
+      return launch_nm<128>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 3);
   }
 }
 

@@ -77,7 +77,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     float* __restrict__ C, int64_t ldc, int M, int N, int K,
                     int tiles_m, int tiles_n, int vec_c,
-                    unsigned int* __restrict__ status) {
+                    unsigned int* __restrict__ status, EpiParams epi) {
   extern __shared__ uint8_t smem_raw[];
   // The swizzle atoms must start on 1024-byte boundaries.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -234,18 +234,12 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         tmem_ld_wait();
         const int gn = tc.n * BN + c * 32;
         if (row < M) {
-          if (vec_c && gn + 31 < N) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(crow + gn + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]),
-                              __uint_as_float(r[j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gn + j < N) crow[gn + j] = __uint_as_float(r[j]);
-          }
+          for (int j = 0; j < 32; ++j)
+            if (gn + j < N)
+              crow[gn + j] = epi_apply(epi, __uint_as_float(r[j]),
+                                       epi.beta != 0.0f ? crow[gn + j] : 0.0f,
+                                       epi.bias ? epi.bias[gn + j] : 0.0f);
         }
       }
       tc_fence_before_sync();
@@ -273,7 +267,7 @@ size_t tc_smem_bytes() {
 cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 float* C, int64_t ldc, int M, int N, int K,
                                 bool vec_c, int grid, unsigned int* status,
-                                cudaStream_t stream) {
+                                const EpiParams& epi, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -288,7 +282,7 @@ cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
   gemm_bf16_tc_kernel<<<grid, THREADS, smem, stream>>>(
-      tmA, tmB, C, ldc, M, N, K, tiles_m, tiles_n, vec_c ? 1 : 0, status);
+      tmA, tmB, C, ldc, M, N, K, tiles_m, tiles_n, vec_c ? 1 : 0, status, epi);
   note_launches(1);
   return cudaGetLastError();
 }

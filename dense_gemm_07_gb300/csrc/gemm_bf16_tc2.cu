@@ -202,7 +202,8 @@ __device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
 template <int W>
 __device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
                                            int64_t ldc, int row, int n0, int M,
-                                           int N, int vec_c) {
+                                           int N, int vec_c,
+                                           const EpiParams& epi) {
   float* crow = C + static_cast<int64_t>(row) * ldc;
 #pragma unroll 1
   for (int c = 0; c < W / 32; ++c) {
@@ -213,14 +214,24 @@ __device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
     if (row < M) {
       if (vec_c && gn + 31 < N) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(crow + gn + j) =
-              make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        for (int j = 0; j < 32; j += 4) {
+          float4 old = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (epi.beta != 0.0f) old = *reinterpret_cast<const float4*>(crow + gn + j);
+          const float o[4] = {old.x, old.y, old.z, old.w};
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = epi_apply(epi, __uint_as_float(r[j + e]), o[e],
+                             epi.bias ? epi.bias[gn + j + e] : 0.0f);
+          *reinterpret_cast<float4*>(crow + gn + j) = make_float4(v[0], v[1], v[2], v[3]);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (gn + j < N) crow[gn + j] = __uint_as_float(r[j]);
+          if (gn + j < N)
+            crow[gn + j] = epi_apply(epi, __uint_as_float(r[j]),
+                                     epi.beta != 0.0f ? crow[gn + j] : 0.0f,
+                                     epi.bias ? epi.bias[gn + j] : 0.0f);
       }
     }
   }
@@ -236,7 +247,9 @@ __device__ __forceinline__ void store_unit_tma(uint32_t taddr,
                                                const CUtensorMap* tmC,
                                                uint8_t* ebuf, int row0, int n0,
                                                int M, int N, int lane,
-                                               int& chunk) {
+                                               int& chunk, const float* C,
+                                               int64_t ldc,
+                                               const EpiParams& epi) {
 #pragma unroll 1
   for (int c = 0; c < W / 32; ++c) {
     // Boxes wholly outside C are skipped (warp-uniform test); every other
@@ -249,6 +262,27 @@ __device__ __forceinline__ void store_unit_tma(uint32_t taddr,
     if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
     __syncwarp();
     tmem_ld_wait();
+    if (epi.alpha != 1.0f || epi.beta != 0.0f || epi.bias != nullptr || epi.act != 0) {
+      // Fused epilogue on this lane's row (N % 4 == 0 on this path, so each
+      // 16-byte group is wholly inside or outside C).
+      const int row = row0 + lane;
+      const int gn = n0 + c * 32;
+      const float* crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 old = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (epi.beta != 0.0f && row < M && gn + j < N)
+          old = *reinterpret_cast<const float4*>(crow + gn + j);
+        const float o[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool in = gn + j + e < N;
+          r[j + e] = __float_as_uint(epi_apply(
+              epi, __uint_as_float(r[j + e]), o[e],
+              (epi.bias != nullptr && in) ? epi.bias[gn + j + e] : 0.0f));
+        }
+      }
+    }
     uint8_t* rowp = buf + lane * 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -270,7 +304,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmC,
                       float* __restrict__ C, int64_t ldc, int M, int N, int K,
                       int tiles_m, int tiles_n, int num_full, int split,
-                      int vec_c, int tma_c, unsigned int* __restrict__ status) {
+                      int vec_c, int tma_c, unsigned int* __restrict__ status,
+                      EpiParams epi) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
@@ -399,14 +434,15 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const int row0 = row - lane;
       if (tma_c) {
         if (u.width == BN)
-          store_unit_tma<BN>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane, chunk);
+          store_unit_tma<BN>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane, chunk,
+                             C, ldc, epi);
         else
           store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane,
-                                 chunk);
+                                 chunk, C, ldc, epi);
       } else if (u.width == BN) {
-        store_unit<BN>(taddr, C, ldc, row, u.n0, M, N, vec_c);
+        store_unit<BN>(taddr, C, ldc, row, u.n0, M, N, vec_c, epi);
       } else {
-        store_unit<BN / 2>(taddr, C, ldc, row, u.n0, M, N, vec_c);
+        store_unit<BN / 2>(taddr, C, ldc, row, u.n0, M, N, vec_c, epi);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -477,7 +513,8 @@ int pair_max_active(cudaStream_t stream) {
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const CUtensorMap* tmC, float* C, int64_t ldc,
                                   int M, int N, int K, bool vec_c, int max_pairs,
-                                  unsigned int* status, cudaStream_t stream) {
+                                  unsigned int* status, const EpiParams& epi,
+                                  cudaStream_t stream) {
   const int tiles_m = (M + PAIR_M - 1) / PAIR_M;
   const int tiles_n = (N + BN - 1) / BN;
   const int tiles = tiles_m * tiles_n;
@@ -504,7 +541,8 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   if (tmC == nullptr) std::memset(&unused, 0, sizeof(unused));
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused, C, ldc, M, N,
-      K, tiles_m, tiles_n, num_full, split, vec_c ? 1 : 0, tmC ? 1 : 0, status);
+      K, tiles_m, tiles_n, num_full, split, vec_c ? 1 : 0, tmC ? 1 : 0, status,
+      epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

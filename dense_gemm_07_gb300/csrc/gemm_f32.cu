@@ -166,16 +166,25 @@ struct SliceLoader {
   }
 };
 
-// Guarded store of one 4-wide group of row `crow` at column gn.
+// Guarded store of one 4-wide group of row `crow` at column gn, through the
+// epilogue (prior C and bias read only when the epilogue needs them).
 __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
-                                       float4 v) {
+                                       float4 v, const EpiParams& epi) {
+  float e[4] = {v.x, v.y, v.z, v.w};
   if (vec_c && gn + 3 < N) {
-    *reinterpret_cast<float4*>(crow + gn) = v;
-  } else {
-    const float e[4] = {v.x, v.y, v.z, v.w};
+    float4 old = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (epi.beta != 0.0f) old = *reinterpret_cast<const float4*>(crow + gn);
+    const float o[4] = {old.x, old.y, old.z, old.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (gn + j < N) crow[gn + j] = e[j];
+      e[j] = epi_apply(epi, e[j], o[j], epi.bias ? epi.bias[gn + j] : 0.0f);
+    *reinterpret_cast<float4*>(crow + gn) = make_float4(e[0], e[1], e[2], e[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (gn + j < N)
+        crow[gn + j] = epi_apply(epi, e[j], epi.beta != 0.0f ? crow[gn + j] : 0.0f,
+                                 epi.bias ? epi.bias[gn + j] : 0.0f);
   }
 }
 
@@ -184,7 +193,7 @@ __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
 __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
                                            float* C, int64_t ldc, int M, int N,
                                            int m0, int n0, int row_a, int col_b,
-                                           int vec_c) {
+                                           int vec_c, EpiParams epi) {
 #pragma unroll 1
   for (int i = 0; i < 8; ++i) {
     const int r = row_a + (i < 4 ? i : 12 + i);
@@ -202,7 +211,7 @@ __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
         sum.z += v.z;
         sum.w += v.w;
       }
-      store4(crow, n0 + col_b + 32 * h, N, vec_c, sum);
+      store4(crow, n0 + col_b + 32 * h, N, vec_c, sum, epi);
     }
   }
 }
@@ -220,7 +229,8 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
                          int64_t lda, const float* __restrict__ B, int64_t ldb,
                          float* __restrict__ C, int64_t ldc, int tiles_m,
                          int tiles_n, int first, int split, int vec_c,
-                         float* __restrict__ ws, unsigned int* __restrict__ counters) {
+                         float* __restrict__ ws, unsigned int* __restrict__ counters,
+                         EpiParams epi) {
   constexpr int TN = BN;
   constexpr int JP = TN / 32;      // float2 accumulators per row
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -309,7 +319,7 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     __syncthreads();
     if (last_block) {
       __threadfence();
-      reduce_ranges(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c);
+      reduce_ranges(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c, epi);
       if (tid == 0) counters[local_tile] = 0;  // leave the counter as found
     }
     return;
@@ -322,18 +332,11 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     if (gm >= M) continue;
     float* crow = C + static_cast<int64_t>(gm) * ldc;
 #pragma unroll
-    for (int h = 0; h < JP / 2; ++h) {
-      const int gn = n0 + col_b + 32 * h;
-      const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                          acc[i][2 * h + 1].y};
-      if (vec_c && gn + 3 < N) {
-        *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (gn + j < N) crow[gn + j] = v[j];
-      }
-    }
+    for (int h = 0; h < JP / 2; ++h)
+      store4(crow, n0 + col_b + 32 * h, N, vec_c,
+             make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
+                         acc[i][2 * h + 1].y),
+             epi);
   }
 }
 
@@ -342,11 +345,11 @@ cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int64_t lda, const float* B, int64_t ldb, float* C,
                         int64_t ldc, int tiles_m, int tiles_n, int first,
                         int split, int vec_c, float* ws, unsigned int* counters,
-                        cudaStream_t stream) {
+                        const EpiParams& epi, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<BN>);
   gemm_f32_regblock_kernel<VEC_B><<<blocks, THREADS, smem, stream>>>(
       M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
-      counters);
+      counters, epi);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -420,27 +423,28 @@ F32Plan f32_plan(int M, int N, int K, int64_t slots) {
 cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             const float* B, int64_t ldb, float* C, int64_t ldc,
                             bool vec_b, bool vec_c, const F32Plan& p, float* ws,
-                            unsigned int* counters, cudaStream_t stream) {
+                            unsigned int* counters, const EpiParams& epi,
+                            cudaStream_t stream) {
   if (f32_slots() <= 0) return cudaErrorInvalidDeviceFunction;
   const int vc = vec_c ? 1 : 0;
   cudaError_t e = cudaSuccess;
   if (p.full > 0) {
     e = vec_b ? launch_part<true>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
                                   p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
-                                  nullptr, stream)
+                                  nullptr, epi, stream)
               : launch_part<false>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
                                    p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
-                                   nullptr, stream);
+                                   nullptr, epi, stream);
     if (e != cudaSuccess) return e;
   }
   if (p.tail > 0) {
     const int blocks = p.tail * p.split;
     e = vec_b ? launch_part<true>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
                                   p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
-                                  counters, stream)
+                                  counters, epi, stream)
               : launch_part<false>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
                                    p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
-                                   counters, stream);
+                                   counters, epi, stream);
   }
   return e;
 }

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
+
 namespace g07 {
 
 // Records `n` kernel launches by this library (defined in api.cu); the total
@@ -34,7 +36,7 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             const float* B, int64_t ldb, float* C, int64_t ldc,
                             bool vec_b, bool vec_c, const F32Plan& plan,
                             float* ws, unsigned int* counters,
-                            cudaStream_t stream);
+                            const EpiParams& epi, cudaStream_t stream);
 
 // ---- BF16 tensor-core path (gemm_bf16_tc.cu)
 constexpr int kTcTileM = 128;
@@ -50,7 +52,7 @@ size_t tc_smem_bytes();
 cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 float* C, int64_t ldc, int M, int N, int K,
                                 bool vec_c, int grid, unsigned int* status,
-                                cudaStream_t stream);
+                                const EpiParams& epi, cudaStream_t stream);
 
 // ---- BF16 tensor-core path on SM pairs (gemm_bf16_tc2.cu): 256 x 256 tiles
 constexpr int kPairTileM = 256;
@@ -67,7 +69,8 @@ int pair_max_active(cudaStream_t stream);
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                   const CUtensorMap* tmC, float* C, int64_t ldc,
                                   int M, int N, int K, bool vec_c, int max_pairs,
-                                  unsigned int* status, cudaStream_t stream);
+                                  unsigned int* status, const EpiParams& epi,
+                                  cudaStream_t stream);
 
 // ---- BF16 small-M path (gemm_bf16_skinny.cu): swap-AB, split-K over a
 // cluster, partial sums reduced through distributed shared memory.
@@ -81,7 +84,8 @@ int skinny_split(int N, int K, int sms);
 cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,
                                     const CUtensorMap& tmB, float* C,
                                     int64_t ldc, int M, int N, int K, int cs,
-                                    unsigned int* status, cudaStream_t stream);
+                                    unsigned int* status, const EpiParams& epi,
+                                    cudaStream_t stream);
 
 // ---- FP32 teaching rungs (gemm_f32_ladder.cu): 0 naive, 1 smem-tiled,
 // 2 one-dimensional register tiling.
@@ -90,8 +94,9 @@ cudaError_t launch_gemm_f32_ladder(int rung, int M, int N, int K, const float* A
                                    float* C, int64_t ldc, cudaStream_t stream);
 
 // ---- small helpers (gemm_aux.cu)
+// K == 0: C := act(beta * C + bias) (zeros for the identity epilogue).
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
-                                 cudaStream_t stream);
+                                 const EpiParams& epi, cudaStream_t stream);
 // Copy a rows x cols matrix of 16-bit elements to dst with row stride ld_dst.
 cudaError_t launch_copy_rows_u16(const uint16_t* src, int64_t ld_src,
                                  uint16_t* dst, int64_t ld_dst, int rows,

@@ -104,6 +104,42 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
                                float *C, int64_t ldc, void *stream);
 
 /*
+ * Fused epilogue ("How a Matrix Multiply Runs on a GPU", "Level 2": the
+ * output step alpha * acc + beta * C, plus bias and activation, applied while
+ * the accumulators are still on chip):
+ *   C[i][j] := act(alpha * (A*B)[i][j] + beta * C[i][j] + bias[j])
+ * evaluated in FP32 as v = alpha*acc; v = fma(beta, C_old, v); v += bias;
+ * v = act(v).  beta == 0: the prior contents of C are not read (they may be
+ * uninitialised).  bias: DEVICE pointer to N floats, or NULL.  A NULL
+ * epilogue pointer means alpha = 1, beta = 0, no bias, no activation: the
+ * plain product, bit for bit.
+ */
+typedef enum gemm_activation {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1      /* max(x, 0) */
+} gemm_activation_t;
+
+typedef struct gemm_epilogue {
+    float alpha;
+    float beta;
+    const float *bias;
+    int32_t activation;    /* a gemm_activation_t */
+} gemm_epilogue_t;
+
+/* gemm_f32 / gemm_bf16_f32acc with a fused epilogue; an unknown activation
+ * returns GEMM_ERR_INVALID_ARG. */
+GEMM07_API gemm_status_t gemm_f32_ex(int64_t M, int64_t N, int64_t K,
+                          const float *A, int64_t lda,
+                          const float *B, int64_t ldb,
+                          float *C, int64_t ldc,
+                          const gemm_epilogue_t *epilogue, void *stream);
+GEMM07_API gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K,
+                                  const uint16_t *A, int64_t lda,
+                                  const uint16_t *B, int64_t ldb,
+                                  float *C, int64_t ldc,
+                                  const gemm_epilogue_t *epilogue, void *stream);
+
+/*
  * gemm_bf16_f32acc_noalloc -- the same operation, arguments and results as
  * gemm_bf16_f32acc, for callers that must not allocate device memory.
  *   The pages describe no such entry point; it has no counterpart there.

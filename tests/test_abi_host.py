@@ -140,6 +140,14 @@ def test_plan_and_calls_reject_bad_arguments(lib):
     assert _abi.gemm_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == _abi.GEMM_OK
 
 
+def test_epilogue_entry_points_validate_on_host(lib):
+    epi = _abi.GemmEpilogue(1.0, 0.0, None, 9)
+    assert _abi.gemm_bf16_f32acc_ex(4, 4, 4, 16, 4, 16, 4, 16, 4, epi, None) == \
+        _abi.GEMM_ERR_INVALID_ARG
+    assert _abi.gemm_f32_ex(-1, 4, 4, 16, 4, 16, 4, 16, 4, None, None) == \
+        _abi.GEMM_ERR_INVALID_ARG
+
+
 def test_ladder_rejects_bad_rungs(lib):
     assert _abi.gemm_f32_ladder(3, 4, 4, 4, 16, 4, 16, 4, 16, 4, None) == _abi.GEMM_ERR_INVALID_ARG
     assert _abi.gemm_f32_ladder(-1, 4, 4, 4, 16, 4, 16, 4, 16, 4, None) == _abi.GEMM_ERR_INVALID_ARG

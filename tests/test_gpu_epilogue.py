@@ -1,0 +1,104 @@
+"""The fused epilogue C := act(alpha * A@B + beta * C + bias) on every path,
+against the oracle's epilogue step applied to its exact product.
+
+Bound: |C - C_ref| <= rtol * (|alpha| * S + |beta * C0| + |bias|) + atol, the
+product's bound scaled by alpha plus one rounding of the added terms; with
+integer-valued operands, alpha, beta and bias the result is exact."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import _abi, inputs
+import oracle
+from gemm_check import ATOL, RTOL, oracle_ref
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist):
+    dtype = torch.float32 if kind == "f32" else torch.bfloat16
+    a, b = inputs.make_pair(M, N, K, seed, dist, dtype=dtype)
+    g = torch.Generator().manual_seed(seed + 1000)
+    c0 = torch.randint(-5, 6, (M, N), generator=g).float()
+    bias = torch.randint(-4, 5, (N,), generator=g).float() if use_bias else None
+    out = c0.to(DEV).clone()
+    fn = g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex
+    fn(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
+       bias=bias.to(DEV) if bias is not None else None, activation=act)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    ab, s = oracle_ref(kind, a, b)
+    want = oracle.gemm_epilogue(ab, alpha=alpha, beta=beta,
+                                C0=c0.numpy() if beta != 0 else None,
+                                bias=bias.numpy() if bias is not None else None,
+                                act=1 if act == "relu" else 0)
+    got = out.cpu().numpy().astype(np.float64)
+    if exact:
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, f"{len(bad)} mismatches, first {tuple(bad[0])}"
+    else:
+        scale = abs(alpha) * s + abs(beta) * np.abs(c0.numpy()) + \
+            (np.abs(bias.numpy())[None, :] if bias is not None else 0)
+        err = np.abs(got - want)
+        lim = RTOL[kind] * scale + ATOL[kind]
+        assert np.all(err <= lim), float(np.max(err - lim))
+
+
+PATHS = [
+    ("bf16", 512, 768, 320),   # SM pairs, TMA-store epilogue
+    ("bf16", 300, 258, 200),   # SM pairs, N % 4 != 0: direct stores
+    ("bf16", 48, 1000, 777),   # small M, cluster reduction
+    ("f32", 640, 520, 2000),   # FP32, one partial wave split along K
+    ("f32", 2560, 2048, 640),  # FP32, whole waves + split tail
+]
+
+
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: f"{p[0]}-{p[1]}x{p[2]}x{p[3]}")
+@pytest.mark.parametrize("epi", [(2.0, -1.0, True, "none"), (1.0, 0.0, True, "relu"),
+                                 (-3.0, 2.0, False, "relu"), (0.5, 0.0, False, "none")],
+                         ids=["ab+c+bias", "bias+relu", "beta_relu", "alpha_only"])
+def test_epilogue_exact_integers(path, epi):
+    kind, M, N, K = path
+    alpha, beta, use_bias, act = epi
+    _case(kind, M, N, K, 50, alpha, beta, use_bias, act, exact=True,
+          dist=inputs.INT3)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_epilogue_general_values(kind):
+    _case(kind, 700, 900, 1000, 51, 0.75, -1.25, True, "none", exact=False,
+          dist=inputs.NORMAL if kind == "bf16" else inputs.UNIFORM)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_epilogue_with_zero_k(kind):
+    _case(kind, 33, 45, 0, 52, 2.0, 3.0, True, "relu", exact=True, dist=inputs.INT3)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_identity_epilogue_equals_plain_entry_point_bitwise(kind):
+    dtype = torch.float32 if kind == "f32" else torch.bfloat16
+    a, b = inputs.make_pair(600, 500, 300, 53, inputs.NORMAL, dtype=dtype)
+    a, b = a.to(DEV), b.to(DEV)
+    plain = (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a, b)
+    ex = (g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex)(a, b)
+    assert torch.equal(plain.view(torch.int32), ex.view(torch.int32))
+
+
+def test_beta_zero_does_not_read_c():
+    a, b = inputs.make_pair(300, 260, 100, 54, inputs.INT3, dtype=torch.bfloat16)
+    out = torch.full((300, 260), float("nan"), device=DEV)
+    g7.gemm_bf16_f32acc_ex(a.to(DEV), b.to(DEV), out=out, alpha=1.0, beta=0.0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+
+
+def test_unknown_activation_rejected():
+    epi = _abi.GemmEpilogue(1.0, 0.0, None, 5)
+    a = torch.ones((4, 4), device=DEV)
+    c = torch.zeros((4, 4), device=DEV)
+    st = torch.cuda.current_stream().cuda_stream
+    assert _abi.gemm_f32_ex(4, 4, 4, a.data_ptr(), 4, a.data_ptr(), 4, c.data_ptr(), 4,
+                            epi, st) == _abi.GEMM_ERR_INVALID_ARG
