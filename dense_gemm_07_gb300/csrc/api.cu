@@ -33,6 +33,8 @@ struct DeviceState {
   int sms = 0;
   unsigned int* status = nullptr;  // address of g_status_word on this device
   cudaMemPool_t pool = nullptr;
+  cudaStream_t up = nullptr;    // host-variant uploads
+  cudaStream_t down = nullptr;  // host-variant downloads
 };
 
 std::mutex g_mutex;
@@ -206,6 +208,24 @@ gemm_status_t device_state(DeviceState** out) {
   }
   if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
   *out = &d;
+  return GEMM_OK;
+}
+
+// The two helper streams of the host-buffer variants (created once).
+gemm_status_t host_streams(DeviceState* d) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (d->up == nullptr &&
+      cudaStreamCreateWithFlags(&d->up, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    d->up = nullptr;
+    return GEMM_ERR_LAUNCH;
+  }
+  if (d->down == nullptr &&
+      cudaStreamCreateWithFlags(&d->down, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    d->down = nullptr;
+    return GEMM_ERR_LAUNCH;
+  }
   return GEMM_OK;
 }
 
@@ -394,37 +414,84 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
 }
 
 // Host-buffer variant: stage through pool memory, run, copy back, sync.
+// Host-buffer variant: stage through pool memory and overlap the copies with
+// the GEMM.  B is copied first (every output row needs all of it); A is then
+// copied in `chunks` row blocks on an internal upload stream, each block's
+// GEMM runs on the caller's stream as soon as its rows have arrived, and each
+// block of C goes back on an internal download stream while the next block
+// computes.  Uploads and downloads use both directions of the link at once.
 template <typename T, typename Run>
 gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
                        int64_t lda, const T* B, int64_t ldb, float* C,
-                       int64_t ldc, cudaStream_t stream, Run run) {
+                       int64_t ldc, cudaStream_t stream, int max_chunks,
+                       int64_t min_chunk_rows, Run run) {
   gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (s != GEMM_OK || M == 0 || N == 0) return s;
   DeviceState* d = nullptr;
   s = device_state(&d);
   if (s != GEMM_OK) return s;
-  void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  s = host_streams(d);
+  if (s != GEMM_OK) return s;
   const int64_t eb = static_cast<int64_t>(sizeof(T));
-  s = pool_alloc(d, &dA, M * K * eb, stream);
+  int64_t chunks = M / (min_chunk_rows > 0 ? min_chunk_rows : 1);
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1 || K == 0) chunks = 1;
+  constexpr int kMaxChunks = 8;
+  if (chunks > kMaxChunks) chunks = kMaxChunks;
+
+  void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  cudaEvent_t ev[2 * kMaxChunks + 1] = {};
+  int n_ev = 0;
+  for (; n_ev < 2 * chunks + 1; ++n_ev)
+    if (cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      s = GEMM_ERR_LAUNCH;
+      break;
+    }
+  cudaEvent_t start = ev[0];
+  if (s == GEMM_OK) s = pool_alloc(d, &dA, M * K * eb, stream);
   if (s == GEMM_OK) s = pool_alloc(d, &dB, K * N * eb, stream);
   if (s == GEMM_OK) s = pool_alloc(d, &dC, M * N * 4, stream);
-  if (s == GEMM_OK && K > 0)
-    s = from_cuda(cudaMemcpy2DAsync(dA, K * eb, A, lda * eb, K * eb, M,
-                                    cudaMemcpyHostToDevice, stream));
+  // the helper streams start after everything already queued on `stream`
+  if (s == GEMM_OK) s = from_cuda(cudaEventRecord(start, stream));
+  if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->up, start, 0));
+  if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->down, start, 0));
   if (s == GEMM_OK && K > 0)
     s = from_cuda(cudaMemcpy2DAsync(dB, N * eb, B, ldb * eb, N * eb, K,
                                     cudaMemcpyHostToDevice, stream));
-  if (s == GEMM_OK)
-    s = run(M, N, K, static_cast<const T*>(dA), K > 0 ? K : 1,
-            static_cast<const T*>(dB), N, static_cast<float*>(dC), N, stream);
-  if (s == GEMM_OK)
-    s = from_cuda(cudaMemcpy2DAsync(C, ldc * 4, dC, N * 4, N * 4, M,
-                                    cudaMemcpyDeviceToHost, stream));
+  for (int64_t i = 0; s == GEMM_OK && i < chunks; ++i) {
+    const int64_t r0 = M * i / chunks, r1 = M * (i + 1) / chunks, rows = r1 - r0;
+    cudaEvent_t a_ready = ev[1 + 2 * i], c_ready = ev[2 + 2 * i];
+    if (K > 0) {
+      s = from_cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(dA) + r0 * K * eb, K * eb,
+                                      A + r0 * lda, lda * eb, K * eb, rows,
+                                      cudaMemcpyHostToDevice, d->up));
+      if (s == GEMM_OK) s = from_cuda(cudaEventRecord(a_ready, d->up));
+      if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(stream, a_ready, 0));
+    }
+    if (s == GEMM_OK)
+      s = run(rows, N, K,
+              reinterpret_cast<const T*>(static_cast<uint8_t*>(dA) + r0 * K * eb),
+              K > 0 ? K : 1, static_cast<const T*>(dB), N,
+              static_cast<float*>(dC) + r0 * N, N, stream);
+    if (s == GEMM_OK) s = from_cuda(cudaEventRecord(c_ready, stream));
+    if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->down, c_ready, 0));
+    if (s == GEMM_OK)
+      s = from_cuda(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4,
+                                      static_cast<float*>(dC) + r0 * N, N * 4,
+                                      N * 4, rows, cudaMemcpyDeviceToHost,
+                                      d->down));
+  }
+  // Every copy is done before the buffers go back to the pool.
+  if (s == GEMM_OK) s = from_cuda(cudaEventRecord(ev[0], d->down));
+  if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(stream, ev[0], 0));
   pool_free(dA, stream);
   pool_free(dB, stream);
   pool_free(dC, stream);
-  const cudaError_t e = cudaStreamSynchronize(stream);
-  if (s == GEMM_OK) s = from_cuda(e);
+  const cudaError_t e1 = cudaStreamSynchronize(stream);
+  const cudaError_t e2 = cudaStreamSynchronize(d->down);
+  for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
+  if (s == GEMM_OK) s = from_cuda(e1 != cudaSuccess ? e1 : e2);
   return s;
 }
 
@@ -626,7 +693,7 @@ gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
                             int64_t ldc, void* stream) {
   return run_host<float>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la,
+      /*max_chunks=*/2, /*min_chunk_rows=*/1024, [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la,
          const float* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
         return run_f32(m, n, k, a, la, b, lb, c, lc, st);
       });
@@ -638,7 +705,7 @@ gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
                                     int64_t ldc, void* stream) {
   return run_host<uint16_t>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
+      /*max_chunks=*/4, /*min_chunk_rows=*/512, [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
          const uint16_t* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
         return run_bf16(m, n, k, a, la, b, lb, c, lc, st);
       });
@@ -683,10 +750,12 @@ void gemm_shutdown(void) {
   const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
   for (int i = 0; i < kMaxDevices; ++i) {
     DeviceState& d = g_dev[i];
-    if (d.pool) {
+    if (d.pool || d.up || d.down) {
       if (cudaSetDevice(i) == cudaSuccess) {
         cudaDeviceSynchronize();
-        cudaMemPoolDestroy(d.pool);
+        if (d.pool) cudaMemPoolDestroy(d.pool);
+        if (d.up) cudaStreamDestroy(d.up);
+        if (d.down) cudaStreamDestroy(d.down);
       }
     }
     d = DeviceState();

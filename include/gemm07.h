@@ -188,9 +188,14 @@ GEMM07_API gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t
 /*
  * Host-buffer variants: the same operations with A, B and C in HOST memory
  * (pinned memory gives the fastest copies; pageable memory works).  The
- * call copies A and B to device staging buffers on `stream`, runs the GEMM,
- * copies C back and synchronises `stream` before it returns.  Staging
- * buffers come from the library's memory pool on the current device.
+ * call stages A and B in device buffers from the library's memory pool,
+ * runs the GEMM and copies C back, and returns once C is in host memory
+ * (it synchronises `stream`).  B is copied first; A is then copied in row
+ * blocks on a library-owned upload stream, each block's product is computed
+ * on `stream` as soon as its rows arrive, and each block of C is copied
+ * back on a library-owned download stream while the next block computes,
+ * so uploads, downloads and compute overlap.  Work already queued on
+ * `stream` completes before any of this starts.
  */
 GEMM07_API gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K,
                             const float *A, int64_t lda,

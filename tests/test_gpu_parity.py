@@ -246,6 +246,24 @@ def test_host_buffer_variant_matches_device(kind):
     assert torch.equal(c_host.view(torch.int32), c_dev.view(torch.int32))
 
 
+@pytest.mark.parametrize("kind,shape", [("f32", (2048, 300, 700)), ("bf16", (2048, 520, 333)),
+                                        ("bf16", (3000, 1000, 1000))])
+def test_host_buffer_variant_in_row_blocks_exact(kind, shape):
+    # large enough that the host variant overlaps copies with per-block GEMMs
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 22, inputs.INT3, dtype=_dtype(kind))
+    host_fn = g7.gemm_f32_host if kind == "f32" else g7.gemm_bf16_f32acc_host
+    c = host_fn(a.pin_memory(), b.pin_memory())
+    c_ref, _ = oracle_ref(kind, a, b, with_abs=False)
+    assert_within(kind, c.numpy(), c_ref, None, exact=True)
+    # a strided host C: rows ldc apart, padding untouched
+    ldc = N + 3
+    buf = torch.full((M, ldc), -7.0).pin_memory()
+    host_fn(a.pin_memory(), b.pin_memory(), out=buf[:, :N])
+    assert torch.all(buf[:, N:] == -7.0)
+    assert_within(kind, buf[:, :N].numpy(), c_ref, None, exact=True)
+
+
 def test_streams_are_respected():
     a, b = inputs.make_pair(1024, 1024, 1024, 15, inputs.INT3, dtype=torch.bfloat16)
     s = torch.cuda.Stream()
