@@ -34,7 +34,9 @@ class GemmPlan(ctypes.Structure):
                 ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32)]
+                ("pack_a", ctypes.c_int32), ("pack_b", ctypes.c_int32),
+                ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64),
+                ("sk_pairs", ctypes.c_int32), ("pairs", ctypes.c_int32)]
 
 
 class GemmEpilogue(ctypes.Structure):
@@ -70,6 +72,8 @@ SIGNATURES = [
                               ctypes.POINTER(GemmPlan)]),
     ("gemm_plan_f32", _i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                              ctypes.POINTER(GemmPlan)]),
+    ("gemm_pair_units", _i64, [_i64, _i64, _i64, _i32, _i32, _i32, _vp, _i64]),
+    ("gemm_set_bf16_schedule", _i32, [_i32]),
 ]
 
 
@@ -184,3 +188,25 @@ def gemm_plan_bf16(M, N, K, A, lda, B, ldb, C, ldc):
 
 def gemm_plan_f32(M, N, K, A, lda, B, ldb, C, ldc):
     return _plan(lib().gemm_plan_f32, M, N, K, A, lda, B, ldb, C, ldc)
+
+
+SCHEDULE_AUTO = 0
+SCHEDULE_STREAM_K = 1
+SCHEDULE_COLUMN_SPLIT = 2
+
+
+def gemm_set_bf16_schedule(schedule: int) -> int:
+    return lib().gemm_set_bf16_schedule(schedule)
+
+
+def gemm_pair_units(M, N, K, max_pairs, pair, schedule=SCHEDULE_AUTO):
+    """The BF16 paired-SM kernel's work units for one pair, in order, as a
+    list of (tile, k0, k1, slot, first_pair, segments, stream_k, n_off,
+    width) tuples; raises on bad arguments."""
+    n = lib().gemm_pair_units(M, N, K, max_pairs, schedule, pair, None, 0)
+    if n < 0:
+        raise ValueError("gemm_pair_units: argument out of range")
+    buf = (ctypes.c_int64 * (9 * max(n, 1)))()
+    n2 = lib().gemm_pair_units(M, N, K, max_pairs, schedule, pair, buf, n)
+    assert n2 == n
+    return [tuple(buf[9 * i:9 * i + 9]) for i in range(n)]

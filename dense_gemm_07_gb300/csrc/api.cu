@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <chrono>
 #include <mutex>
 
 #include <cuda.h>
@@ -27,6 +28,17 @@ __device__ unsigned int g_status_word[4];
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 0x7FFFFFFF;  // M, N, K < 2^31
 
+// Scratch kept between calls for one stream: calls on a stream run in order,
+// so they can share it without allocating each time (a stream-ordered
+// allocate/free pair costs about 2 us of GPU time per call).
+struct StreamScratch {
+  cudaStream_t stream = nullptr;
+  void* ptr = nullptr;
+  int64_t bytes = 0;
+  uint64_t last_use = 0;
+};
+constexpr int kScratchStreams = 8;
+
 struct DeviceState {
   bool ready = false;
   bool supported = false;
@@ -35,10 +47,22 @@ struct DeviceState {
   cudaMemPool_t pool = nullptr;
   cudaStream_t up = nullptr;    // host-variant uploads
   cudaStream_t down = nullptr;  // host-variant downloads
+  StreamScratch scratch[kScratchStreams];
+  uint64_t scratch_clock = 0;
+  uint64_t launch_tags = 0;     // stream-K launches so far (tag source)
+  uint64_t tag_salt = 0;
 };
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+
+// How the BF16 paired-SM kernel shares a partial last wave (a
+// gemm_schedule_t; the values match PairScheduleMode).
+std::atomic<int> g_schedule{GEMM_SCHEDULE_AUTO};
+static_assert(static_cast<int>(GEMM_SCHEDULE_AUTO) == kScheduleAuto &&
+                  static_cast<int>(GEMM_SCHEDULE_STREAM_K) == kScheduleStreamK &&
+                  static_cast<int>(GEMM_SCHEDULE_COLUMN_SPLIT) == kScheduleNoSplitK,
+              "schedule values");
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType,
                                    cuuint32_t, void*, const cuuint64_t*,
@@ -65,6 +89,20 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
   if (C == nullptr) return GEMM_ERR_INVALID_ARG;
   if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
   return GEMM_OK;
+}
+
+// Scratch of the copies that make A and B readable by the copy engine.
+int64_t pack_bytes(int64_t M, int64_t N, int64_t K, bool pack_a, bool pack_b) {
+  int64_t ws = 0;
+  if (pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
+  if (pack_b) ws += round_up(K * round_up(N, 8) * 2, 256);
+  return ws;
+}
+
+// Scratch of a stream-K schedule: partial sums, then synchronisation words.
+int64_t sk_bytes(const PairSchedule& ps) {
+  if (ps.sk_tiles == 0) return 0;
+  return round_up(sk_partial_bytes(ps), 256) + round_up(sk_sync_words(ps) * 8, 256);
 }
 
 void plan_clear(gemm_plan_t* p) {
@@ -115,10 +153,7 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->pack_a = (aligned16(A) && lda % 8 == 0) ? 0 : 1;
   p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
   p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
-  int64_t ws = 0;
-  if (p->pack_a) ws += round_up(M * round_up(K, 8) * 2, 256);
-  if (p->pack_b) ws += round_up(K * round_up(N, 8) * 2, 256);
-  p->workspace_bytes = ws;
+  p->workspace_bytes = pack_bytes(M, N, K, p->pack_a, p->pack_b);
   if (M <= kSkinnyMaxM) {
     // Small M: 128-column tiles of C, K split over a cluster (the split is
     // reported for the 152 SMs of a GB300; launches use the device's count).
@@ -131,14 +166,23 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
     p->tiles = ((N + kSkinnyTileN - 1) / kSkinnyTileN) * p->split_k;
     return GEMM_OK;
   }
-  // 256 x 256 tiles on SM pairs.
+  // 256 x 256 tiles on SM pairs (the work sharing is reported for the 76
+  // pairs of a 152-SM GB300; launches use the device's resident count).
   const bool pair = M > kTcTileM;
   p->tile_m = pair ? kPairTileM : kTcTileM;
   p->tile_n = pair ? kPairTileN : kTcTileN;
-  p->tile_k = kTcTileK;
+  p->tile_k = pair ? kPairTileK : kTcTileK;
   p->stages = pair ? kPairStages : kTcStages;
   p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  if (pair) {
+    const PairSchedule ps = pair_schedule(M, N, K, 76, g_schedule.load());
+    p->dp_tiles = ps.dp_tiles;
+    p->sk_tiles = ps.sk_tiles;
+    p->sk_pairs = ps.sk_pairs;
+    p->pairs = ps.pairs;
+    p->workspace_bytes += sk_bytes(ps);
+  }
   return GEMM_OK;
 }
 
@@ -203,6 +247,13 @@ gemm_status_t device_state(DeviceState** out) {
       }
       uint64_t keep = ~0ull;  // keep freed blocks for the next call
       cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      // tags of different processes or library loads sharing leftover
+      // memory differ
+      d.tag_salt = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&d)) ^
+                   (static_cast<uint64_t>(std::chrono::steady_clock::now()
+                                              .time_since_epoch()
+                                              .count()) *
+                    0x9E3779B97F4A7C15ull);
     }
     d.ready = true;
   }
@@ -276,6 +327,17 @@ gemm_status_t make_map(CUtensorMap* map, const void* base, int64_t inner,
                         outer, ld, box_inner, box_outer);
 }
 
+// BF16 operand maps: A boxes of 64 k x `a_rows` rows, B boxes of 64
+// columns x 64 k, both 128-byte swizzled.
+gemm_status_t make_operand_maps(CUtensorMap* tmA, CUtensorMap* tmB,
+                                const uint16_t* a, int64_t lda,
+                                const uint16_t* b, int64_t ldb, int64_t M,
+                                int64_t N, int64_t K, uint32_t a_rows) {
+  gemm_status_t s = make_map(tmA, a, K, M, lda, kTcTileK, a_rows);
+  if (s == GEMM_OK) s = make_map(tmB, b, N, K, ldb, 64, kTcTileK);
+  return s;
+}
+
 // The TMA-store epilogue needs C 16-byte aligned with rows a multiple of 16
 // bytes apart, and N a multiple of 4: the copy engine clips the inner
 // dimension of a store in 16-byte units, so a row that ends mid-unit would
@@ -306,6 +368,77 @@ gemm_status_t pool_alloc(DeviceState* d, void** p, int64_t bytes,
 
 void pool_free(void* p, cudaStream_t stream) {
   if (p) cudaFreeAsync(p, stream);
+}
+
+std::mutex g_scratch_mutex;
+
+// At least `bytes` of scratch for work queued on `stream`, kept for later
+// calls on the same stream.  Growing frees the old block in stream order;
+// reusing another stream's entry (more than kScratchStreams streams) first
+// waits for the device, since that stream's work may still use the block.
+gemm_status_t stream_scratch(DeviceState* d, cudaStream_t stream, int64_t bytes,
+                             void** out) {
+  *out = nullptr;
+  if (bytes <= 0) return GEMM_OK;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  StreamScratch* e = nullptr;
+  for (StreamScratch& x : d->scratch)
+    if (x.ptr && x.stream == stream) e = &x;
+  if (e == nullptr) {
+    for (StreamScratch& x : d->scratch)
+      if (!x.ptr) {
+        e = &x;
+        break;
+      }
+  }
+  if (e == nullptr) {
+    e = &d->scratch[0];
+    for (StreamScratch& x : d->scratch)
+      if (x.last_use < e->last_use) e = &x;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    cudaFreeAsync(e->ptr, stream);
+    *e = StreamScratch();
+  }
+  if (e->ptr && e->bytes < bytes) {
+    cudaFreeAsync(e->ptr, stream);
+    e->ptr = nullptr;
+  }
+  if (!e->ptr) {
+    const int64_t want = round_up(bytes, int64_t(1) << 20);
+    if (cudaMallocFromPoolAsync(&e->ptr, static_cast<size_t>(want), d->pool,
+                                stream) != cudaSuccess) {
+      cudaGetLastError();
+      *e = StreamScratch();
+      return GEMM_ERR_NO_MEMORY;
+    }
+    e->bytes = want;
+  }
+  e->stream = stream;
+  e->last_use = ++d->scratch_clock;
+  *out = e->ptr;
+  return GEMM_OK;
+}
+
+// A fresh 56-bit nonzero tag for one stream-K launch.
+unsigned long long next_launch_tag(DeviceState* d) {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  uint64_t z = ++d->launch_tags + d->tag_salt;
+  // splitmix64 finaliser
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  z &= (1ull << 56) - 1;
+  return z ? z : 1ull;
+}
+
+// Map of the stream-K partial-sum workspace (see gemm_bf16_tc2.cu).
+gemm_status_t make_map_partials(CUtensorMap* map, float* ws,
+                                const PairSchedule& ps) {
+  return make_map_typed(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, 256,
+                        static_cast<int64_t>(ps.sk_pairs) * 512, 256, 32, 32);
 }
 
 gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
@@ -362,14 +495,31 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
 
   const int m = static_cast<int>(M), n = static_cast<int>(N),
             k = static_cast<int>(K);
+  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
+  const int max_pairs =
+      !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
+  PairSchedule ps;
+  if (max_pairs > 0) ps = pair_schedule(M, N, K, max_pairs, g_schedule.load());
+  const int64_t pack_ws = pack_bytes(M, N, K, plan.pack_a, plan.pack_b);
   void* ws = nullptr;
-  s = pool_alloc(d, &ws, plan.workspace_bytes, stream);
+  s = pool_alloc(d, &ws, pack_ws, stream);
   if (s != GEMM_OK) return s;
+  // stream-K scratch: partial sums, then tagged synchronisation words
+  void* sk = nullptr;
+  s = stream_scratch(d, stream, sk_bytes(ps), &sk);
+  float* sk_ws = static_cast<float*>(sk);
+  unsigned long long* sk_sync = nullptr;
+  CUtensorMap tmW;
+  if (s == GEMM_OK && ps.sk_tiles > 0) {
+    sk_sync = reinterpret_cast<unsigned long long*>(
+        static_cast<uint8_t*>(sk) + round_up(sk_partial_bytes(ps), 256));
+    s = make_map_partials(&tmW, sk_ws, ps);
+  }
   const uint16_t* a_op = A;
   const uint16_t* b_op = B;
   int64_t lda_op = lda, ldb_op = ldb;
   uint8_t* cursor = static_cast<uint8_t*>(ws);
-  if (plan.pack_a) {
+  if (s == GEMM_OK && plan.pack_a) {
     uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
     lda_op = round_up(K, 8);
     cursor += round_up(M * lda_op * 2, 256);
@@ -383,24 +533,22 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     b_op = dst;
   }
   CUtensorMap tmA, tmB;
-  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
   if (s == GEMM_OK)
-    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK,
-                 skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
-  if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
+    s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
+                          skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
   if (s == GEMM_OK && skinny) {
     s = from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                           skinny_split(n, k, d->sms), d->status,
                                           epi, stream));
   } else if (s == GEMM_OK) {
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
-    const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
     if (max_pairs > 0) {
       CUtensorMap tmC;
       const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
-      s = from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
-                                          ldc, m, n, k, vec_c, max_pairs,
-                                          d->status, epi, stream));
+      const unsigned long long tag = ps.sk_tiles > 0 ? next_launch_tag(d) : 0;
+      s = from_cuda(launch_gemm_bf16_pair(
+          tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
+          ldc, m, n, ps, sk_sync, tag, vec_c, d->status, epi, stream));
     } else {
       const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
                             ((N + kTcTileN - 1) / kTcTileN);
@@ -509,8 +657,22 @@ struct NoallocState {
   int sms = 0;
   unsigned int* status = nullptr;
   uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch
+  uint64_t launch_tags = 0;    // stream-K launches so far (tag source)
 };
 NoallocState g_noalloc[kMaxDevices];
+
+// A fresh 56-bit nonzero tag for one stream-K launch on the fixed scratch.
+unsigned long long next_noalloc_tag(NoallocState* d) {
+  static std::mutex m;
+  std::lock_guard<std::mutex> lock(m);
+  uint64_t z = ++d->launch_tags + 0x5851F42D4C957F2Dull *
+                                      static_cast<uint64_t>(reinterpret_cast<uintptr_t>(d));
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  z &= (1ull << 56) - 1;
+  return z ? z : 1ull;
+}
 
 // Once per device, with that device current: capability check and the device
 // addresses of the status word and of the scratch array.  Allocates nothing.
@@ -559,8 +721,8 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   gemm_plan_t plan;
   gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan);
   if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
-  if (plan.workspace_bytes > kNoallocScratchBytes)
-    return GEMM_ERR_SCRATCH_TOO_SMALL;
+  const int64_t pack_ws = pack_bytes(M, N, K, plan.pack_a, plan.pack_b);
+  if (pack_ws > kNoallocScratchBytes) return GEMM_ERR_SCRATCH_TOO_SMALL;
   NoallocState* d = nullptr;
   s = noalloc_device(&d);
   if (s != GEMM_OK) return s;
@@ -590,23 +752,39 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   }
   CUtensorMap tmA, tmB;
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
+  const int max_pairs =
+      !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (s == GEMM_OK)
-    s = make_map(&tmA, a_op, K, M, lda_op, kTcTileK,
-                 skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
-  if (s == GEMM_OK) s = make_map(&tmB, b_op, N, K, ldb_op, 64, kTcTileK);
+    s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
+                          skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
   if (s != GEMM_OK) return s;
   if (skinny)
     return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                              skinny_split(n, k, d->sms),
                                              d->status, epi_identity(), stream));
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
-  const int max_pairs = plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (max_pairs > 0) {
+    // Stream-K only when its scratch fits after the packed operands.
+    PairSchedule ps = pair_schedule(M, N, K, max_pairs, g_schedule.load());
+    if (pack_ws + sk_bytes(ps) > kNoallocScratchBytes)
+      ps = pair_schedule(M, N, K, max_pairs, kScheduleNoSplitK);
+    float* sk_ws = nullptr;
+    unsigned long long* sk_sync = nullptr;
+    CUtensorMap tmW;
+    unsigned long long tag = 0;
+    if (ps.sk_tiles > 0) {
+      sk_ws = reinterpret_cast<float*>(d->scratch + pack_ws);
+      sk_sync = reinterpret_cast<unsigned long long*>(
+          d->scratch + pack_ws + round_up(sk_partial_bytes(ps), 256));
+      s = make_map_partials(&tmW, sk_ws, ps);
+      if (s != GEMM_OK) return s;
+      tag = next_noalloc_tag(d);
+    }
     CUtensorMap tmC;
     const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
-    return from_cuda(launch_gemm_bf16_pair(tmA, tmB, tma_c ? &tmC : nullptr, C,
-                                           ldc, m, n, k, vec_c, max_pairs,
-                                           d->status, epi_identity(), stream));
+    return from_cuda(launch_gemm_bf16_pair(
+        tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
+        ldc, m, n, ps, sk_sync, tag, vec_c, d->status, epi_identity(), stream));
   }
   const int64_t tiles =
       ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
@@ -753,6 +931,9 @@ void gemm_shutdown(void) {
     if (d.pool || d.up || d.down) {
       if (cudaSetDevice(i) == cudaSuccess) {
         cudaDeviceSynchronize();
+        for (StreamScratch& x : d.scratch)
+          if (x.ptr) cudaFreeAsync(x.ptr, 0);
+        cudaDeviceSynchronize();
         if (d.pool) cudaMemPoolDestroy(d.pool);
         if (d.up) cudaStreamDestroy(d.up);
         if (d.down) cudaStreamDestroy(d.down);
@@ -764,7 +945,54 @@ void gemm_shutdown(void) {
   cudaGetLastError();
 }
 
-int gemm_abi_version(void) { return 1; }
+int gemm_abi_version(void) { return 2; }
+
+int gemm_set_bf16_schedule(int schedule) {
+  if (schedule < GEMM_SCHEDULE_AUTO || schedule > GEMM_SCHEDULE_COLUMN_SPLIT)
+    return -1;
+  return g_schedule.exchange(schedule);
+}
+
+int64_t gemm_pair_units(int64_t M, int64_t N, int64_t K, int32_t max_pairs,
+                        int32_t schedule, int32_t pair, int64_t* out,
+                        int64_t cap) {
+  if (M < 0 || N < 0 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return -1;
+  if (max_pairs < 1 || pair < 0 || pair >= max_pairs) return -1;
+  if (schedule < GEMM_SCHEDULE_AUTO || schedule > GEMM_SCHEDULE_COLUMN_SPLIT)
+    return -1;
+  if (cap > 0 && out == nullptr) return -1;
+  const PairSchedule ps = pair_schedule(M, N, K, max_pairs, schedule);
+  if (pair >= ps.pairs) return 0;
+  WorkIter wi;
+  wi.init(ps, pair);
+  WorkUnit w;
+  int64_t n = 0;
+  while (wi.next(ps, ps.pairs, w)) {
+    if (n < cap) {
+      int64_t* o = out + 9 * n;
+      o[6] = w.tile >= ps.dp_tiles ? 1 : 0;
+      o[7] = w.n_off;
+      o[8] = w.width;
+      o[0] = w.tile;
+      o[1] = w.k0;
+      o[2] = w.k1;
+      const bool whole = w.k0 == 0 && w.k1 == ps.num_kb;
+      if (whole) {
+        o[3] = -1;
+        o[4] = pair;
+        o[5] = 1;
+      } else {
+        const SkTile st = sk_tile(ps, w.tile);
+        o[3] = sk_slot(ps, pair, w.tile);
+        o[4] = st.q_first;
+        o[5] = st.nseg;
+      }
+    }
+    ++n;
+  }
+  return n;
+}
 
 gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns) {
   if (mode < 0 || mode > 1) return GEMM_ERR_INVALID_ARG;

@@ -18,7 +18,9 @@ struct EpiParams {
   int act;             // 0 identity, 1 ReLU
 };
 
-inline EpiParams epi_identity() { return EpiParams{1.0f, 0.0f, nullptr, 0}; }
+__host__ __device__ inline EpiParams epi_identity() {
+  return EpiParams{1.0f, 0.0f, nullptr, 0};
+}
 
 __device__ __forceinline__ float epi_apply(const EpiParams& e, float acc,
                                            float c_old, float bias) {

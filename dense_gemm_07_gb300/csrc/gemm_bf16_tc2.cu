@@ -7,10 +7,20 @@
 // computed by two SMs together ("Production tensor-core kernels use larger
 // tiles", same section of "GEMM, step by step").
 //
-// Wave tail: when the tiles left for the last wave fill at most half of the
-// resident pairs, each of them is computed as two 256 x 128 units (an N=128
-// pair MMA, one 64-column box of B per CTA), so that wave takes half as long.
-// Every output element is still one tile's k-sum in one accumulator.
+// Work sharing (stream_k.cuh): whole tiles round-robin over the resident
+// pairs while they fill whole waves.  A last wave that fills at most half of
+// the pairs runs as 256 x 128 units (an N = 128 pair MMA, one 64-column box
+// of B per CTA), so that it takes about half as long.  In a stream-K
+// schedule the last wave's tiles (and, with two or more whole waves, those
+// of the last whole wave) are instead cut into equal runs of k-slices, one
+// per pair, which every pair computes before its whole tiles.  A tile cut
+// into segments is finished by the epilogue warp that arrives last
+// on the tile's ticket: the others store their partial sums to a workspace
+// and raise a ready flag; the last one adds all segments in k order (its own
+// from tensor memory) and applies the output step.  No warp waits for work
+// that has not started: a flag is only awaited after its writer has taken
+// its ticket.  Partial sums move through the same staging boxes and copy
+// engine as C, so the fix-up traffic is bulk traffic.
 //
 // sm_103a realisation: clusters of two CTAs, one per SM.  CTA r of the pair
 // owns rows [128r, 128r+128) of the 256-row tile and stages only those rows
@@ -19,8 +29,7 @@
 // reads A and B from both CTAs' shared memory and writes each CTA's 128 rows
 // of D into that CTA's tensor memory.  Per SM this halves the bytes that
 // have to be copied into shared memory per FLOP compared with one SM
-// computing a 128 x 256 tile, which is what lets six 32 KB stages keep the
-// tensor core busy.
+// computing a 128 x 256 tile.
 //
 // Roles (192 threads per CTA):
 //   warp 0 (both CTAs)  TMA producer.  Both CTAs' copies count their bytes on
@@ -28,23 +37,24 @@
 //                       for 64 KB per stage.
 //   warp 1 (even CTA)   MMA issuer: waits on "full", issues 4 pair MMAs per
 //                       stage, commits to "empty" in both CTAs, and after the
-//                       last slice of a tile to "accumulator full" in both.
+//                       last slice of a unit to "accumulator full" in both.
 //   warps 2-5 (both)    epilogue: TMEM -> registers -> swizzled shared
 //                       staging box -> TMA tensor store of C (whole lines;
 //                       rows/columns outside C are clipped), or guarded
 //                       direct stores when C's layout does not allow TMA;
 //                       then arrive on the even CTA's "accumulator empty"
-//                       (8 arrivals per tile).
+//                       (8 arrivals per unit).
 // Tensor memory: NUM_ACC 256-column FP32 accumulators per CTA; with two, a
-// tile's epilogue overlaps the next tile's MMAs.  Every wait is bounded; on expiry
-// the CTA raises its own and its peer's abort flag and the status word, all
-// roles unwind, copies and MMAs in flight are drained, and both CTAs meet at
-// a final cluster barrier before tensor memory is released.
+// unit's epilogue overlaps the next unit's MMAs.  Every wait is bounded; on
+// expiry the CTA raises its own and its peer's abort flag and the status
+// word, all roles unwind, copies and MMAs in flight are drained, and both
+// CTAs meet at a final cluster barrier before tensor memory is released.
 #include <cstdint>
 #include <cstring>
 
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "stream_k.cuh"
 #include "tile_order.cuh"
 
 namespace g07 {
@@ -54,8 +64,8 @@ constexpr int PAIR_M = 256;                       // rows per pair tile
 constexpr int CTA_M = 128;                        // rows per CTA
 constexpr int BN = 256;                           // columns per pair tile
 constexpr int CTA_N = 128;                        // B columns staged per CTA
-constexpr int BK = 64;
-constexpr int STAGES = 6;
+constexpr int BK = kPairTileK;                    // 64: one 128-byte A row
+constexpr int STAGES = kPairStages;               // 6
 constexpr int A_STAGE_BYTES = CTA_M * BK * 2;     // 16 KB
 constexpr int B_BOX_COLS = 64;
 constexpr int B_BOX_BYTES = BK * B_BOX_COLS * 2;  // 8 KB
@@ -69,6 +79,7 @@ constexpr int EPI_WARPS = 4;
 constexpr int EPI_BOX_BYTES = 32 * 32 * 4;            // one 32 x 32 FP32 box
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BOX_BYTES;  // double-buffered
 constexpr int GROUP = 8;
+static_assert(BK == kSkSliceK, "stream-K slices are pipeline k-slices");
 
 struct alignas(8) PairControl {
   uint64_t full[STAGES];      // used in the even CTA only
@@ -76,32 +87,10 @@ struct alignas(8) PairControl {
   uint64_t acc_full[NUM_ACC];
   uint64_t acc_empty[NUM_ACC];  // used in the even CTA only (8 arrivals)
   uint64_t drain;
+  uint64_t part[EPI_WARPS];     // per epilogue warp: partial-sum box loaded
   uint32_t tmem_base;
   int abort;
 };
-
-// One unit of work: a 256-row tile of C, columns [n0, n0 + width).
-struct Unit {
-  int m0;
-  int n0;
-  int width;
-};
-
-__device__ __forceinline__ Unit unit_of(int unit, int num_full, int split,
-                                        int tiles_m, int tiles_n) {
-  int tile = unit, piece = 0, width = BN;
-  if (unit >= num_full) {
-    tile = num_full + (unit - num_full) / split;
-    piece = (unit - num_full) % split;
-    width = BN / split;
-  }
-  const TileCoord tc = tile_order(tile, tiles_m, tiles_n, GROUP);
-  Unit u;
-  u.m0 = tc.m * PAIR_M;
-  u.n0 = tc.n * BN + piece * width;
-  u.width = width;
-  return u;
-}
 
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, uint64_t tmo) {
@@ -128,12 +117,12 @@ struct Ring {
   }
 };
 
-// Producer for one unit of width W: per k-slice, wait for the stage to be
-// free, arm the even CTA's "full" barrier (even CTA only), copy this CTA's
-// 128 rows of A and W/2 columns of B.
+// Producer for one unit of width W: per k-slice in [k0, k1), wait for the
+// stage to be free, arm the even CTA's "full" barrier (even CTA only), copy
+// this CTA's 128 rows of A and W / 2 columns of B.
 template <int W>
-__device__ __forceinline__ bool produce_unit(const Unit& u, Ring& ring,
-                                             int num_kb, uint8_t* smem,
+__device__ __forceinline__ bool produce_unit(int m0, int n0, int k0, int k1,
+                                             Ring& ring, uint8_t* smem,
                                              PairControl* ctl,
                                              const CUtensorMap* tmA,
                                              const CUtensorMap* tmB,
@@ -142,11 +131,11 @@ __device__ __forceinline__ bool produce_unit(const Unit& u, Ring& ring,
                                              bool skip_first) {
   constexpr int BOXES = W / 2 / B_BOX_COLS;
   constexpr uint32_t TX = 2u * (A_STAGE_BYTES + BOXES * B_BOX_BYTES);
-  const int a_row = u.m0 + static_cast<int>(rank) * CTA_M;
-  const int b_col = u.n0 + static_cast<int>(rank) * (W / 2);
-  for (int kb = 0; kb < num_kb; ++kb) {
+  const int a_row = m0 + static_cast<int>(rank) * CTA_M;
+  const int b_col = n0 + static_cast<int>(rank) * (W / 2);
+  for (int kb = k0; kb < k1; ++kb) {
     if (!mbar_wait(&ctl->empty[ring.stage], ring.phase ^ 1u, abort, tmo)) return false;
-    if (skip_first && kb == 0) {
+    if (skip_first && kb == k0) {
       // Test fault: this k-slice is never copied, so the MMA's wait for it
       // runs out and the kernel unwinds with a timeout status.
       ring.advance();
@@ -169,15 +158,16 @@ __device__ __forceinline__ bool produce_unit(const Unit& u, Ring& ring,
   return true;
 }
 
-// MMA issue for one unit of width W into the accumulator at d_tmem.
+// MMA issue for k-slices [k0, k1) of one unit of width W into the
+// accumulator at d_tmem (the first slice overwrites it).
 template <int W>
-__device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
-                                         int num_kb, uint8_t* smem,
+__device__ __forceinline__ bool mma_unit(uint32_t d_tmem, int k0, int k1,
+                                         Ring& ring, uint8_t* smem,
                                          PairControl* ctl,
                                          volatile int* abort, uint64_t tmo) {
   constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, W, /*a_mn_major=*/false,
                                             /*b_mn_major=*/true);
-  for (int kb = 0; kb < num_kb; ++kb) {
+  for (int kb = k0; kb < k1; ++kb) {
     if (!mbar_wait(&ctl->full[ring.stage], ring.phase, abort, tmo)) return false;
     tc_fence_after_sync();
     const uint32_t a_addr = smem_u32(smem + ring.stage * STAGE_BYTES);
@@ -190,7 +180,8 @@ __device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
       // apart (SBO); a 16-deep k step is 16 rows = 2 KB in.
       const uint64_t bdesc =
           sdesc_sw128(b_addr + kk * MMA_K * 128, B_BOX_BYTES, 1024);
-      mma_f16_ss_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+      mma_f16_ss_pair(d_tmem, adesc, bdesc, IDESC,
+                      (kb != k0 || kk != 0) ? 1u : 0u);
     }
     mma_commit_pair(&ctl->empty[ring.stage], 0x3);
     ring.advance();
@@ -198,7 +189,143 @@ __device__ __forceinline__ bool mma_unit(uint32_t d_tmem, Ring& ring,
   return true;
 }
 
-// Epilogue of one unit: this thread's row, W columns from TMEM to C.
+// ------------------------------------------------------ stream-K fix-up
+//
+// Partial sums live in an FP32 workspace of 256 columns whose rows are, per
+// stream-K pair q, slot (0: its first segment, 1: its last), CTA rank and
+// epilogue warp, the warp's 32 rows of the accumulator:
+//   row = ((q * 2 + slot) * 2 + rank) * 128 + warp * 32 + lane.
+// It is read and written in 32 x 32 boxes by the copy engine (tensor map
+// tmW, same box and swizzle as C's).
+__device__ __forceinline__ int sk_row(int q, int slot, uint32_t rank, int wq) {
+  return ((q * 2 + slot) * 2 + static_cast<int>(rank)) * CTA_M + wq * 32;
+}
+
+// Synchronisation words, 64-bit, tagged with the launch so that nothing has
+// to be cleared between launches: ticket counters [sk_tiles][rank 2][warp 4]
+// hold (tag << 8) | arrivals, ready flags [sk_pairs][slot 2][rank 2][warp 4]
+// hold the tag once the slot's partial sums are stored.  A word with another
+// tag counts as zero.
+__device__ __forceinline__ unsigned long long* sk_ticket(
+    unsigned long long* sync, const PairSchedule& s, int tile, uint32_t rank,
+    int wq) {
+  return sync + (static_cast<int64_t>(tile - s.dp_tiles) * 2 + rank) * 4 + wq;
+}
+__device__ __forceinline__ unsigned long long* sk_ready(
+    unsigned long long* sync, const PairSchedule& s, int q, int slot,
+    uint32_t rank, int wq) {
+  return sync + static_cast<int64_t>(s.sk_tiles) * 8 +
+         ((static_cast<int64_t>(q) * 2 + slot) * 2 + rank) * 4 + wq;
+}
+
+// Take this launch's next ticket of a counter (0 = first arrival).  At most
+// kSkMaxSeg warps contend, so the exchange loop ends after a few rounds; it
+// is bounded all the same (-1: gave up).
+__device__ __forceinline__ int sk_take_ticket(unsigned long long* w,
+                                              unsigned long long tag) {
+  unsigned long long cur = atomicAdd(w, 0ull);
+  for (int i = 0; i < 1024; ++i) {
+    const bool same = (cur >> 8) == tag;
+    const unsigned long long want = same ? cur + 1 : ((tag << 8) | 1ull);
+    const unsigned long long prev = atomicCAS(w, cur, want);
+    if (prev == cur) return same ? static_cast<int>(cur & 0xFFull) : 0;
+    cur = prev;
+  }
+  return -1;
+}
+
+// Wait (bounded) until a ready flag holds this launch's tag.
+__device__ __forceinline__ bool sk_wait_ready(const unsigned long long* f,
+                                              unsigned long long tag,
+                                              volatile int* abort,
+                                              uint64_t limit_ns) {
+  if (ld_acquire_gpu_u64(f) == tag) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_gpu_u64(f) == tag) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// What the finishing warp needs to add up one tile's segments.
+struct SkCombine {
+  const CUtensorMap* tmW;
+  const PairSchedule* sched;
+  int tile, q_first, nseg, mine;
+  uint32_t rank;
+  int wq;
+  uint64_t* bar;        // this warp's "partial box loaded" barrier
+  uint32_t* bar_uses;   // its completed phases
+  volatile int* abort;
+  uint64_t tmo;
+};
+
+// Row `lane` of a swizzled 32 x 32 FP32 staging box (the layout both the
+// epilogue writes and TMA loads produce).
+__device__ __forceinline__ void box_read_row(const uint8_t* buf, int lane,
+                                             float (&v)[32]) {
+  const uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 x = *reinterpret_cast<const float4*>(rowp + ((j ^ (lane & 7)) << 4));
+    v[4 * j] = x.x;
+    v[4 * j + 1] = x.y;
+    v[4 * j + 2] = x.z;
+    v[4 * j + 3] = x.w;
+  }
+}
+
+// Replace this lane's 32 accumulator values of column chunk c by the sum of
+// every segment's values in segment (k) order, loading the other segments'
+// boxes through `buf` (free on entry).  False: a wait ran out.
+__device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
+                                              const SkCombine& cb, int c,
+                                              uint8_t* buf, int lane) {
+  float acc[32];
+#pragma unroll 1
+  for (int s = 0; s < cb.nseg; ++s) {
+    float v[32];
+    if (s == cb.mine) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    } else {
+      const int q = cb.q_first + s;
+      const uint32_t parity = *cb.bar_uses & 1u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(cb.bar, EPI_BOX_BYTES);
+        tma_load_2d(buf, cb.tmW, cb.bar, c * 32,
+                    sk_row(q, sk_slot(*cb.sched, q, cb.tile), cb.rank, cb.wq));
+      }
+      ++*cb.bar_uses;
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(cb.bar, parity, cb.abort, cb.tmo) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return false;
+      box_read_row(buf, lane, v);
+      // all lanes have read the box before the copy engine refills it
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    if (s == 0) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = v[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] += v[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i]);
+  return true;
+}
+
+// ------------------------------------------------------------ output step
+
+// Epilogue of one unit of width W: this thread's row, W columns from TMEM
+// to C.
 template <int W>
 __device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
                                            int64_t ldc, int row, int n0, int M,
@@ -241,15 +368,20 @@ __device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
 // chunk the warp writes its 32 x 32 block into a 128-byte-swizzled staging
 // box (each lane one row, conflict-free 16-byte stores) and one lane stores
 // the box with the copy engine, which writes whole lines and clips rows and
-// columns outside C.  Two staging boxes per warp alternate.
+// columns outside the tensor.  Two staging boxes per warp alternate.  With
+// cb set, each chunk is first combined with the other segments' partial
+// sums (loaded into the same box); tmOut is C's map, or the workspace's
+// when a segment leaves its partial sums (identity epilogue, M = N = the
+// workspace's extent).  W: the unit's width.  False: a wait ran out.
 template <int W>
-__device__ __forceinline__ void store_unit_tma(uint32_t taddr,
-                                               const CUtensorMap* tmC,
+__device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
+                                               const CUtensorMap* tmOut,
                                                uint8_t* ebuf, int row0, int n0,
                                                int M, int N, int lane,
                                                int& chunk, const float* C,
                                                int64_t ldc,
-                                               const EpiParams& epi) {
+                                               const EpiParams& epi,
+                                               const SkCombine* cb) {
 #pragma unroll 1
   for (int c = 0; c < W / 32; ++c) {
     // Boxes wholly outside C are skipped (warp-uniform test); every other
@@ -262,6 +394,7 @@ __device__ __forceinline__ void store_unit_tma(uint32_t taddr,
     if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
     __syncwarp();
     tmem_ld_wait();
+    if (cb && !combine_chunk(r, *cb, c, buf, lane)) return false;
     if (epi.alpha != 1.0f || epi.beta != 0.0f || epi.bias != nullptr || epi.act != 0) {
       // Fused epilogue on this lane's row (N % 4 == 0 on this path, so each
       // 16-byte group is wholly inside or outside C).
@@ -292,20 +425,59 @@ __device__ __forceinline__ void store_unit_tma(uint32_t taddr,
     __syncwarp();
     // partial boxes are clipped by the copy engine
     if (lane == 0) {
-      tma_store_2d(tmC, buf, n0 + c * 32, row0);
+      tma_store_2d(tmOut, buf, n0 + c * 32, row0);
       bulk_commit();
     }
   }
+  return true;
+}
+
+// Direct-store epilogue of a full-width unit (C's layout does not allow TMA
+// stores), combined with the other segments' partial sums when cb is set;
+// the partial boxes are loaded through this warp's first staging box.
+__device__ __forceinline__ bool store_unit_direct(uint32_t taddr, float* C,
+                                                  int64_t ldc, int row, int n0,
+                                                  int M, int N, int vec_c,
+                                                  const EpiParams& epi,
+                                                  const SkCombine* cb,
+                                                  uint8_t* ebuf, int lane) {
+  if (!cb) {
+    store_unit<BN>(taddr, C, ldc, row, n0, M, N, vec_c, epi);
+    return true;
+  }
+  // the staging box may still be read by a partial-sum store of this warp
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  float* crow = C + static_cast<int64_t>(row) * ldc;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    tmem_ld_wait();
+    if (!combine_chunk(r, *cb, c, ebuf, lane)) return false;
+    const int gn = n0 + c * 32;
+    if (row < M) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gn + j < N)
+          crow[gn + j] = epi_apply(epi, __uint_as_float(r[j]),
+                                   epi.beta != 0.0f ? crow[gn + j] : 0.0f,
+                                   epi.bias ? epi.bias[gn + j] : 0.0f);
+    }
+  }
+  return true;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC,
-                      float* __restrict__ C, int64_t ldc, int M, int N, int K,
-                      int tiles_m, int tiles_n, int num_full, int split,
-                      int vec_c, int tma_c, unsigned int* __restrict__ status,
-                      EpiParams epi) {
+                      const __grid_constant__ CUtensorMap tmW,
+                      float* __restrict__ C, int64_t ldc, int M, int N,
+                      const PairSchedule sched,
+                      unsigned long long* __restrict__ sk_sync,
+                      unsigned long long sk_tag, int vec_c, int tma_c,
+                      unsigned int* __restrict__ status, EpiParams epi) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
@@ -319,11 +491,6 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const bool even = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
-  const int num_tiles = tiles_m * tiles_n;
-  // Work units: tiles [0, num_full) at full width, then every remaining tile
-  // as `split` column pieces of BN / split (the last, partial wave).
-  const int num_units = num_full + (num_tiles - num_full) * split;
-  const int num_kb = (K + BK - 1) / BK;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -335,6 +502,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(&ctl->acc_empty[a], 8);  // 4 epilogue warps x 2 CTAs
     }
     mbar_init(&ctl->drain, 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&ctl->part[w], 1);
     ctl->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -360,14 +528,18 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       int last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       bool ok = true;
-      for (int unit = pair; ok && unit < num_units; unit += num_pairs) {
-        const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
-        const bool skip = fault == 1 && unit == pair;
-        ok = u.width == BN
-                 ? produce_unit<BN>(u, ring, num_kb, smem, ctl, &tmA, &tmB, rank,
-                                    last_phase, abort, tmo, skip)
-                 : produce_unit<BN / 2>(u, ring, num_kb, smem, ctl, &tmA, &tmB,
-                                        rank, last_phase, abort, tmo, skip);
+      WorkIter wi;
+      wi.init(sched, pair);
+      WorkUnit w;
+      for (bool first = true; ok && wi.next(sched, num_pairs, w); first = false) {
+        const TileCoord tc = tile_order(w.tile, sched.tiles_m, sched.tiles_n, GROUP);
+        const int m0 = tc.m * PAIR_M, n0 = tc.n * BN + w.n_off;
+        const bool skip = fault == 1 && first;
+        ok = w.width == BN
+                 ? produce_unit<BN>(m0, n0, w.k0, w.k1, ring, smem, ctl, &tmA, &tmB,
+                                    rank, last_phase, abort, tmo, skip)
+                 : produce_unit<BN / 2>(m0, n0, w.k0, w.k1, ring, smem, ctl, &tmA,
+                                        &tmB, rank, last_phase, abort, tmo, skip);
       }
       if (!ok) raise_abort(abort, peer_abort, status);
       // The even CTA's "full" barriers count both CTAs' copies: every phase
@@ -385,9 +557,10 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       Ring ring;
       bool ok = true;
       bool issued = false;
-      int t = 0;
-      for (int unit = pair; ok && unit < num_units; unit += num_pairs, ++t) {
-        const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
+      WorkIter wi;
+      wi.init(sched, pair);
+      WorkUnit w;
+      for (int t = 0; ok && wi.next(sched, num_pairs, w); ++t) {
         const int acc = t % NUM_ACC;
         const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
         if (!pair_wait(&ctl->acc_empty[acc], acc_phase ^ 1u, abort, tmo)) {
@@ -396,9 +569,10 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        issued |= num_kb > 0;
-        ok = u.width == BN ? mma_unit<BN>(d_tmem, ring, num_kb, smem, ctl, abort, tmo)
-                           : mma_unit<BN / 2>(d_tmem, ring, num_kb, smem, ctl, abort, tmo);
+        issued |= w.k1 > w.k0;
+        ok = w.width == BN
+                 ? mma_unit<BN>(d_tmem, w.k0, w.k1, ring, smem, ctl, abort, tmo)
+                 : mma_unit<BN / 2>(d_tmem, w.k0, w.k1, ring, smem, ctl, abort, tmo);
         if (!ok) break;
         mma_commit_pair(&ctl->acc_full[acc], 0x3);
       }
@@ -415,8 +589,11 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     const int q = warp & 3;
     uint8_t* ebuf = epi_smem + (warp - 2) * 2 * EPI_BOX_BYTES;
     int chunk = 0;
-    int t = 0;
-    for (int unit = pair; unit < num_units; unit += num_pairs, ++t) {
+    uint32_t part_uses = 0;
+    WorkIter wi;
+    wi.init(sched, pair);
+    WorkUnit w;
+    for (int t = 0; wi.next(sched, num_pairs, w); ++t) {
       const int acc = t % NUM_ACC;
       const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
       int ok = 0;
@@ -427,27 +604,97 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       }
       tc_fence_after_sync();
-      const Unit u = unit_of(unit, num_full, split, tiles_m, tiles_n);
-      const int row = u.m0 + static_cast<int>(rank) * CTA_M + q * 32 + lane;
+      const TileCoord tc = tile_order(w.tile, sched.tiles_m, sched.tiles_n, GROUP);
+      const int m0 = tc.m * PAIR_M, n0 = tc.n * BN + w.n_off;
+      const int row = m0 + static_cast<int>(rank) * CTA_M + q * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int row0 = row - lane;
-      if (tma_c) {
-        if (u.width == BN)
-          store_unit_tma<BN>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane, chunk,
-                             C, ldc, epi);
-        else
-          store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, u.n0, M, N, lane,
-                                 chunk, C, ldc, epi);
-      } else if (u.width == BN) {
-        store_unit<BN>(taddr, C, ldc, row, u.n0, M, N, vec_c, epi);
-      } else {
-        store_unit<BN / 2>(taddr, C, ldc, row, u.n0, M, N, vec_c, epi);
+
+      int ready_slot = -1;  // >= 0: partial sums left in this slot
+      SkCombine cb;
+      const SkCombine* cbp = nullptr;
+      bool good = true;
+      if (w.k0 != 0 || w.k1 != sched.num_kb) {
+        // A stream-K segment: take a ticket; the last of the tile's
+        // segments finishes it, the others leave their partial sums.
+        const SkTile st = sk_tile(sched, w.tile);
+        int ticket = 0;
+        if (lane == 0)
+          ticket = sk_take_ticket(sk_ticket(sk_sync, sched, w.tile, rank, q), sk_tag);
+        ticket = __shfl_sync(0xffffffffu, ticket, 0);
+        if (ticket < 0) {
+          good = false;
+        } else if (ticket + 1 < st.nseg) {
+          ready_slot = sk_slot(sched, pair, w.tile);
+          good = store_unit_tma<BN>(taddr, &tmW, ebuf,
+                                    sk_row(pair, ready_slot, rank, q), 0,
+                                    0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
+                                    epi_identity(), nullptr);
+        } else {
+          cb.tmW = &tmW;
+          cb.sched = &sched;
+          cb.tile = w.tile;
+          cb.q_first = st.q_first;
+          cb.nseg = st.nseg;
+          cb.mine = pair - st.q_first;
+          cb.rank = rank;
+          cb.wq = q;
+          cb.bar = &ctl->part[q];
+          cb.bar_uses = &part_uses;
+          cb.abort = abort;
+          cb.tmo = tmo;
+          // Every other segment's writer has taken its ticket, so it is
+          // running; wait (bounded) until its partial sums are stored.
+          int got = 1;
+          if (lane == 0) {
+            for (int sg = 0; got && sg < st.nseg; ++sg) {
+              if (sg == cb.mine) continue;
+              const int qq = st.q_first + sg;
+              got = sk_wait_ready(sk_ready(sk_sync, sched, qq, sk_slot(sched, qq, w.tile), rank, q),
+                                  sk_tag, abort, tmo) ? 1 : 0;
+            }
+            // the flags were read by this thread; the boxes will be read by
+            // the copy engine
+            fence_proxy_async_global();
+          }
+          got = __shfl_sync(0xffffffffu, got, 0);
+          good = got != 0;
+          cbp = &cb;
+        }
+      }
+      if (good && ready_slot < 0) {
+        if (w.width != BN) {
+          // a column-split unit of the last wave (never a stream-K segment)
+          if (tma_c)
+            store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
+                                   chunk, C, ldc, epi, nullptr);
+          else
+            store_unit<BN / 2>(taddr, C, ldc, row, n0, M, N, vec_c, epi);
+        } else {
+          good = tma_c ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N,
+                                            lane, chunk, C, ldc, epi, cbp)
+                       : store_unit_direct(taddr, C, ldc, row, n0, M, N, vec_c,
+                                           epi, cbp, ebuf, lane);
+        }
+      }
+      if (!good) {
+        if (lane == 0) raise_abort(abort, peer_abort, status);
+        break;
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0)
+      if (lane == 0) {
         mbar_arrive_cluster(map_to_rank(smem_u32(&ctl->acc_empty[acc]), 0));
+        if (ready_slot >= 0) {
+          // The partial sums are in global memory (copies complete) before
+          // the flag says so.
+          bulk_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+          st_release_gpu_u64(sk_ready(sk_sync, sched, pair, ready_slot, rank, q), sk_tag);
+        }
+      }
     }
     // Every store issued must have completed before the CTA exits.
     if (lane == 0) bulk_wait_all();
@@ -511,38 +758,35 @@ int pair_max_active(cudaStream_t stream) {
 }
 
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                  const CUtensorMap* tmC, float* C, int64_t ldc,
-                                  int M, int N, int K, bool vec_c, int max_pairs,
+                                  const CUtensorMap* tmC, const CUtensorMap* tmW,
+                                  float* C, int64_t ldc, int M, int N,
+                                  const PairSchedule& sched,
+                                  unsigned long long* sk_sync,
+                                  unsigned long long sk_tag, bool vec_c,
                                   unsigned int* status, const EpiParams& epi,
                                   cudaStream_t stream) {
-  const int tiles_m = (M + PAIR_M - 1) / PAIR_M;
-  const int tiles_n = (N + BN - 1) / BN;
-  const int tiles = tiles_m * tiles_n;
-  // A last wave that fills at most half of the pairs runs as half-width
-  // units instead, so it takes half as long.
-  const int tail = tiles % max_pairs;
-  const int split = (tail > 0 && 2 * tail <= max_pairs) ? 2 : 1;
-  const int num_full = split == 2 ? tiles - tail : tiles;
-  const int units = num_full + (tiles - num_full) * split;
-  const int pairs = units < max_pairs ? units : max_pairs;
+  if (sched.pairs <= 0) return cudaErrorInvalidValue;
+  if (sched.sk_tiles > 0 &&
+      (tmW == nullptr || sk_sync == nullptr || sk_tag == 0 || (sk_tag >> 56) != 0))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.pairs), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = pair_smem_bytes();
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   CUtensorMap unused;
-  if (tmC == nullptr) std::memset(&unused, 0, sizeof(unused));
+  std::memset(&unused, 0, sizeof(unused));
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused, C, ldc, M, N,
-      K, tiles_m, tiles_n, num_full, split, vec_c ? 1 : 0, tmC ? 1 : 0, status,
-      epi);
+      &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused,
+      tmW ? *tmW : unused, C, ldc, M, N, sched, sk_sync, sk_tag, vec_c ? 1 : 0,
+      tmC ? 1 : 0, status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "epilogue.cuh"
+#include "stream_k.cuh"
 
 namespace g07 {
 
@@ -57,18 +58,28 @@ cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
 // ---- BF16 tensor-core path on SM pairs (gemm_bf16_tc2.cu): 256 x 256 tiles
 constexpr int kPairTileM = 256;
 constexpr int kPairTileN = 256;
+constexpr int kPairTileK = 64;
 constexpr int kPairStages = 6;
 
 size_t pair_smem_bytes();
 // Clusters of two CTAs that can be resident at once (0 if the pair kernel
 // cannot run on this device).
 int pair_max_active(cudaStream_t stream);
-// `max_pairs` clusters at most (persistent); the last wave may be split.
-// tmC: FP32 tensor map of C (box 32 x 32, 128-byte swizzle) for TMA stores,
-// or nullptr to store directly from registers.
+// tmA: box {64, 128}, tmB: box {64, 64}, both 128-byte swizzled.  tmC: FP32
+// map of C (box 32 x 32, 128-byte swizzle) for TMA stores, or nullptr to
+// store directly from registers.  sched: work sharing from pair_schedule()
+// (stream_k.cuh); sched.pairs clusters are launched.  When sched.sk_tiles >
+// 0: tmW maps the partial-sum workspace (FP32, 256 columns,
+// sched.sk_pairs * 512 rows, box 32 x 32, 128-byte swizzle), sk_sync points
+// at sk_sync_words(sched) 64-bit words of any content, and sk_tag is this
+// launch's tag (nonzero, below 2^56, not used by an earlier launch on the
+// same words).
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                  const CUtensorMap* tmC, float* C, int64_t ldc,
-                                  int M, int N, int K, bool vec_c, int max_pairs,
+                                  const CUtensorMap* tmC, const CUtensorMap* tmW,
+                                  float* C, int64_t ldc, int M, int N,
+                                  const PairSchedule& sched,
+                                  unsigned long long* sk_sync,
+                                  unsigned long long sk_tag, bool vec_c,
                                   unsigned int* status, const EpiParams& epi,
                                   cudaStream_t stream);
 

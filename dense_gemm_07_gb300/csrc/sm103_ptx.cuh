@@ -89,6 +89,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------- flags in global memory
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(
+    const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];"
+               : "=l"(v)
+               : "l"(reinterpret_cast<uint64_t>(p))
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p,
+                                                   unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(
+                   reinterpret_cast<uint64_t>(p)),
+               "l"(v)
+               : "memory");
+}
+
+// Order this thread's global-memory accesses through the generic proxy
+// with those of the copy engine (async proxy), in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -279,6 +305,28 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   float v;
   asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
+}
+
+// 16 TMEM lanes x 256 bits, repeated 8 times along the columns (64 FP32
+// columns).  Thread t receives, for j = 0..7, columns 8j + 2(t % 4) and
+// 8j + 2(t % 4) + 1 of lane t / 4 in r[4j], r[4j + 1] and of lane t / 4 + 8
+// in r[4j + 2], r[4j + 3] (lanes relative to the address, whose lane field
+// is a multiple of 16 inside the warp's quarter).
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr,
+                                                   uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]),
+        "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -280,7 +280,65 @@ typedef struct gemm_plan {
     int64_t workspace_bytes; /* device scratch the call takes from the pool */
     int32_t pack_a;        /* 1 if A is first copied to aligned workspace    */
     int32_t pack_b;        /* 1 if B is first copied to aligned workspace    */
+    /* BF16 paired-SM path only (0 elsewhere); reported for the 76 resident
+     * SM pairs of a 152-SM GB300 under the current gemm_set_bf16_schedule: */
+    int64_t dp_tiles;      /* tiles computed whole, round-robin over pairs   */
+    int64_t sk_tiles;      /* tiles after them split into runs of k-slices
+                              shared evenly by sk_pairs pairs (stream-K)     */
+    int32_t sk_pairs;      /* pairs sharing the stream-K slices              */
+    int32_t pairs;         /* SM pairs launched                              */
 } gemm_plan_t;
+
+/*
+ * How the BF16 paired-SM kernel (M > 128) shares out a partial last wave of
+ * 256 x 256 tiles ("GEMM Optimization", section "L2 Cache and Wave Analysis":
+ * a partial last wave leaves SMs idle).
+ *   GEMM_SCHEDULE_AUTO: a last wave that fills at most half of the SM pairs
+ *       runs as 256 x 128 units; stream-K only when there are fewer tiles
+ *       than half the pairs and K has at least 96 64-deep slices.  Default.
+ *   GEMM_SCHEDULE_STREAM_K: wherever it applies (a last wave at most 85 %
+ *       full, K at least 8 slices), the last wave's tiles -- and with two or
+ *       more whole waves also the last whole wave's -- are cut into equal
+ *       runs of k-slices, one per pair; a tile cut into segments is finished
+ *       by adding the segments' partial sums in k order.  Needs 512 KB of
+ *       device scratch per SM pair, kept per stream between calls.
+ *   GEMM_SCHEDULE_COLUMN_SPLIT: never split along K.
+ * Every schedule gives the same results up to the order of FP32 additions
+ * across a split tile; each is deterministic run to run.
+ */
+typedef enum gemm_schedule {
+    GEMM_SCHEDULE_AUTO = 0,
+    GEMM_SCHEDULE_STREAM_K = 1,
+    GEMM_SCHEDULE_COLUMN_SPLIT = 2
+} gemm_schedule_t;
+
+/*
+ * gemm_set_bf16_schedule: choose the schedule (a gemm_schedule_t) for BF16
+ * calls issued after it returns, process-wide.  Returns the previous
+ * schedule, or -1 (nothing changed) for an unknown value.  No GPU needed.
+ */
+GEMM07_API int gemm_set_bf16_schedule(int schedule);
+
+/*
+ * gemm_pair_units: the work units that SM pair `pair` computes in the BF16
+ * paired-SM kernel for an M x N x K problem when `max_pairs` pairs are
+ * resident, under `schedule` (a gemm_schedule_t), in the order it computes
+ * them (no GPU needed; a test hook for the work sharing).  Unit i is written
+ * to out[9*i .. 9*i+8] as
+ *   tile (index in the tile order), k0, k1 (64-deep k-slices [k0, k1)),
+ *   slot (-1 unless the unit is a segment of a split tile, else the pair's
+ *   partial-sum slot 0/1), first pair and number of segments of the tile
+ *   (pair, 1 when not split along K), 1 if the unit belongs to the stream-K
+ *   part, else 0, and the unit's first column within the tile and its
+ *   width (0 and 256, or 0 / 128 and 128 for the halves of a column-split
+ *   tile),
+ * for i < cap (out may be NULL when cap is 0).  Returns the number of units,
+ * or -1 for an argument out of range (sizes, max_pairs < 1, pair outside
+ * [0, max_pairs), unknown schedule).  Tiles are 256 x 256.
+ */
+GEMM07_API int64_t gemm_pair_units(int64_t M, int64_t N, int64_t K,
+                                   int32_t max_pairs, int32_t schedule,
+                                   int32_t pair, int64_t *out, int64_t cap);
 
 /*
  * gemm_plan_bf16 / gemm_plan_f32: fill *plan with the path that the

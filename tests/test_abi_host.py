@@ -44,7 +44,7 @@ def test_library_is_in_tree_and_for_sm103a():
 
 
 def test_abi_version(lib):
-    assert _abi.gemm_abi_version() == 1
+    assert _abi.gemm_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -97,6 +97,8 @@ def test_plan_paths():
     assert _path("f32", 5, 5, 0)[0] == "zero_fill"
     path, p = _path("bf16", 4096, 4096, 4096)
     assert path == "bf16_tma" and p.tiles == 16 * 16 and p.workspace_bytes == 0
+    # three whole waves on 76 pairs, the last 28 tiles as 56 half-width units
+    assert (p.dp_tiles, p.sk_tiles, p.sk_pairs, p.pairs) == (256, 0, 0, 76)
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
     path, p = _path("bf16", 129, 4096, 4096)
     assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (256, 256, 6)

@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist):
+def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist,
+          schedule=None):
     dtype = torch.float32 if kind == "f32" else torch.bfloat16
     a, b = inputs.make_pair(M, N, K, seed, dist, dtype=dtype)
     g = torch.Generator().manual_seed(seed + 1000)
@@ -25,9 +26,14 @@ def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist):
     bias = torch.randint(-4, 5, (N,), generator=g).float() if use_bias else None
     out = c0.to(DEV).clone()
     fn = g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex
-    fn(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
-       bias=bias.to(DEV) if bias is not None else None, activation=act)
-    torch.cuda.synchronize()
+    prev = _abi.gemm_set_bf16_schedule(schedule) if schedule is not None else None
+    try:
+        fn(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
+           bias=bias.to(DEV) if bias is not None else None, activation=act)
+        torch.cuda.synchronize()
+    finally:
+        if prev is not None:
+            _abi.gemm_set_bf16_schedule(prev)
     assert g7.gemm_get_device_status() == 0
     ab, s = oracle_ref(kind, a, b)
     want = oracle.gemm_epilogue(ab, alpha=alpha, beta=beta,
@@ -47,11 +53,13 @@ def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist):
 
 
 PATHS = [
-    ("bf16", 512, 768, 320),   # SM pairs, TMA-store epilogue
-    ("bf16", 300, 258, 200),   # SM pairs, N % 4 != 0: direct stores
-    ("bf16", 48, 1000, 777),   # small M, cluster reduction
-    ("f32", 640, 520, 2000),   # FP32, one partial wave split along K
-    ("f32", 2560, 2048, 640),  # FP32, whole waves + split tail
+    ("bf16", 512, 768, 320, None),   # SM pairs, TMA-store epilogue
+    ("bf16", 300, 258, 200, None),   # SM pairs, N % 4 != 0: direct stores
+    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + TMA stores
+    ("bf16", 2560, 2302, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + direct stores
+    ("bf16", 48, 1000, 777, None),   # small M, cluster reduction
+    ("f32", 640, 520, 2000, None),   # FP32, one partial wave split along K
+    ("f32", 2560, 2048, 640, None),  # FP32, whole waves + split tail
 ]
 
 
@@ -60,10 +68,10 @@ PATHS = [
                                  (-3.0, 2.0, False, "relu"), (0.5, 0.0, False, "none")],
                          ids=["ab+c+bias", "bias+relu", "beta_relu", "alpha_only"])
 def test_epilogue_exact_integers(path, epi):
-    kind, M, N, K = path
+    kind, M, N, K, schedule = path
     alpha, beta, use_bias, act = epi
     _case(kind, M, N, K, 50, alpha, beta, use_bias, act, exact=True,
-          dist=inputs.INT3)
+          dist=inputs.INT3, schedule=schedule)
 
 
 @pytest.mark.parametrize("kind", ["f32", "bf16"])

@@ -141,6 +141,81 @@ def test_bf16_linear_layer_shapes_sampled(NK):
            rows=_sample_rows(2048, 24, 3))
 
 
+# Stream-K: tiles split into runs of k-slices over several SM pairs, finished
+# by adding the segments' partial sums.  Integer inputs make every order of
+# summation exact, so the split must not change a single bit.
+@pytest.fixture
+def stream_k():
+    prev = g7.abi.gemm_set_bf16_schedule(g7.abi.SCHEDULE_STREAM_K)
+    yield
+    g7.abi.gemm_set_bf16_schedule(prev)
+
+
+@pytest.mark.parametrize("shape", [(512, 1024, 8192),    # 8 tiles halved over 16 pairs
+                                   (512, 512, 8192),     # 4 tiles, long K
+                                   (2560, 2304, 1024),   # 90 tiles: 1 wave + 14 split
+                                   (2560, 2302, 640),    # N % 4: direct stores
+                                   (3100, 3100, 700),    # 169 tiles, ragged edges
+                                   (2900, 3300, 1000)])  # 156 tiles, ragged K
+def test_bf16_stream_k_exact(stream_k, shape):
+    M, N, K = shape
+    s, p = g7.plan("bf16", M, N, K)
+    assert p.sk_tiles > 0
+    _check("bf16", M, N, K, 23, inputs.INT3, exact=True)
+
+
+def test_bf16_stream_k_chosen_automatically_for_long_k():
+    # few tiles and a long K: the automatic schedule halves each tile along K
+    M, N, K = 512, 1024, 8192
+    s, p = g7.plan("bf16", M, N, K)
+    assert (p.sk_tiles, p.sk_pairs) == (8, 16)
+    _check("bf16", M, N, K, 27, inputs.NORMAL, rows=_sample_rows(M, 32, 27))
+
+
+def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
+    # 128 tiles: one whole wave and 52 more, shared as k-slice runs
+    M, N, K = 4096, 2048, 1024
+    rows = np.unique(np.concatenate([_sample_rows(M, 40, 24),
+                                     [255, 256, 2047, 2048, 3839, 3840]]))
+    _check("bf16", M, N, K, 24, inputs.INT3, exact=True, rows=rows)
+
+
+@pytest.mark.parametrize("shape", [(2560, 2304, 1024), (4096, 4096, 1024)])
+def test_bf16_stream_k_deterministic_bits(stream_k, shape):
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 25, inputs.NORMAL, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    first = g7.gemm_bf16_f32acc(a_d, b_d).clone()
+    for _ in range(5):
+        again = g7.gemm_bf16_f32acc(a_d, b_d)
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+    c_ref, s_ref = oracle_ref("bf16", a, b, rows=_sample_rows(M, 16, 25))
+    assert_within("bf16", first.cpu().numpy()[_sample_rows(M, 16, 25)], c_ref, s_ref)
+
+
+@pytest.mark.parametrize("shape", [(3100, 3100, 700), (2048, 4096, 1024), (700, 1300, 6200)])
+def test_bf16_every_schedule_same_bits_on_integers(shape):
+    # column split, stream-K and the automatic choice: exact sums everywhere
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 28, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    outs = []
+    prev = g7.abi.gemm_set_bf16_schedule(g7.abi.SCHEDULE_AUTO)
+    try:
+        for sched in (g7.abi.SCHEDULE_AUTO, g7.abi.SCHEDULE_STREAM_K,
+                      g7.abi.SCHEDULE_COLUMN_SPLIT):
+            g7.abi.gemm_set_bf16_schedule(sched)
+            outs.append(g7.gemm_bf16_f32acc(a_d, b_d).clone())
+            assert g7.gemm_get_device_status() == 0
+    finally:
+        g7.abi.gemm_set_bf16_schedule(prev)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    rows = _sample_rows(M, 24, 28)
+    c_ref, _ = oracle_ref("bf16", a, b, rows=rows, with_abs=False)
+    assert_within("bf16", outs[0].cpu().numpy()[rows], c_ref, None, exact=True)
+
+
 @pytest.mark.parametrize("M", [127, 1000, 3001])
 @pytest.mark.parametrize("N", [127, 1000, 3001])
 @pytest.mark.parametrize("K", [127, 1000, 3001])

@@ -77,6 +77,27 @@ def test_noalloc_matches_pooled_entry_point_two_calls_in_a_row():
                           what="noalloc vs pooled entry point")
 
 
+def test_noalloc_stream_k_matches_pooled_bitwise():
+    # 14 of 90 tiles shared as k-slice runs by 28 SM pairs: the partial sums
+    # and the synchronisation words live in the fixed scratch array too
+    M, N, K = 2560, 2304, 1024
+    a, b = inputs.make_pair(M, N, K, 26, inputs.NORMAL, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)
+    try:
+        s, plan = g7.plan("bf16", M, N, K)
+        assert s == 0 and plan.sk_tiles > 0
+        ref = g7.gemm_bf16_f32acc(a_d, b_d)
+        for _ in range(2):
+            out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+            assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
+            torch.cuda.synchronize()
+            assert g7.gemm_get_device_status() == 0
+            assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+    finally:
+        _abi.gemm_set_bf16_schedule(prev)
+
+
 def test_noalloc_rejects_requests_beyond_its_scratch():
     # A needs a copy (lda odd); 4096 rows of 8200 BF16 exceed the 64 MiB scratch
     M, K, N = 4096, 8199, 64
