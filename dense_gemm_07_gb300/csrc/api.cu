@@ -28,16 +28,25 @@ __device__ unsigned int g_status_word[4];
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = 0x7FFFFFFF;  // M, N, K < 2^31
 
-// Scratch kept between calls for one stream: calls on a stream run in order,
-// so they can share it without allocating each time (a stream-ordered
-// allocate/free pair costs about 2 us of GPU time per call).
+// Scratch kept between calls for one stream and one use: calls on a stream
+// run in order, so they can share it without allocating each time (a
+// stream-ordered allocate/free pair costs about 2 us of GPU time per call).
+enum ScratchUse {
+  kScratchStreamK = 0,  // BF16 stream-K partial sums + tagged sync words
+  kScratchSplitK = 1,   // FP32 split-K counters (kept zero) + partial sums
+  kScratchPack = 2,     // BF16 operands copied to aligned rows
+  kScratchUses = 3
+};
 struct StreamScratch {
   cudaStream_t stream = nullptr;
+  int use = 0;
   void* ptr = nullptr;
   int64_t bytes = 0;
   uint64_t last_use = 0;
 };
-constexpr int kScratchStreams = 8;
+constexpr int kScratchEntries = 8 * kScratchUses;
+// Scratch blocks of one use above this size are allocated per call instead.
+constexpr int64_t kScratchKeepMax = int64_t(1) << 30;
 
 struct DeviceState {
   bool ready = false;
@@ -47,7 +56,7 @@ struct DeviceState {
   cudaMemPool_t pool = nullptr;
   cudaStream_t up = nullptr;    // host-variant uploads
   cudaStream_t down = nullptr;  // host-variant downloads
-  StreamScratch scratch[kScratchStreams];
+  StreamScratch scratch[kScratchEntries];
   uint64_t scratch_clock = 0;
   uint64_t launch_tags = 0;     // stream-K launches so far (tag source)
   uint64_t tag_salt = 0;
@@ -372,18 +381,20 @@ void pool_free(void* p, cudaStream_t stream) {
 
 std::mutex g_scratch_mutex;
 
-// At least `bytes` of scratch for work queued on `stream`, kept for later
-// calls on the same stream.  Growing frees the old block in stream order;
-// reusing another stream's entry (more than kScratchStreams streams) first
+// At least `bytes` of scratch of one use for work queued on `stream`, kept
+// for later calls on the same stream.  *fresh is set when the block is new
+// (its contents are undefined).  Growing frees the old block in stream
+// order; taking over another stream's entry (all entries in use) first
 // waits for the device, since that stream's work may still use the block.
-gemm_status_t stream_scratch(DeviceState* d, cudaStream_t stream, int64_t bytes,
-                             void** out) {
+gemm_status_t stream_scratch(DeviceState* d, cudaStream_t stream, int use,
+                             int64_t bytes, void** out, bool* fresh) {
   *out = nullptr;
+  *fresh = false;
   if (bytes <= 0) return GEMM_OK;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   StreamScratch* e = nullptr;
   for (StreamScratch& x : d->scratch)
-    if (x.ptr && x.stream == stream) e = &x;
+    if (x.ptr && x.stream == stream && x.use == use) e = &x;
   if (e == nullptr) {
     for (StreamScratch& x : d->scratch)
       if (!x.ptr) {
@@ -415,11 +426,26 @@ gemm_status_t stream_scratch(DeviceState* d, cudaStream_t stream, int64_t bytes,
       return GEMM_ERR_NO_MEMORY;
     }
     e->bytes = want;
+    *fresh = true;
   }
   e->stream = stream;
+  e->use = use;
   e->last_use = ++d->scratch_clock;
   *out = e->ptr;
   return GEMM_OK;
+}
+
+// Scratch for one call: the stream's kept block when small enough, else a
+// block from the pool for this call only (*owned: free it after the call).
+gemm_status_t call_scratch(DeviceState* d, cudaStream_t stream, int use,
+                           int64_t bytes, void** out, bool* fresh, bool* owned) {
+  *owned = false;
+  if (bytes > kScratchKeepMax) {
+    *owned = true;
+    *fresh = true;
+    return pool_alloc(d, out, bytes, stream);
+  }
+  return stream_scratch(d, stream, use, bytes, out, fresh);
 }
 
 // A fresh 56-bit nonzero tag for one stream-K launch.
@@ -461,21 +487,25 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   const int64_t slots = f32_slots();
   if (slots <= 0) return GEMM_ERR_LAUNCH;
   const F32Plan fp = f32_plan(m, n, k, slots);
+  // Split-K scratch: one counter per resident slot first (zero between
+  // launches: the last block of each split tile puts its counter back to
+  // zero, so they are cleared only when the block is new), then partials.
+  const int64_t counter_area = round_up(slots * 4, 256);
   void* ws = nullptr;
-  const int64_t ws_bytes = round_up(fp.workspace_bytes, 256) + fp.counter_bytes;
-  s = pool_alloc(d, &ws, ws_bytes, stream);
-  if (s != GEMM_OK) return s;
-  float* partials = static_cast<float*>(ws);
-  unsigned int* counters = nullptr;
+  bool fresh = false, owned = false;
   if (fp.split > 1) {
-    counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) +
-                                               round_up(fp.workspace_bytes, 256));
-    s = from_cuda(cudaMemsetAsync(counters, 0, fp.counter_bytes, stream));
+    s = call_scratch(d, stream, kScratchSplitK, counter_area + fp.workspace_bytes, &ws,
+                     &fresh, &owned);
+    if (s != GEMM_OK) return s;
+    if (fresh) s = from_cuda(cudaMemsetAsync(ws, 0, counter_area, stream));
   }
+  unsigned int* counters = static_cast<unsigned int*>(ws);
+  float* partials =
+      ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counter_area) : nullptr;
   if (s == GEMM_OK)
     s = from_cuda(launch_gemm_f32(m, n, k, A, lda, B, ldb, C, ldc, vec_b, vec_c,
                                   fp, partials, counters, epi, stream));
-  pool_free(ws, stream);
+  if (owned) pool_free(ws, stream);
   return s;
 }
 
@@ -502,11 +532,14 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (max_pairs > 0) ps = pair_schedule(M, N, K, max_pairs, g_schedule.load());
   const int64_t pack_ws = pack_bytes(M, N, K, plan.pack_a, plan.pack_b);
   void* ws = nullptr;
-  s = pool_alloc(d, &ws, pack_ws, stream);
+  bool fresh = false, owned = false;
+  s = call_scratch(d, stream, kScratchPack, pack_ws, &ws, &fresh, &owned);
   if (s != GEMM_OK) return s;
-  // stream-K scratch: partial sums, then tagged synchronisation words
+  // stream-K scratch: partial sums, then tagged synchronisation words (any
+  // contents will do)
   void* sk = nullptr;
-  s = stream_scratch(d, stream, sk_bytes(ps), &sk);
+  bool sk_fresh = false;
+  s = stream_scratch(d, stream, kScratchStreamK, sk_bytes(ps), &sk, &sk_fresh);
   float* sk_ws = static_cast<float*>(sk);
   unsigned long long* sk_sync = nullptr;
   CUtensorMap tmW;
@@ -557,7 +590,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                                         d->status, epi, stream));
     }
   }
-  pool_free(ws, stream);
+  if (owned) pool_free(ws, stream);
   return s;
 }
 
