@@ -171,48 +171,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 
-// ------------------------------------------------------ L2 cache policies
-
-// Policy that keeps lines in L2 in preference to others (operands reused by
-// many CTAs) / lets them go first (output written once).
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// tma_load_2d_pair with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst,
-                                                      const CUtensorMap* map,
-                                                      uint32_t bar_cluster_addr,
-                                                      int32_t x, int32_t y,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
-      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x),
-      "r"(y), "l"(policy)
-      : "memory");
-}
-
-// tma_store_2d with an L2 cache policy.
-__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map,
-                                                  const void* src, int32_t x,
-                                                  int32_t y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint "
-      "[%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -305,28 +263,6 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   float v;
   asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
-}
-
-// 16 TMEM lanes x 256 bits, repeated 8 times along the columns (64 FP32
-// columns).  Thread t receives, for j = 0..7, columns 8j + 2(t % 4) and
-// 8j + 2(t % 4) + 1 of lane t / 4 in r[4j], r[4j + 1] and of lane t / 4 + 8
-// in r[4j + 2], r[4j + 3] (lanes relative to the address, whose lane field
-// is a multiple of 16 inside the warp's quarter).
-__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr,
-                                                   uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]),
-        "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
