@@ -594,18 +594,24 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   return s;
 }
 
-// Host-buffer variant: stage through pool memory, run, copy back, sync.
 // Host-buffer variant: stage through pool memory and overlap the copies with
-// the GEMM.  B is copied first (every output row needs all of it); A is then
-// copied in `chunks` row blocks on an internal upload stream, each block's
-// GEMM runs on the caller's stream as soon as its rows have arrived, and each
+// the GEMM.  A is split into `chunks` row blocks; each block's GEMM runs on
+// the caller's stream as soon as its rows (and B) have arrived, and each
 // block of C goes back on an internal download stream while the next block
-// computes.  Uploads and downloads use both directions of the link at once.
+// computes, so both directions of the link are busy at once.
+//
+// Every output row needs all of B, so the first block would wait for the
+// whole of B.  Instead, with `max_parts` > 1, several blocks and a long K, B
+// and the first block of A go up in pieces along K, and the first block's
+// product is accumulated piece by piece (C := A_k B_k, then
+// C := A_k B_k + C): its first GEMM starts once one piece of the operands
+// has arrived.  The first rows' sums are then added in that order.  This
+// pays when the GEMM, not the link, takes the time (FP32).
 template <typename T, typename Run>
 gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
                        int64_t lda, const T* B, int64_t ldb, float* C,
                        int64_t ldc, cudaStream_t stream, int max_chunks,
-                       int64_t min_chunk_rows, Run run) {
+                       int64_t min_chunk_rows, int max_parts, Run run) {
   gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (s != GEMM_OK || M == 0 || N == 0) return s;
   DeviceState* d = nullptr;
@@ -619,17 +625,27 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   if (chunks < 1 || K == 0) chunks = 1;
   constexpr int kMaxChunks = 8;
   if (chunks > kMaxChunks) chunks = kMaxChunks;
+  constexpr int kParts = 8;          // at most this many pieces of K
+  constexpr int64_t kMinPartK = 512;
+  int k_parts = max_parts < kParts ? max_parts : kParts;
+  if (k_parts < 1 || chunks < 2 || K < k_parts * kMinPartK) k_parts = 1;
 
   void *dA = nullptr, *dB = nullptr, *dC = nullptr;
-  cudaEvent_t ev[2 * kMaxChunks + 1] = {};
+  // events: start, one per piece of the first block, then a_ready / c_ready
+  // per block
+  constexpr int kMaxEvents = 1 + kParts + 2 * kMaxChunks;
+  cudaEvent_t ev[kMaxEvents] = {};
+  const int want_ev = 1 + k_parts + 2 * static_cast<int>(chunks);
   int n_ev = 0;
-  for (; n_ev < 2 * chunks + 1; ++n_ev)
+  for (; n_ev < want_ev; ++n_ev)
     if (cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       s = GEMM_ERR_LAUNCH;
       break;
     }
   cudaEvent_t start = ev[0];
+  cudaEvent_t* piece_ready = ev + 1;
+  cudaEvent_t* block_ev = ev + 1 + k_parts;
   if (s == GEMM_OK) s = pool_alloc(d, &dA, M * K * eb, stream);
   if (s == GEMM_OK) s = pool_alloc(d, &dB, K * N * eb, stream);
   if (s == GEMM_OK) s = pool_alloc(d, &dC, M * N * 4, stream);
@@ -637,31 +653,68 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   if (s == GEMM_OK) s = from_cuda(cudaEventRecord(start, stream));
   if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->up, start, 0));
   if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->down, start, 0));
-  if (s == GEMM_OK && K > 0)
-    s = from_cuda(cudaMemcpy2DAsync(dB, N * eb, B, ldb * eb, N * eb, K,
-                                    cudaMemcpyHostToDevice, stream));
-  for (int64_t i = 0; s == GEMM_OK && i < chunks; ++i) {
-    const int64_t r0 = M * i / chunks, r1 = M * (i + 1) / chunks, rows = r1 - r0;
-    cudaEvent_t a_ready = ev[1 + 2 * i], c_ready = ev[2 + 2 * i];
-    if (K > 0) {
-      s = from_cuda(cudaMemcpy2DAsync(static_cast<uint8_t*>(dA) + r0 * K * eb, K * eb,
-                                      A + r0 * lda, lda * eb, K * eb, rows,
-                                      cudaMemcpyHostToDevice, d->up));
-      if (s == GEMM_OK) s = from_cuda(cudaEventRecord(a_ready, d->up));
-      if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(stream, a_ready, 0));
-    }
+  uint8_t* dA8 = static_cast<uint8_t*>(dA);
+  uint8_t* dB8 = static_cast<uint8_t*>(dB);
+  // Uploads, in the order they are needed, on the upload stream: B (in
+  // k_parts pieces, each with its columns of the first block of A), then the
+  // other blocks of A.
+  // block i covers rows [row_at(i), row_at(i + 1)): equal shares, boundaries
+  // on whole 128-row tiles where the rows allow
+  auto row_at = [&](int64_t i) -> int64_t {
+    if (i >= chunks) return M;
+    const int64_t r = M * i / chunks;
+    const int64_t q = (r + 64) / 128 * 128;
+    return q > 0 && q < M ? q : r;
+  };
+  const int64_t rows0 = row_at(1);
+  // piece p covers k in [piece_k(p), piece_k(p + 1)), on 64-element bounds
+  auto piece_k = [&](int p) -> int64_t {
+    return p >= k_parts ? K : (K * p / k_parts) / 64 * 64;
+  };
+  for (int p = 0; s == GEMM_OK && K > 0 && p < k_parts; ++p) {
+    const int64_t k0 = piece_k(p), k1 = piece_k(p + 1);
+    s = from_cuda(cudaMemcpy2DAsync(dB8 + k0 * N * eb, N * eb, B + k0 * ldb, ldb * eb,
+                                    N * eb, k1 - k0, cudaMemcpyHostToDevice, d->up));
     if (s == GEMM_OK)
-      s = run(rows, N, K,
-              reinterpret_cast<const T*>(static_cast<uint8_t*>(dA) + r0 * K * eb),
-              K > 0 ? K : 1, static_cast<const T*>(dB), N,
-              static_cast<float*>(dC) + r0 * N, N, stream);
+      s = from_cuda(cudaMemcpy2DAsync(dA8 + k0 * eb, K * eb, A + k0, lda * eb,
+                                      (k1 - k0) * eb, rows0, cudaMemcpyHostToDevice,
+                                      d->up));
+    if (s == GEMM_OK) s = from_cuda(cudaEventRecord(piece_ready[p], d->up));
+  }
+  for (int64_t i = 1; s == GEMM_OK && K > 0 && i < chunks; ++i) {
+    const int64_t r0 = row_at(i), r1 = row_at(i + 1);
+    s = from_cuda(cudaMemcpy2DAsync(dA8 + r0 * K * eb, K * eb, A + r0 * lda, lda * eb,
+                                    K * eb, r1 - r0, cudaMemcpyHostToDevice, d->up));
+    if (s == GEMM_OK) s = from_cuda(cudaEventRecord(block_ev[2 * i], d->up));
+  }
+  // GEMMs on the caller's stream, downloads on the download stream.
+  EpiParams accumulate = epi_identity();
+  accumulate.beta = 1.0f;
+  for (int64_t i = 0; s == GEMM_OK && i < chunks; ++i) {
+    const int64_t r0 = row_at(i), r1 = row_at(i + 1), rows = r1 - r0;
+    const T* a_blk = reinterpret_cast<const T*>(dA8 + r0 * K * eb);
+    float* c_blk = static_cast<float*>(dC) + r0 * N;
+    if (i == 0) {
+      for (int p = 0; s == GEMM_OK && p < k_parts; ++p) {
+        const int64_t k0 = piece_k(p), k1 = piece_k(p + 1);
+        if (K > 0) s = from_cuda(cudaStreamWaitEvent(stream, piece_ready[p], 0));
+        if (s == GEMM_OK)
+          s = run(rows, N, k1 - k0, a_blk + k0, K > 0 ? K : 1,
+                  reinterpret_cast<const T*>(dB8 + k0 * N * eb), N, c_blk, N,
+                  p == 0 ? epi_identity() : accumulate, stream);
+      }
+    } else {
+      s = from_cuda(cudaStreamWaitEvent(stream, block_ev[2 * i], 0));
+      if (s == GEMM_OK)
+        s = run(rows, N, K, a_blk, K, reinterpret_cast<const T*>(dB8), N, c_blk, N,
+                epi_identity(), stream);
+    }
+    cudaEvent_t c_ready = block_ev[2 * i + 1];
     if (s == GEMM_OK) s = from_cuda(cudaEventRecord(c_ready, stream));
     if (s == GEMM_OK) s = from_cuda(cudaStreamWaitEvent(d->down, c_ready, 0));
     if (s == GEMM_OK)
-      s = from_cuda(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4,
-                                      static_cast<float*>(dC) + r0 * N, N * 4,
-                                      N * 4, rows, cudaMemcpyDeviceToHost,
-                                      d->down));
+      s = from_cuda(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, c_blk, N * 4, N * 4, rows,
+                                      cudaMemcpyDeviceToHost, d->down));
   }
   // Every copy is done before the buffers go back to the pool.
   if (s == GEMM_OK) s = from_cuda(cudaEventRecord(ev[0], d->down));
@@ -671,8 +724,9 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   pool_free(dC, stream);
   const cudaError_t e1 = cudaStreamSynchronize(stream);
   const cudaError_t e2 = cudaStreamSynchronize(d->down);
+  const cudaError_t e3 = cudaStreamSynchronize(d->up);
   for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
-  if (s == GEMM_OK) s = from_cuda(e1 != cudaSuccess ? e1 : e2);
+  if (s == GEMM_OK) s = from_cuda(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
   return s;
 }
 
@@ -904,9 +958,10 @@ gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
                             int64_t ldc, void* stream) {
   return run_host<float>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      /*max_chunks=*/2, /*min_chunk_rows=*/1024, [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la,
-         const float* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
-        return run_f32(m, n, k, a, la, b, lb, c, lc, st);
+      /*max_chunks=*/3, /*min_chunk_rows=*/1024, /*max_parts=*/4,
+      [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la, const float* b,
+         int64_t lb, float* c, int64_t lc, const EpiParams& e, cudaStream_t st) {
+        return run_f32(m, n, k, a, la, b, lb, c, lc, st, e);
       });
 }
 
@@ -916,10 +971,10 @@ gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
                                     int64_t ldc, void* stream) {
   return run_host<uint16_t>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      /*max_chunks=*/4, /*min_chunk_rows=*/512, [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
-         const uint16_t* b, int64_t lb, float* c, int64_t lc, cudaStream_t st) {
-        return run_bf16(m, n, k, a, la, b, lb, c, lc, st);
-      });
+      /*max_chunks=*/4, /*min_chunk_rows=*/512, /*max_parts=*/1,
+      [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
+         const uint16_t* b, int64_t lb, float* c, int64_t lc, const EpiParams& e,
+         cudaStream_t st) { return run_bf16(m, n, k, a, la, b, lb, c, lc, st, e); });
 }
 
 const char* gemm_status_string(gemm_status_t status) {

@@ -190,12 +190,17 @@ GEMM07_API gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t
  * (pinned memory gives the fastest copies; pageable memory works).  The
  * call stages A and B in device buffers from the library's memory pool,
  * runs the GEMM and copies C back, and returns once C is in host memory
- * (it synchronises `stream`).  B is copied first; A is then copied in row
- * blocks on a library-owned upload stream, each block's product is computed
- * on `stream` as soon as its rows arrive, and each block of C is copied
+ * (it synchronises `stream`).  A is split into row blocks (up to 3 for
+ * FP32, 4 for BF16, boundaries on whole 128-row tiles); uploads run on a
+ * library-owned upload stream, each block's product is computed on
+ * `stream` as soon as its operands arrive, and each block of C is copied
  * back on a library-owned download stream while the next block computes,
- * so uploads, downloads and compute overlap.  Work already queued on
- * `stream` completes before any of this starts.
+ * so uploads, downloads and compute overlap.  For FP32 with K >= 2048 and
+ * several blocks, B and the first block of A go up in 4 pieces along K and
+ * the first block's product is accumulated piece by piece, so its GEMM
+ * starts after a quarter of B has arrived; those rows' sums are then taken
+ * in that order (within the FP32 bound, not bit-identical to gemm_f32).
+ * Work already queued on `stream` completes before any of this starts.
  */
 GEMM07_API gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K,
                             const float *A, int64_t lda,

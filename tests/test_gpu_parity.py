@@ -339,6 +339,28 @@ def test_host_buffer_variant_in_row_blocks_exact(kind, shape):
     assert_within(kind, buf[:, :N].numpy(), c_ref, None, exact=True)
 
 
+@pytest.mark.parametrize("kind,shape", [("f32", (2048, 300, 2100)), ("f32", (2100, 256, 4099)),
+                                        ("bf16", (2048, 256, 4099))])
+def test_host_buffer_variant_k_pieces(kind, shape):
+    # several row blocks and a long K: B and the first block of A go up in
+    # pieces along K and the first block accumulates piece by piece
+    # (K = 4099: ragged last piece and odd row strides)
+    M, N, K = shape
+    host_fn = g7.gemm_f32_host if kind == "f32" else g7.gemm_bf16_f32acc_host
+    a, b = inputs.make_pair(M, N, K, 29, inputs.INT3, dtype=_dtype(kind))
+    c = host_fn(a.pin_memory(), b.pin_memory())
+    c_ref, _ = oracle_ref(kind, a, b, with_abs=False)
+    assert_within(kind, c.numpy(), c_ref, None, exact=True)
+    # general values: the piecewise sums stay within the FP32 bound
+    a, b = inputs.make_pair(M, N, K, 30, inputs.NORMAL if kind == "bf16" else inputs.UNIFORM,
+                            dtype=_dtype(kind))
+    c = host_fn(a.pin_memory(), b.pin_memory())
+    rows = _sample_rows(M, 32, 30)
+    c_ref, s_ref = oracle_ref(kind, a, b, rows=rows)
+    assert_within(kind, c.numpy()[rows], c_ref, s_ref)
+    assert g7.gemm_get_device_status() == 0
+
+
 def test_streams_are_respected():
     a, b = inputs.make_pair(1024, 1024, 1024, 15, inputs.INT3, dtype=torch.bfloat16)
     s = torch.cuda.Stream()
