@@ -33,3 +33,31 @@ def test_bounded_wait_runs_out_and_gpu_stays_usable():
     assert g7.gemm_get_device_status() == _abi.GEMM_OK
     c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
     assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
+
+
+def test_stream_k_timeout_then_next_launch_exact():
+    # Stream-K schedule: the timed-out launch leaves its tickets and flags
+    # half-counted; the next launch carries a new tag, so they read as zero
+    # and its fix-up is exact.
+    M, N, K = 2560, 2304, 512        # one wave + 14 tiles shared by 28 pairs
+    a, b = inputs.make_pair(M, N, K, 32, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.cuda(), b.cuda()
+    prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)
+    try:
+        s, plan = g7.plan("bf16", M, N, K)
+        assert plan.sk_tiles > 0
+        assert g7.gemm_get_device_status() == _abi.GEMM_OK
+        assert _abi.gemm_debug_inject(1, 20_000_000) == _abi.GEMM_OK
+        try:
+            g7.gemm_bf16_f32acc(a_d, b_d)
+            assert g7.gemm_get_device_status() == _abi.GEMM_ERR_TIMEOUT
+        finally:
+            assert _abi.gemm_debug_inject(0, 0) == _abi.GEMM_OK
+        c = g7.gemm_bf16_f32acc(a_d, b_d)
+        torch.cuda.synchronize()
+        assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    finally:
+        _abi.gemm_set_bf16_schedule(prev)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1]]))
+    c_ref, _ = oracle_ref("bf16", a, b, rows=rows, with_abs=False)
+    assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
