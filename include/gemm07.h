@@ -10,7 +10,8 @@
  *   - "GEMM Optimization" (infra.bea.ai), section 1 "The Problem".
  *   - "How a Matrix Multiply Runs on a GPU", "Level 0": the row-major
  *     indexing A[row*K + k], B[k*N + col], C[row*N + col].
- * C is overwritten (no alpha/beta).  K == 0 writes zeros into C (the empty
+ * C is overwritten (the _ex variants below add alpha, beta, a bias and an
+ * activation).  K == 0 writes zeros into C (the empty
  * sum); M == 0 or N == 0 is a no-op.  Out-of-range rows and columns of a
  * ragged edge tile contribute zero and are never written ("A06 -- Tiled
  * Matrix Multiply (GEMM)", section 3, the guarded tiled kernel and ": 0.0f").
@@ -31,7 +32,11 @@
  *   - Results are deterministic: the same inputs, sizes and device give the
  *     same bits on every call (no atomics in any reduction).
  *   - Calls are thread-safe.  The library may hold per-device state (a
- *     status word, a workspace pool) until gemm_shutdown() or process exit.
+ *     status word, a workspace pool, scratch blocks kept per stream) until
+ *     gemm_shutdown() or process exit.  Scratch is reused by later calls on
+ *     the same stream handle, which the stream orders after the earlier
+ *     ones; work still queued on a destroyed stream must have finished
+ *     before a new stream that may reuse its handle calls the library.
  *
  * Errors: every entry point returns a gemm_status_t.  Argument errors are
  * detected on the host before anything is enqueued and leave C untouched.
