@@ -1,7 +1,7 @@
 // stream_k.cuh -- how the paired-SM BF16 kernel shares its work among the
 // resident pairs: whole tiles in full waves, and a partial last wave either
-// split along N (each tile as two 256 x 128 units, so the wave takes about
-// half as long) or, in stream-K schedules, split along K.
+// split along N (each tile as two 256 x 128 units on twice as many pairs)
+// or, in stream-K schedules, split along K.
 //
 // Stream-K part ("GEMM Optimization", section "L2 Cache and Wave Analysis":
 // a partial last wave leaves SMs idle; spreading the k-iterations of the
