@@ -234,6 +234,16 @@ def ladder_context(g7, roofline, A32, B32, C32, flush, stream, sms, sm_mhz, hbm_
     return out
 
 
+def arm_config(world):
+    """The workload description both arms report."""
+    return {"workload": "gemm 4096^3 bf16->f32acc (N(0,1), seed 2) + "
+                        "gemm 4096^3 f32 (U[-1,1), seed 1)",
+            "M": SIZE, "N": SIZE, "K": SIZE,
+            "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
+            "l2": "flushed before each GEMM by a 256 MiB write outside "
+                  "the kernel events"}
+
+
 # ------------------------------------------------------------- reference
 
 def run_reference(args):
@@ -271,8 +281,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gemm 4096^3 bf16->f32acc + gemm 4096^3 f32, "
-                   "oracle sample", "rows_per_gemm_per_step": rows},
+        "config": arm_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -431,12 +440,7 @@ def main():
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16+f32", "data": "synthetic",
-            "config": {"workload": "gemm 4096^3 bf16->f32acc (N(0,1), seed 2) + "
-                                   "gemm 4096^3 f32 (U[-1,1), seed 1)",
-                       "M": SIZE, "N": SIZE, "K": SIZE,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
-                       "l2": "flushed before each GEMM by a 256 MiB write outside "
-                             "the kernel events"},
+            "config": arm_config(world),
             "paths": {
                 "bf16_f32acc": {"ms": ms_bf16, "tflops": tf_bf16, "roofline": rl_bf16},
                 "f32": {"ms": ms_f32, "tflops": tf_f32, "roofline": rl_f32},
