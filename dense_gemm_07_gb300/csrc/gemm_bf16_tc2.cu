@@ -13,16 +13,16 @@
 // of B per CTA) on twice as many pairs.  On sm_103a an N = 128 pair MMA
 // takes about as long per k-slice as an N = 256 one, so this mainly halves
 // the last epilogue (measured: 4 us of 93 at 4096^3).  In a stream-K
-// schedule the last wave's tiles (and, with two or more whole waves, those
-// of the last whole wave) are instead cut into equal runs of k-slices, one
-// per pair, which every pair computes before its whole tiles.  A tile cut
-// into segments is finished by the epilogue warp that arrives last
-// on the tile's ticket: the others store their partial sums to a workspace
-// and raise a ready flag; the last one adds all segments in k order (its own
-// from tensor memory) and applies the output step.  No warp waits for work
-// that has not started: a flag is only awaited after its writer has taken
-// its ticket.  Partial sums move through the same staging boxes and copy
-// engine as C, so the fix-up traffic is bulk traffic.
+// schedule the tiles of the last whole wave and of the partial one are
+// instead cut into equal runs of k-slices, one per pair, which every pair
+// computes after its whole tiles.  A tile cut into segments is finished by
+// the epilogue warp that arrives last on the tile's ticket: the others store
+// their partial sums to a workspace and raise a ready flag; the last one
+// adds all segments in k order (its own from tensor memory) and applies the
+// output step.  No warp waits for work that has not started: a flag is only
+// awaited after its writer has taken its ticket.  Partial sums move by the
+// copy engine; when the finishing unit is the pair's last, its operand ring
+// is idle and each warp loads its 32 x 256 partial sums there in one batch.
 //
 // sm_103a realisation: clusters of two CTAs, one per SM.  CTA r of the pair
 // owns rows [128r, 128r+128) of the 256-row tile and stages only those rows
@@ -263,6 +263,10 @@ struct SkCombine {
   uint32_t* bar_uses;   // its completed phases
   volatile int* abort;
   uint64_t tmo;
+  // Two segments, loaded in advance: the other segment's 8 boxes (one per
+  // 32-column chunk, 4 KB each, as the copy engine lays them out), or null
+  // to load each box when its chunk is combined.
+  const uint8_t* stash;
 };
 
 // Row `lane` of a swizzled 32 x 32 FP32 staging box (the layout both the
@@ -293,6 +297,8 @@ __device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
     if (s == cb.mine) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    } else if (cb.stash) {
+      box_read_row(cb.stash + c * EPI_BOX_BYTES, lane, v);
     } else {
       const int q = cb.q_first + s;
       const uint32_t parity = *cb.bar_uses & 1u;
@@ -598,6 +604,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int t = 0; wi.next(sched, num_pairs, w); ++t) {
       const int acc = t % NUM_ACC;
       const uint32_t acc_phase = static_cast<uint32_t>(t / NUM_ACC) & 1u;
+      WorkIter peek = wi;
+      WorkUnit after;
+      const bool last_unit = !peek.next(sched, num_pairs, after);
       int ok = 0;
       if (lane == 0) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort, tmo) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -646,6 +655,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           cb.bar_uses = &part_uses;
           cb.abort = abort;
           cb.tmo = tmo;
+          cb.stash = nullptr;
           // Every other segment's writer has taken its ticket, so it is
           // running; wait (bounded) until its partial sums are stored.
           int got = 1;
@@ -662,6 +672,26 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           got = __shfl_sync(0xffffffffu, got, 0);
           good = got != 0;
+          if (good && last_unit && st.nseg == 2) {
+            // This CTA's operand ring is idle: every MMA of the pair has
+            // completed (this unit's accumulator is full) and no copy is
+            // left to issue.  Load the other segment's 8 boxes at once into
+            // this warp's 32 KB of it.
+            uint8_t* stash = smem + q * (BN / 32) * EPI_BOX_BYTES;
+            const int oq = st.q_first + (1 - cb.mine);
+            const int orow = sk_row(oq, sk_slot(sched, oq, w.tile), rank, q);
+            const uint32_t parity = part_uses & 1u;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&ctl->part[q], (BN / 32) * EPI_BOX_BYTES);
+              for (int c = 0; c < BN / 32; ++c)
+                tma_load_2d(stash + c * EPI_BOX_BYTES, &tmW, &ctl->part[q], c * 32, orow);
+            }
+            ++part_uses;
+            int ld = 0;
+            if (lane == 0) ld = mbar_wait(&ctl->part[q], parity, abort, tmo) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, ld, 0) != 0;
+            cb.stash = stash;
+          }
           cbp = &cb;
         }
       }

@@ -17,10 +17,11 @@
 // taking units p, p + pairs, p + 2 * pairs, ...: tiles [0, num_full) whole,
 // each later one as `split` units of 256 / split columns.
 //
-// Each pair does its stream-K range first and its whole tiles after it, so
-// that combining split tiles (which waits on other pairs' partial sums and
-// reads them back) overlaps the main loops of whole tiles instead of ending
-// the kernel.
+// Each pair does its data-parallel units first and its stream-K range last.
+// A split tile's first segment is then the end of one pair's range and its
+// second the start of the next pair's: the second is computed early and
+// leaves its partial sums, the first is computed last and adds them, as the
+// pair's final unit, when its operand ring is idle and can hold them.
 //
 // Everything here is plain integer arithmetic shared by the kernel and by
 // the host (planning, and a host-side listing used by the tests).
@@ -52,7 +53,8 @@ enum PairScheduleMode {
 constexpr int kSkSliceK = 64;
 
 // Most segments one stream-K tile can be split into (the planner keeps every
-// range at least half a tile long, which bounds it by 3).
+// range at least half a tile long, which bounds it by 3; whole-wave
+// schedules and aligned halves give 2).
 constexpr int kSkMaxSeg = 3;
 // Shortest k extent (in slices) worth splitting at all, and the shortest
 // one worth splitting when no whole wave follows to hide the combining.
@@ -82,7 +84,7 @@ struct WorkUnit {
   int n_off, width;
 };
 
-// Walks one pair's units: its stream-K range, then its data-parallel units.
+// Walks one pair's units: its data-parallel units, then its stream-K range.
 struct WorkIter {
   int next_dp;
   int64_t it, end;
@@ -99,19 +101,6 @@ struct WorkIter {
   }
 
   __host__ __device__ bool next(const PairSchedule& s, int num_pairs, WorkUnit& u) {
-    if (it < end) {
-      const int64_t t = it / s.num_kb;
-      const int k0 = static_cast<int>(it - t * s.num_kb);
-      const int64_t left = end - it;
-      const int k1 = left < s.num_kb - k0 ? k0 + static_cast<int>(left) : s.num_kb;
-      u.tile = s.dp_tiles + static_cast<int>(t);
-      u.k0 = k0;
-      u.k1 = k1;
-      u.n_off = 0;
-      u.width = 256;
-      it += k1 - k0;
-      return true;
-    }
     const int units = s.num_full + (s.dp_tiles - s.num_full) * s.split;
     if (next_dp < units) {
       const int v = next_dp;
@@ -127,6 +116,19 @@ struct WorkIter {
         u.width = 256 / s.split;
         u.n_off = ((v - s.num_full) % s.split) * u.width;
       }
+      return true;
+    }
+    if (it < end) {
+      const int64_t t = it / s.num_kb;
+      const int k0 = static_cast<int>(it - t * s.num_kb);
+      const int64_t left = end - it;
+      const int k1 = left < s.num_kb - k0 ? k0 + static_cast<int>(left) : s.num_kb;
+      u.tile = s.dp_tiles + static_cast<int>(t);
+      u.k0 = k0;
+      u.k1 = k1;
+      u.n_off = 0;
+      u.width = 256;
+      it += k1 - k0;
       return true;
     }
     return false;
@@ -165,11 +167,9 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 //     tiles run as 2T units of 256 x 128;
 //   stream-K (kScheduleStreamK; kScheduleAuto only for W == 0 with at least
 //   kSkMinSlicesExposed k-slices):
-//   - W >= 2: the last whole wave and the partial one (P + T tiles) are
-//     shared by all P pairs (at least a tile's worth each, so a tile has at
-//     most two segments), then W - 1 whole waves follow;
-//   - W == 1: the T tiles are shared by min(P, 2T) pairs (at least half a
-//     tile each: at most three segments), then one whole wave follows;
+//   - W >= 1: the last whole wave and the partial one (P + T tiles) are
+//     shared by all P pairs after W - 1 whole waves (at least a tile's worth
+//     each, so a tile has at most two segments);
 //   - W == 0: each tile is halved over 2T pairs (if 2T <= P).
 // A last wave more than 85 % full, or fewer than kSkMinSlices k-slices, is
 // never split along K.
@@ -203,12 +203,9 @@ inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
       (waves > 0 || s.num_kb < kSkMinSlicesExposed))
     return column_split();
   int64_t sk_tiles = 0, sk_pairs = 0;
-  if (waves >= 2) {
+  if (waves >= 1) {
     sk_tiles = P + tail;
     sk_pairs = P;
-  } else if (waves == 1) {
-    sk_tiles = tail;
-    sk_pairs = 2 * tail < P ? 2 * tail : P;
   } else {
     if (2 * tiles > P) return column_split();
     sk_tiles = tiles;

@@ -39,7 +39,7 @@ def test_stream_k_timeout_then_next_launch_exact():
     # Stream-K schedule: the timed-out launch leaves its tickets and flags
     # half-counted; the next launch carries a new tag, so they read as zero
     # and its fix-up is exact.
-    M, N, K = 2560, 2304, 512        # one wave + 14 tiles shared by 28 pairs
+    M, N, K = 2560, 2304, 512        # 90 tiles shared as k-slice runs by 76 pairs
     a, b = inputs.make_pair(M, N, K, 32, inputs.INT3, dtype=torch.bfloat16)
     a_d, b_d = a.cuda(), b.cuda()
     prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)

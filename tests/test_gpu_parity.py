@@ -153,7 +153,7 @@ def stream_k():
 
 @pytest.mark.parametrize("shape", [(512, 1024, 8192),    # 8 tiles halved over 16 pairs
                                    (512, 512, 8192),     # 4 tiles, long K
-                                   (2560, 2304, 1024),   # 90 tiles: 1 wave + 14 split
+                                   (2560, 2304, 1024),   # 90 tiles: 1 wave + 14, all shared
                                    (2560, 2302, 640),    # N % 4: direct stores
                                    (3100, 3100, 700),    # 169 tiles, ragged edges
                                    (2900, 3300, 1000)])  # 156 tiles, ragged K

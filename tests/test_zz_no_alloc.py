@@ -78,7 +78,7 @@ def test_noalloc_matches_pooled_entry_point_two_calls_in_a_row():
 
 
 def test_noalloc_stream_k_matches_pooled_bitwise():
-    # 14 of 90 tiles shared as k-slice runs by 28 SM pairs: the partial sums
+    # 90 tiles shared as k-slice runs by 76 SM pairs: the partial sums
     # and the synchronisation words live in the fixed scratch array too
     M, N, K = 2560, 2304, 1024
     a, b = inputs.make_pair(M, N, K, 26, inputs.NORMAL, dtype=torch.bfloat16)
