@@ -207,7 +207,9 @@ __device__ __forceinline__ int sk_row(int q, int slot, uint32_t rank, int wq) {
 // to be cleared between launches: ticket counters [sk_tiles][rank 2][warp 4]
 // hold (tag << 8) | arrivals, ready flags [sk_pairs][slot 2][rank 2][warp 4]
 // hold the tag once the slot's partial sums are stored.  A word with another
-// tag counts as zero.
+// tag counts as zero.  The finishing warp of a tile also puts its ticket and
+// the flags it consumed back to zero, so a launch replayed with the same tag
+// (a CUDA graph) starts from clean words.
 __device__ __forceinline__ unsigned long long* sk_ticket(
     unsigned long long* sync, const PairSchedule& s, int tile, uint32_t rank,
     int wq) {
@@ -669,6 +671,17 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             // the flags were read by this thread; the boxes will be read by
             // the copy engine
             fence_proxy_async_global();
+            if (got) {
+              // Every segment has taken its ticket and raised its flag: put
+              // the words back to zero, so that a replay of this launch
+              // (same tag, e.g. from a CUDA graph) finds them clean.
+              *sk_ticket(sk_sync, sched, w.tile, rank, q) = 0ull;
+              for (int sg = 0; sg < st.nseg; ++sg)
+                if (sg != cb.mine) {
+                  const int qq = st.q_first + sg;
+                  *sk_ready(sk_sync, sched, qq, sk_slot(sched, qq, w.tile), rank, q) = 0ull;
+                }
+            }
           }
           got = __shfl_sync(0xffffffffu, got, 0);
           good = got != 0;

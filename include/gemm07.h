@@ -37,6 +37,9 @@
  *     the same stream handle, which the stream orders after the earlier
  *     ones; work still queued on a destroyed stream must have finished
  *     before a new stream that may reuse its handle calls the library.
+ *     The device-buffer entry points can be captured in a CUDA graph; a
+ *     replay must not run concurrently with other library work on the
+ *     stream it was captured from (it uses that stream's scratch).
  *
  * Errors: every entry point returns a gemm_status_t.  Argument errors are
  * detected on the host before anything is enqueued and leave C untouched.

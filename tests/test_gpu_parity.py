@@ -384,3 +384,34 @@ def test_invalid_arguments_rejected_before_launch():
                            c.data_ptr(), 4, st) == g7.abi.GEMM_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(c == 0)
+
+
+def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
+    # A captured stream-K launch replays with the same launch tag; the
+    # finishing warps leave the synchronisation words clean, so every replay
+    # is exact.
+    M, N, K = 2560, 2304, 1024
+    a, b = inputs.make_pair(M, N, K, 33, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    c = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    g7.gemm_bf16_f32acc(a_d, b_d, out=c)      # warm-up: scratch and tensor maps
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g7.gemm_bf16_f32acc(a_d, b_d, out=c)
+    torch.cuda.current_stream().wait_stream(s)
+    rows = _sample_rows(M, 24, 33)
+    for r in range(3):
+        # new operand values each replay: stale partial sums or tickets from
+        # the previous replay would show
+        a_r, _ = inputs.make_pair(M, N, K, 34 + r, inputs.INT3, dtype=torch.bfloat16)
+        a_d.copy_(a_r.to(DEV))
+        c.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g7.gemm_get_device_status() == 0
+        c_ref, _ = oracle_ref("bf16", a_r, b, rows=rows, with_abs=False)
+        assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
