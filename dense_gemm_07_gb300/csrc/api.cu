@@ -437,10 +437,31 @@ gemm_status_t stream_scratch(DeviceState* d, cudaStream_t stream, int use,
 
 // Scratch for one call: the stream's kept block when small enough, else a
 // block from the pool for this call only (*owned: free it after the call).
+// While the stream is being captured into a CUDA graph and its kept block is
+// missing or too small, the block is allocated for the call too (inside the
+// graph, which owns it), never kept: memory allocated during a capture
+// belongs to the graph.
 gemm_status_t call_scratch(DeviceState* d, cudaStream_t stream, int use,
                            int64_t bytes, void** out, bool* fresh, bool* owned) {
   *owned = false;
-  if (bytes > kScratchKeepMax) {
+  *out = nullptr;
+  *fresh = false;
+  if (bytes <= 0) return GEMM_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  if (cap != cudaStreamCaptureStatusNone) {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    for (StreamScratch& x : d->scratch)
+      if (x.ptr && x.stream == stream && x.use == use && x.bytes >= bytes) {
+        x.last_use = ++d->scratch_clock;
+        *out = x.ptr;
+        return GEMM_OK;
+      }
+  }
+  if (bytes > kScratchKeepMax || cap != cudaStreamCaptureStatusNone) {
     *owned = true;
     *fresh = true;
     return pool_alloc(d, out, bytes, stream);
@@ -538,8 +559,10 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   // stream-K scratch: partial sums, then tagged synchronisation words (any
   // contents will do)
   void* sk = nullptr;
-  bool sk_fresh = false;
-  s = stream_scratch(d, stream, kScratchStreamK, sk_bytes(ps), &sk, &sk_fresh);
+  bool sk_fresh = false, sk_owned = false;
+  if (s == GEMM_OK)
+    s = call_scratch(d, stream, kScratchStreamK, sk_bytes(ps), &sk, &sk_fresh,
+                     &sk_owned);
   float* sk_ws = static_cast<float*>(sk);
   unsigned long long* sk_sync = nullptr;
   CUtensorMap tmW;
@@ -591,6 +614,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     }
   }
   if (owned) pool_free(ws, stream);
+  if (sk_owned) pool_free(sk, stream);
   return s;
 }
 

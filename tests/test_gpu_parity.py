@@ -415,3 +415,41 @@ def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
         assert g7.gemm_get_device_status() == 0
         c_ref, _ = oracle_ref("bf16", a_r, b, rows=rows, with_abs=False)
         assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
+
+
+@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed"])
+def test_capture_on_fresh_stream_then_replay(case):
+    # Captured on a stream the library has never seen: its scratch is then
+    # allocated inside the graph (owned by it) rather than kept, and every
+    # replay on new operand values is exact.
+    kind = "f32" if case.startswith("f32") else "bf16"
+    M, N, K = {"f32_split_k": (2560, 2048, 640), "bf16_stream_k": (2560, 2304, 1024),
+               "bf16_packed": (700, 500, 333)}[case]
+    dtype = _dtype(kind)
+    fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
+    a, b = inputs.make_pair(M, N, K, 35, inputs.INT3, dtype=dtype)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    c = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    prev = g7.abi.gemm_set_bf16_schedule(
+        g7.abi.SCHEDULE_STREAM_K if case == "bf16_stream_k" else g7.abi.SCHEDULE_AUTO)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                fn(a_d, b_d, out=c)
+        torch.cuda.current_stream().wait_stream(s)
+        rows = _sample_rows(M, 16, 35)
+        for r in range(2):
+            a_r, _ = inputs.make_pair(M, N, K, 36 + r, inputs.INT3, dtype=dtype)
+            a_d.copy_(a_r.to(DEV))
+            c.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert g7.gemm_get_device_status() == 0
+            c_ref, _ = oracle_ref(kind, a_r, b, rows=rows, with_abs=False)
+            assert_within(kind, c.cpu().numpy()[rows], c_ref, None, exact=True)
+        del graph
+    finally:
+        g7.abi.gemm_set_bf16_schedule(prev)
