@@ -1,6 +1,7 @@
 """Time every workload configuration of the method on one GPU and print a
 markdown table (CUDA events on the calling stream, 3 warm-up calls, then
-`--reps` timed calls with a 256 MiB L2 flush before each; median and best).
+`--reps` timed calls with a 256 MiB L2 flush before each, queued behind a
+short spin so that host call overhead is not timed; median and best).
 
     python -m dense_gemm_07_gb300.config_table [--reps 20] [--peaks MEASURED_PEAKS.json]
 
@@ -54,6 +55,10 @@ def time_call(fn, reps, flush):
         fn()
     ts = []
     for _ in range(reps):
+        # a ~0.2 ms torch spin kernel holds the stream while the host queues
+        # the flush and the call, so the host's call overhead stays outside
+        # the events
+        torch.cuda._sleep(400_000)
         flush.fill_(1.0)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)

@@ -108,6 +108,33 @@ int64_t pack_bytes(int64_t M, int64_t N, int64_t K, bool pack_a, bool pack_b) {
   return ws;
 }
 
+// Copy the operands the tensor-memory accelerator cannot read in place into
+// `cursor` (packed A first, then packed B, each on a 256-byte boundary, row
+// strides rounded up to 8 elements), both in one launch; the operand
+// pointers and strides are replaced by the copies'.
+cudaError_t pack_operands(const gemm_plan_t& plan, const uint16_t* A, int64_t lda,
+                          const uint16_t* B, int64_t ldb, int64_t M, int64_t N,
+                          int64_t K, uint8_t* cursor, const uint16_t** a_op,
+                          int64_t* lda_op, const uint16_t** b_op, int64_t* ldb_op,
+                          cudaStream_t stream) {
+  PackJob jobs[2];
+  int n = 0;
+  if (plan.pack_a) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    *lda_op = round_up(K, 8);
+    cursor += round_up(M * *lda_op * 2, 256);
+    jobs[n++] = PackJob{A, lda, dst, *lda_op, static_cast<int>(M), static_cast<int>(K)};
+    *a_op = dst;
+  }
+  if (plan.pack_b) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
+    *ldb_op = round_up(N, 8);
+    jobs[n++] = PackJob{B, ldb, dst, *ldb_op, static_cast<int>(K), static_cast<int>(N)};
+    *b_op = dst;
+  }
+  return launch_pack_u16(jobs, n, stream);
+}
+
 // Scratch of a stream-K schedule: partial sums, then synchronisation words.
 int64_t sk_bytes(const PairSchedule& ps) {
   if (ps.sk_tiles == 0) return 0;
@@ -575,19 +602,9 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   const uint16_t* b_op = B;
   int64_t lda_op = lda, ldb_op = ldb;
   uint8_t* cursor = static_cast<uint8_t*>(ws);
-  if (s == GEMM_OK && plan.pack_a) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
-    lda_op = round_up(K, 8);
-    cursor += round_up(M * lda_op * 2, 256);
-    s = from_cuda(launch_copy_rows_u16(A, lda, dst, lda_op, m, k, stream));
-    a_op = dst;
-  }
-  if (s == GEMM_OK && plan.pack_b) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
-    ldb_op = round_up(N, 8);
-    s = from_cuda(launch_copy_rows_u16(B, ldb, dst, ldb_op, k, n, stream));
-    b_op = dst;
-  }
+  if (s == GEMM_OK)
+    s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
+                                &b_op, &ldb_op, stream));
   CUtensorMap tmA, tmB;
   if (s == GEMM_OK)
     s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
@@ -604,7 +621,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
       const unsigned long long tag = ps.sk_tiles > 0 ? next_launch_tag(d) : 0;
       s = from_cuda(launch_gemm_bf16_pair(
           tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
-          ldc, m, n, ps, sk_sync, tag, vec_c, d->status, epi, stream));
+          ldc, m, n, ps, sk_sync, tag, d->status, epi, stream));
     } else {
       const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
                             ((N + kTcTileN - 1) / kTcTileN);
@@ -848,19 +865,8 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   const uint16_t* b_op = B;
   int64_t lda_op = lda, ldb_op = ldb;
   uint8_t* cursor = d->scratch;
-  if (plan.pack_a) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
-    lda_op = round_up(K, 8);
-    cursor += round_up(M * lda_op * 2, 256);
-    s = from_cuda(launch_copy_rows_u16(A, lda, dst, lda_op, m, k, stream));
-    a_op = dst;
-  }
-  if (s == GEMM_OK && plan.pack_b) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(cursor);
-    ldb_op = round_up(N, 8);
-    s = from_cuda(launch_copy_rows_u16(B, ldb, dst, ldb_op, k, n, stream));
-    b_op = dst;
-  }
+  s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
+                              &b_op, &ldb_op, stream));
   CUtensorMap tmA, tmB;
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
   const int max_pairs =
@@ -895,7 +901,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
     const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
     return from_cuda(launch_gemm_bf16_pair(
         tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
-        ldc, m, n, ps, sk_sync, tag, vec_c, d->status, epi_identity(), stream));
+        ldc, m, n, ps, sk_sync, tag, d->status, epi_identity(), stream));
   }
   const int64_t tiles =
       ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);

@@ -334,46 +334,6 @@ __device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
 
 // ------------------------------------------------------------ output step
 
-// Epilogue of one unit of width W: this thread's row, W columns from TMEM
-// to C.
-template <int W>
-__device__ __forceinline__ void store_unit(uint32_t taddr, float* C,
-                                           int64_t ldc, int row, int n0, int M,
-                                           int N, int vec_c,
-                                           const EpiParams& epi) {
-  float* crow = C + static_cast<int64_t>(row) * ldc;
-#pragma unroll 1
-  for (int c = 0; c < W / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + c * 32, r);
-    tmem_ld_wait();
-    const int gn = n0 + c * 32;
-    if (row < M) {
-      if (vec_c && gn + 31 < N) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 old = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (epi.beta != 0.0f) old = *reinterpret_cast<const float4*>(crow + gn + j);
-          const float o[4] = {old.x, old.y, old.z, old.w};
-          float v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            v[e] = epi_apply(epi, __uint_as_float(r[j + e]), o[e],
-                             epi.bias ? epi.bias[gn + j + e] : 0.0f);
-          *reinterpret_cast<float4*>(crow + gn + j) = make_float4(v[0], v[1], v[2], v[3]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (gn + j < N)
-            crow[gn + j] = epi_apply(epi, __uint_as_float(r[j]),
-                                     epi.beta != 0.0f ? crow[gn + j] : 0.0f,
-                                     epi.bias ? epi.bias[gn + j] : 0.0f);
-      }
-    }
-  }
-}
-
 // Epilogue of one unit through shared memory and TMA stores: per 32-column
 // chunk the warp writes its 32 x 32 block into a 128-byte-swizzled staging
 // box (each lane one row, conflict-free 16-byte stores) and one lane stores
@@ -442,38 +402,63 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
   return true;
 }
 
-// Direct-store epilogue of a full-width unit (C's layout does not allow TMA
-// stores), combined with the other segments' partial sums when cb is set;
-// the partial boxes are loaded through this warp's first staging box.
-__device__ __forceinline__ bool store_unit_direct(uint32_t taddr, float* C,
-                                                  int64_t ldc, int row, int n0,
-                                                  int M, int N, int vec_c,
-                                                  const EpiParams& epi,
-                                                  const SkCombine* cb,
-                                                  uint8_t* ebuf, int lane) {
-  if (!cb) {
-    store_unit<BN>(taddr, C, ldc, row, n0, M, N, vec_c, epi);
-    return true;
-  }
-  // the staging box may still be read by a partial-sum store of this warp
-  if (lane == 0) bulk_wait_read<0>();
-  __syncwarp();
-  float* crow = C + static_cast<int64_t>(row) * ldc;
+// Epilogue of one unit when C's layout does not allow TMA stores (a row
+// stride that is not a multiple of 16 bytes, or an unaligned base).  Per
+// 32-column chunk the warp writes its 32 x 32 block into a swizzled staging
+// box with one row per lane, as the TMA path does, then reads it back by
+// columns and stores it one row at a time: lane j writes column j, so each
+// store instruction writes 128 contiguous bytes (the fused epilogue's reads
+// of C and of the bias are coalesced the same way).  With cb set, each chunk
+// is first combined with the other segments' partial sums, loaded through
+// the same box.  False: a wait ran out.
+template <int W>
+__device__ __forceinline__ bool store_unit_rows(uint32_t taddr, float* C,
+                                                int64_t ldc, int row0, int n0,
+                                                int M, int N,
+                                                const EpiParams& epi,
+                                                const SkCombine* cb,
+                                                uint8_t* ebuf, int lane,
+                                                int& chunk) {
+  const bool plain = epi.alpha == 1.0f && epi.beta == 0.0f && epi.bias == nullptr &&
+                     epi.act == 0;
+  const int rows = M - row0 < 32 ? M - row0 : 32;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < W / 32; ++c) {
+    if (rows <= 0 || n0 + c * 32 >= N) continue;
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + c * 32, r);
+    uint8_t* buf = ebuf + (chunk++ & 1) * EPI_BOX_BYTES;
+    // the box may still be read by an earlier TMA store of this warp (the
+    // partial sums of a stream-K segment)
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
     tmem_ld_wait();
-    if (!combine_chunk(r, *cb, c, ebuf, lane)) return false;
-    const int gn = n0 + c * 32;
-    if (row < M) {
+    if (cb && !combine_chunk(r, *cb, c, buf, lane)) return false;
+    uint8_t* rowp = buf + lane * 128;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (gn + j < N)
-          crow[gn + j] = epi_apply(epi, __uint_as_float(r[j]),
-                                   epi.beta != 0.0f ? crow[gn + j] : 0.0f,
-                                   epi.bias ? epi.bias[gn + j] : 0.0f);
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+          make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    __syncwarp();
+    const int gn = n0 + c * 32 + lane;
+    if (gn < N) {
+      const float bias = epi.bias != nullptr ? epi.bias[gn] : 0.0f;
+      // column `lane` of box row rr: 16-byte group lane / 4, swizzled by rr
+      const uint32_t in_group = static_cast<uint32_t>(lane & 3) * 4;
+      const uint32_t group = static_cast<uint32_t>(lane >> 2);
+      float* cp = C + static_cast<int64_t>(row0) * ldc + gn;
+#pragma unroll 4
+      for (int rr = 0; rr < rows; ++rr) {
+        const float v = *reinterpret_cast<const float*>(
+            buf + rr * 128 + (((group ^ static_cast<uint32_t>(rr & 7)) << 4) | in_group));
+        float* dst = cp + static_cast<int64_t>(rr) * ldc;
+        *dst = plain ? v : epi_apply(epi, v, epi.beta != 0.0f ? *dst : 0.0f, bias);
+      }
     }
+    // every lane has read the box before it is written again, by this
+    // loop's generic stores or by the copy engine (partial-sum loads)
+    fence_proxy_async_smem();
+    __syncwarp();
   }
   return true;
 }
@@ -486,7 +471,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       float* __restrict__ C, int64_t ldc, int M, int N,
                       const PairSchedule sched,
                       unsigned long long* __restrict__ sk_sync,
-                      unsigned long long sk_tag, int vec_c, int tma_c,
+                      unsigned long long sk_tag, int tma_c,
                       unsigned int* __restrict__ status, EpiParams epi) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -715,12 +700,13 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
                                    chunk, C, ldc, epi, nullptr);
           else
-            store_unit<BN / 2>(taddr, C, ldc, row, n0, M, N, vec_c, epi);
+            store_unit_rows<BN / 2>(taddr, C, ldc, row0, n0, M, N, epi, nullptr,
+                                    ebuf, lane, chunk);
         } else {
           good = tma_c ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N,
                                             lane, chunk, C, ldc, epi, cbp)
-                       : store_unit_direct(taddr, C, ldc, row, n0, M, N, vec_c,
-                                           epi, cbp, ebuf, lane);
+                       : store_unit_rows<BN>(taddr, C, ldc, row0, n0, M, N,
+                                             epi, cbp, ebuf, lane, chunk);
         }
       }
       if (!good) {
@@ -807,7 +793,7 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
                                   float* C, int64_t ldc, int M, int N,
                                   const PairSchedule& sched,
                                   unsigned long long* sk_sync,
-                                  unsigned long long sk_tag, bool vec_c,
+                                  unsigned long long sk_tag,
                                   unsigned int* status, const EpiParams& epi,
                                   cudaStream_t stream) {
   if (sched.pairs <= 0) return cudaErrorInvalidValue;
@@ -830,8 +816,8 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   std::memset(&unused, 0, sizeof(unused));
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused,
-      tmW ? *tmW : unused, C, ldc, M, N, sched, sk_sync, sk_tag, vec_c ? 1 : 0,
-      tmC ? 1 : 0, status, epi);
+      tmW ? *tmW : unused, C, ldc, M, N, sched, sk_sync, sk_tag, tmC ? 1 : 0,
+      status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

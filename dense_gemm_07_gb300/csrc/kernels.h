@@ -67,7 +67,7 @@ size_t pair_smem_bytes();
 int pair_max_active(cudaStream_t stream);
 // tmA: box {64, 128}, tmB: box {64, 64}, both 128-byte swizzled.  tmC: FP32
 // map of C (box 32 x 32, 128-byte swizzle) for TMA stores, or nullptr to
-// store directly from registers.  sched: work sharing from pair_schedule()
+// store row segments from the staging boxes with ordinary stores.  sched: work sharing from pair_schedule()
 // (stream_k.cuh); sched.pairs clusters are launched.  When sched.sk_tiles >
 // 0: tmW maps the partial-sum workspace (FP32, 256 columns,
 // sched.sk_pairs * 512 rows, box 32 x 32, 128-byte swizzle), sk_sync points
@@ -79,7 +79,7 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
                                   float* C, int64_t ldc, int M, int N,
                                   const PairSchedule& sched,
                                   unsigned long long* sk_sync,
-                                  unsigned long long sk_tag, bool vec_c,
+                                  unsigned long long sk_tag,
                                   unsigned int* status, const EpiParams& epi,
                                   cudaStream_t stream);
 
@@ -108,9 +108,19 @@ cudaError_t launch_gemm_f32_ladder(int rung, int M, int N, int K, const float* A
 // K == 0: C := act(beta * C + bias) (zeros for the identity epilogue).
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
                                  const EpiParams& epi, cudaStream_t stream);
-// Copy a rows x cols matrix of 16-bit elements to dst with row stride ld_dst.
-cudaError_t launch_copy_rows_u16(const uint16_t* src, int64_t ld_src,
-                                 uint16_t* dst, int64_t ld_dst, int rows,
-                                 int cols, cudaStream_t stream);
+// Copy a rows x cols matrix of 16-bit elements to dst with row stride ld_dst
+// (a multiple of 8; dst 16-byte aligned); columns cols..round_up(cols, 8)-1
+// of dst are zeroed.  Up to two copies run in one launch.
+struct PackJob {
+  const uint16_t* src;
+  int64_t ld_src;
+  uint16_t* dst;
+  int64_t ld_dst;
+  int rows, cols;
+};
+struct PackJobs {
+  PackJob job[2];
+};
+cudaError_t launch_pack_u16(const PackJob* jobs, int count, cudaStream_t stream);
 
 }  // namespace g07

@@ -278,6 +278,31 @@ def test_guard_bands_untouched(kind, shape):
     assert_within(kind, c.cpu().numpy(), c_ref, s_ref, exact=True)
 
 
+@pytest.mark.parametrize("shape,schedule", [
+    ((2048, 2561, 320), g7.abi.SCHEDULE_AUTO),       # 88 tiles: half-width tail units
+    ((2560, 2302, 640), g7.abi.SCHEDULE_STREAM_K),   # partial sums combined on the way out
+    ((300, 258, 200), g7.abi.SCHEDULE_AUTO),
+    ((1000, 127, 127), g7.abi.SCHEDULE_AUTO)])
+def test_bf16_row_store_epilogue_guarded(shape, schedule):
+    # a row stride that is not a multiple of 16 bytes: C is written through
+    # the staging boxes with ordinary row stores (no TMA store), and nothing
+    # outside [0, M) x [0, N) may change
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 29, inputs.INT3, dtype=torch.bfloat16)
+    ldc = N + 1 if (N + 1) % 4 else N + 2
+    buf, c = guarded_output(M, N, ldc, DEV)
+    prev = g7.abi.gemm_set_bf16_schedule(schedule)
+    try:
+        g7.gemm_bf16_f32acc(a.to(DEV), b.to(DEV), out=c)
+        torch.cuda.synchronize()
+    finally:
+        g7.abi.gemm_set_bf16_schedule(prev)
+    assert g7.gemm_get_device_status() == 0
+    assert_guards_intact(buf, M, N, ldc)
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
+
+
 @pytest.mark.parametrize("kind", ["f32", "bf16"])
 def test_leading_dims_and_misaligned_bases(kind):
     M, N, K = 150, 270, 90
