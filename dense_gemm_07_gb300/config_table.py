@@ -1,9 +1,11 @@
 """Time every workload configuration of the method on one GPU and print a
 markdown table (CUDA events on the calling stream, 3 warm-up calls, then
 `--reps` timed calls with a 256 MiB L2 flush before each, queued behind a
-short spin so that host call overhead is not timed; median and best).
+short spin so that host call overhead is not timed; mean and best.  CUDA
+event timestamps on this GPU advance in steps of about 2 us, so the mean
+over many calls, not the median, resolves the short ones).
 
-    python -m dense_gemm_07_gb300.config_table [--reps 20] [--peaks MEASURED_PEAKS.json]
+    python -m dense_gemm_07_gb300.config_table [--reps 40] [--peaks MEASURED_PEAKS.json]
 
 Configurations (the workloads of "How a Matrix Multiply Runs on a GPU",
 "The problem and the roofline", "A06 -- Tiled Matrix Multiply (GEMM)",
@@ -67,13 +69,12 @@ def time_call(fn, reps, flush):
         e1.record()
         e1.synchronize()
         ts.append(e0.elapsed_time(e1) * 1e3)
-    ts.sort()
-    return ts[len(ts) // 2], ts[0]
+    return sum(ts) / len(ts), min(ts)
 
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--reps", type=int, default=20)
+    p.add_argument("--reps", type=int, default=40)
     p.add_argument("--peaks", default=None)
     a = p.parse_args()
     peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
@@ -90,7 +91,7 @@ def main():
     flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
     print(f"peaks ({src}): FP32 {fp32_peak:.1f} TFLOP/s, BF16 {bf16_peak:.1f} TFLOP/s, "
           f"HBM {hbm:.0f} GB/s")
-    print("| cfg | kind | M x N x K | median us | best us | TFLOP/s | GB/s (min bytes) "
+    print("| cfg | kind | M x N x K | mean us | best us | TFLOP/s | GB/s (min bytes) "
           "| roofline | % of roofline |")
     print("|---|---|---|---|---|---|---|---|---|")
     for name, kind, (M, N, K), dist, dist_b, seed in configs():
@@ -99,16 +100,16 @@ def main():
         X, Y = x.to(dev), y.to(dev)
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
         fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
-        med, best = time_call(lambda: fn(X, Y, out=C), a.reps, flush)
+        mean, best = time_call(lambda: fn(X, Y, out=C), a.reps, flush)
         eb = 4 if kind == "f32" else 2
         flops = roofline.gemm_flops(M, N, K)
         nbytes = roofline.min_bytes(M, N, K, eb, 4)
-        tf = flops / (med * 1e-6) / 1e12
-        gbs = nbytes / (med * 1e-6) / 1e9
+        tf = flops / (mean * 1e-6) / 1e12
+        gbs = nbytes / (mean * 1e-6) / 1e9
         peak = fp32_peak if kind == "f32" else bf16_peak
         roof = min(peak, roofline.intensity(M, N, K, eb, 4) * hbm / 1e3)
         bound = "compute" if roof >= peak else "HBM"
-        print(f"| {name} | {kind} | {M}x{N}x{K} | {med:.1f} | {best:.1f} | {tf:.1f} | "
+        print(f"| {name} | {kind} | {M}x{N}x{K} | {mean:.1f} | {best:.1f} | {tf:.1f} | "
               f"{gbs:.0f} | {roof:.0f} TF ({bound}) | {100 * tf / roof:.1f} |")
     if g7.gemm_get_device_status() != 0:
         raise SystemExit("device status error")

@@ -95,7 +95,7 @@ struct SliceLoader {
   const float* b_ptr;  // B[kr0][n0 + nc], advanced by BK rows per slice
   const float* a_base;
   const float* b_base;
-  int64_t a_step;      // 16 rows of A
+  int64_t a_step;      // A_ROW_STEP rows of A
   int64_t b_step;      // B_ROW_STEP rows of B
   uint32_t a_rows_ok;  // bit i: row m0 + r0 + A_ROW_STEP * i < M
   uint32_t b_bytes;    // bytes of this thread's B group inside [0, N)
@@ -189,29 +189,50 @@ __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
 }
 
 // Last block of a split tile: add the `split` parked partial tiles in range
-// order 0, 1, ..., split-1 and write this thread's 8 x 8 patch of C.
+// order 0, 1, ..., split-1 and write this thread's 8 x 8 patch of C.  Four
+// rows at a time: per range, the 8 float4 loads of those rows are issued
+// together before they are added, so each range costs one L2 round trip
+// rather than one per row.
 __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
                                            float* C, int64_t ldc, int M, int N,
                                            int m0, int n0, int row_a, int col_b,
                                            int vec_c, EpiParams epi) {
 #pragma unroll 1
-  for (int i = 0; i < 8; ++i) {
-    const int r = row_a + (i < 4 ? i : 12 + i);
-    const int gm = m0 + r;
-    if (gm >= M) continue;
-    float* crow = C + static_cast<int64_t>(gm) * ldc;
+  for (int g = 0; g < 2; ++g) {
+    // rows row_a + {0..3} (g = 0) and row_a + {16..19} (g = 1)
+    const float* src = tile_ws + (row_a + 16 * g) * BN + col_b;
+    float4 sum[4][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float* src = tile_ws + r * BN + col_b + 32 * h;
-      float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
-      for (int q = 1; q < split; ++q) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + q * (BM * BN)));
-        sum.x += v.x;
-        sum.y += v.y;
-        sum.z += v.z;
-        sum.w += v.w;
-      }
-      store4(crow, n0 + col_b + 32 * h, N, vec_c, sum, epi);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        sum[i][h] = __ldcg(reinterpret_cast<const float4*>(src + i * BN + 32 * h));
+#pragma unroll 1
+    for (int q = 1; q < split; ++q) {
+      const float* part = src + static_cast<int64_t>(q) * (BM * BN);
+      float4 v[4][2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          v[i][h] = __ldcg(reinterpret_cast<const float4*>(part + i * BN + 32 * h));
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          sum[i][h].x += v[i][h].x;
+          sum[i][h].y += v[i][h].y;
+          sum[i][h].z += v[i][h].z;
+          sum[i][h].w += v[i][h].w;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int gm = m0 + row_a + 16 * g + i;
+      if (gm >= M) continue;
+      float* crow = C + static_cast<int64_t>(gm) * ldc;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) store4(crow, n0 + col_b + 32 * h, N, vec_c, sum[i][h], epi);
     }
   }
 }
@@ -399,13 +420,21 @@ F32Plan f32_plan(int M, int N, int K, int64_t slots) {
   if (p.tail > 0) {
     // Split the tiles of the last, partial wave along K so that its blocks
     // fill the resident slots: choose the split with the lowest estimated
-    // time, rounds x (1/split + a per-round overhead for pipeline fill and
-    // the reduction), keeping at least 4 k-slices per range.
+    // time in units of one tile's main loop, rounds x (1/split + a per-round
+    // overhead for the pipeline fill) plus the last block's reading of the
+    // split partial tiles (about 1/15 of a k-slice each), at most 16 ranges.
+    // Ranges keep at least 4 k-slices, unless the split tiles then still
+    // fit in one round of resident blocks (a short K with few tiles, e.g.
+    // 256^3: 4 tiles of 8 slices, spreads over more SMs).
     double best = 1e30;
-    const int max_split = nk / 4 < 16 ? nk / 4 : 16;
-    for (int s = 1; s <= (max_split > 1 ? max_split : 1); ++s) {
+    const int max_split = nk < 16 ? nk : 16;
+    const int long_split = nk / 4 > 1 ? nk / 4 : 1;
+    const double reduce_per_range = 0.07 / nk;
+    for (int s = 1; s <= max_split; ++s) {
       const int64_t rounds = (static_cast<int64_t>(p.tail) * s + slots - 1) / slots;
-      const double cost = static_cast<double>(rounds) * (1.0 / s + 0.04);
+      if (s > long_split && rounds > 1) break;
+      const double cost = static_cast<double>(rounds) * (1.0 / s + 0.04) +
+                          (s > 1 ? reduce_per_range * s : 0.0);
       if (cost < best - 1e-9) {
         best = cost;
         p.split = s;
