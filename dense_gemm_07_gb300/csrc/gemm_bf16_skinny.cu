@@ -64,41 +64,6 @@ __device__ __forceinline__ void raise_abort(volatile int* abort,
   atomicOr(status, 1u);
 }
 
-// Rows m = rank, rank + CS, ... of one 128-column tile (column n_local,
-// n = n0 + n_local of C): each sum is taken over the CS parked partials in
-// rank order 0, 1, ..., CS-1, read through distributed shared memory.  RB
-// rows at a time, so that RB x CS remote loads (at most 32) are in flight
-// before any sum is formed.
-template <int CS>
-__device__ __forceinline__ void reduce_rows(float* __restrict__ C, int64_t ldc, int N,
-                                            int n, int n_local, uint32_t local,
-                                            int rows, int rank, const EpiParams& epi) {
-  constexpr int RB = 32 / CS > 1 ? 32 / CS : 1;
-#pragma unroll 1
-  for (int m0 = rank; m0 < rows; m0 += RB * CS) {
-    float v[RB][CS];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      const int m = m0 + i * CS;
-      const uint32_t off = static_cast<uint32_t>(((m < rows ? m : 0) * TILE_N + n_local) * 4);
-#pragma unroll
-      for (int q = 0; q < CS; ++q)
-        v[i][q] = ld_cluster_f32(map_to_rank(local + off, static_cast<uint32_t>(q)));
-    }
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      const int m = m0 + i * CS;
-      float sum = v[i][0];
-#pragma unroll
-      for (int q = 1; q < CS; ++q) sum += v[i][q];
-      if (m < rows && n < N) {
-        float* p = C + static_cast<int64_t>(m) * ldc + n;
-        *p = epi_apply(epi, sum, epi.beta != 0.0f ? *p : 0.0f, epi.bias ? epi.bias[n] : 0.0f);
-      }
-    }
-  }
-}
-
 template <int NM>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -248,15 +213,34 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
     const int n = n0 + n_local;
     const uint32_t local = smem_u32(smem);
     const int rows = M < NM ? M : NM;
-    switch (cs) {
-      case 1: reduce_rows<1>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 2: reduce_rows<2>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 3: reduce_rows<3>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 4: reduce_rows<4>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 5: reduce_rows<5>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 6: reduce_rows<6>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      case 7: reduce_rows<7>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
-      default: reduce_rows<8>(C, ldc, N, n, n_local, local, rows, rank, epi); break;
+    // Four rows at a time: all their remote loads are issued before any sum
+    // is formed, so their latencies overlap; each sum is then taken in rank
+    // order 0, 1, ..., cs-1.
+    constexpr int RB = 4;
+    for (int m0 = rank; m0 < rows; m0 += RB * cs) {
+      float v[RB][8];
+#pragma unroll
+      for (int i = 0; i < RB; ++i) {
+        const int m = m0 + i * cs;
+        const uint32_t off = static_cast<uint32_t>(((m < rows ? m : 0) * TILE_N + n_local) * 4);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          v[i][q] = q < cs ? ld_cluster_f32(map_to_rank(local + off, static_cast<uint32_t>(q)))
+                           : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < RB; ++i) {
+        const int m = m0 + i * cs;
+        float sum = v[i][0];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          if (q < cs) sum += v[i][q];
+        if (m < rows && n < N) {
+          float* p = C + static_cast<int64_t>(m) * ldc + n;
+          *p = epi_apply(epi, sum, epi.beta != 0.0f ? *p : 0.0f,
+                         epi.bias ? epi.bias[n] : 0.0f);
+        }
+      }
     }
   }
 

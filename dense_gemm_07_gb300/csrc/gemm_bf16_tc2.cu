@@ -43,7 +43,8 @@
 //   warps 2-5 (both)    epilogue: TMEM -> registers -> swizzled shared
 //                       staging box -> TMA tensor store of C (whole lines;
 //                       rows/columns outside C are clipped), or guarded
-//                       direct stores when C's layout does not allow TMA;
+//                       row stores from the same staging box when C's
+//                       layout does not allow TMA;
 //                       then arrive on the even CTA's "accumulator empty"
 //                       (8 arrivals per unit).
 // Tensor memory: NUM_ACC 256-column FP32 accumulators per CTA; with two, a

@@ -4,7 +4,7 @@
 // Method ("GEMM, step by step", section "Concept", register blocking; "A06 --
 // Tiled Matrix Multiply (GEMM)", section 3; "GEMM Optimization", sections 4-5):
 //   * a block of 256 threads owns a 128 x 128 tile of C and walks K in
-//     16-deep slices, staging a 128 x 16 slice of A and a 16 x 128 slice of B
+//     32-deep slices, staging a 128 x 32 slice of A and a 32 x 128 slice of B
 //     in shared memory;
 //   * each thread owns an 8 x 8 patch of C in registers: per k it reads 8
 //     values of A and 8 of B from shared memory and does 64 FMAs, issued as
@@ -15,7 +15,7 @@
 //     16-byte reads of Bs[k][n];
 //   * multi-stage prefetch ("Double buffering" in "GEMM Optimization",
 //     section 5, written with asynchronous copies as "A06", section 3,
-//     suggests): a 3-deep ring of slices is filled with cp.async, which
+//     suggests): a 2-deep ring of slices is filled with cp.async, which
 //     copies global -> shared without passing through registers and zero-fills
 //     out-of-range elements (the ": 0.0f" of the guarded tiled kernel); one
 //     barrier per slice;
