@@ -18,10 +18,13 @@
 // each later one as `split` units of 256 / split columns.
 //
 // Each pair does its data-parallel units first and its stream-K range last.
-// A split tile's first segment is then the end of one pair's range and its
-// second the start of the next pair's: the second is computed early and
-// leaves its partial sums, the first is computed last and adds them, as the
-// pair's final unit, when its operand ring is idle and can hold them.
+// When the ranges span several tiles, a split tile's first segment is the
+// end of one pair's range and its second the start of the next pair's: the
+// second is computed early and leaves its partial sums, the first is
+// computed last and adds them, as the pair's final unit, when its operand
+// ring is idle and can hold them.  When each tile is halved over two pairs,
+// both halves are their pairs' final units and run at the same time; the
+// later one to finish adds them.
 //
 // Everything here is plain integer arithmetic shared by the kernel and by
 // the host (planning, and a host-side listing used by the tests).
@@ -165,12 +168,15 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 // tiles (0 < T):
 //   column split (every mode but kScheduleStreamK, when 2T <= P): the T
 //     tiles run as 2T units of 256 x 128;
-//   stream-K (kScheduleStreamK; kScheduleAuto only for W == 0 with at least
-//   kSkMinSlicesExposed k-slices):
+//   stream-K (kScheduleStreamK):
 //   - W >= 1: the last whole wave and the partial one (P + T tiles) are
 //     shared by all P pairs after W - 1 whole waves (at least a tile's worth
 //     each, so a tile has at most two segments);
-//   - W == 0: each tile is halved over 2T pairs (if 2T <= P).
+//   - W == 0: each tile is halved over 2T pairs (if 2T <= P);
+//   kScheduleAuto, with at least kSkMinSlicesExposed k-slices and 2T <= P:
+//     each tile of the last wave is halved along K over 2T pairs, after the
+//     W whole waves.  Combining the halves costs about as much as 30-40
+//     k-slices, so shorter K keeps the column split.
 // A last wave more than 85 % full, or fewer than kSkMinSlices k-slices, is
 // never split along K.
 inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
@@ -199,17 +205,16 @@ inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
   const bool sk_ok = tiles > 0 && tail > 0 && s.num_kb >= kSkMinSlices &&
                      20 * tail <= 17 * P;
   if (mode == kScheduleNoSplitK || !sk_ok) return column_split();
-  if (mode == kScheduleAuto &&
-      (waves > 0 || s.num_kb < kSkMinSlicesExposed))
-    return column_split();
+  if (mode == kScheduleAuto && s.num_kb < kSkMinSlicesExposed) return column_split();
   int64_t sk_tiles = 0, sk_pairs = 0;
-  if (waves >= 1) {
+  if (waves >= 1 && mode == kScheduleStreamK) {
     sk_tiles = P + tail;
     sk_pairs = P;
   } else {
-    if (2 * tiles > P) return column_split();
-    sk_tiles = tiles;
-    sk_pairs = 2 * tiles;
+    // the last wave's tiles, each halved over two pairs
+    if (2 * tail > P) return column_split();
+    sk_tiles = tail;
+    sk_pairs = 2 * tail;
   }
   s.sk_tiles = static_cast<int>(sk_tiles);
   s.sk_pairs = static_cast<int>(sk_pairs);

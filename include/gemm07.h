@@ -307,14 +307,16 @@ typedef struct gemm_plan {
  * 256 x 256 tiles ("GEMM Optimization", section "L2 Cache and Wave Analysis":
  * a partial last wave leaves SMs idle).
  *   GEMM_SCHEDULE_AUTO: a last wave that fills at most half of the SM pairs
- *       runs as 256 x 128 units; stream-K only when there are fewer tiles
- *       than half the pairs and K has at least 96 64-deep slices.  Default.
+ *       is split: when K has at least 96 64-deep slices, each of its tiles
+ *       is halved along K over two pairs (a tile's two halves are added in
+ *       k order); otherwise its tiles run as 256 x 128 units.  Default.
  *   GEMM_SCHEDULE_STREAM_K: wherever it applies (a last wave at most 85 %
- *       full, K at least 8 slices), the last wave's tiles -- and with two or
- *       more whole waves also the last whole wave's -- are cut into equal
- *       runs of k-slices, one per pair; a tile cut into segments is finished
- *       by adding the segments' partial sums in k order.  Needs 512 KB of
- *       device scratch per SM pair, kept per stream between calls.
+ *       full, K at least 8 slices), the last wave's tiles -- and, after one
+ *       or more whole waves, also the last whole wave's -- are cut into
+ *       equal runs of k-slices, one per pair; a tile cut into segments is
+ *       finished by adding the segments' partial sums in k order.
+ *   Splits along K need 512 KB of device scratch per SM pair that shares
+ *   them, kept per stream between calls.
  *   GEMM_SCHEDULE_COLUMN_SPLIT: never split along K.
  * Every schedule gives the same results up to the order of FP32 additions
  * across a split tile; each is deterministic run to run.

@@ -180,6 +180,23 @@ def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
     _check("bf16", M, N, K, 24, inputs.INT3, exact=True, rows=rows)
 
 
+@pytest.mark.parametrize("shape", [(2560, 2048, 6200),    # 76 whole tiles, 4 halved along K
+                                   (2600, 2100, 6150)])   # ragged edges and K
+def test_bf16_auto_tail_halves_after_whole_waves_exact(shape):
+    # automatic schedule: a whole wave, then the last wave's tiles each
+    # halved along K over two pairs; sampled rows cover the halved tiles
+    M, N, K = shape
+    s, plan = g7.plan("bf16", M, N, K)
+    assert plan.dp_tiles == 76 and plan.sk_pairs == 2 * plan.sk_tiles > 0
+    a, b = inputs.make_pair(M, N, K, 27, inputs.INT3, dtype=torch.bfloat16)
+    c = g7.gemm_bf16_f32acc(a.to(DEV), b.to(DEV))
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    rows = np.unique(np.concatenate([np.arange(0, M, 173), np.arange(M - 300, M, 37), [M - 1]]))
+    c_ref, _ = oracle_ref("bf16", a, b, rows=rows, with_abs=False)
+    assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
+
+
 @pytest.mark.parametrize("shape", [(2560, 2304, 1024), (4096, 4096, 1024)])
 def test_bf16_stream_k_deterministic_bits(stream_k, shape):
     M, N, K = shape

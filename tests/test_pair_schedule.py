@@ -46,6 +46,8 @@ CASES = [
     (4096, 4096, 4096, 10),     # other resident counts
     (2560, 2304, 777, 7),
     (4096, 4096, 200, 76),      # 4 k-slices: too short to split along K
+    (4096, 4096, 8192, 76),     # 3 whole waves, then 28 tiles halved along K
+    (2560, 2048, 6200, 76),     # 1 whole wave, then 4 tiles halved (ragged K)
 ]
 
 
@@ -138,6 +140,15 @@ def test_schedule_setting_and_plans(lib):
         # few tiles and long K: each of the 8 tiles halved along K
         sched, ws = _plan(512, 1024, 8192)
         assert sched == (0, 8, 16, 16) and ws >= 16 * 4 * 128 * 1024
+        # whole waves, then a last wave of 28 tiles with 128 k-slices: each
+        # tail tile halved along K over 56 pairs; 64 k-slices keep the
+        # column split
+        assert _plan(4096, 4096, 8192) == ((228, 28, 56, 76), 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8)
+        assert _plan(8192, 8192, 8192)[0] == (988, 36, 72, 76)
+        assert _plan(4096, 4096, 6144)[0] == (228, 28, 56, 76)
+        assert _plan(4096, 4096, 6080)[0] == (256, 0, 0, 76)   # 95 k-slices
+        # a last wave of 52 tiles is more than half the pairs: no split
+        assert _plan(2048, 4096, 11008) == ((128, 0, 0, 76), 0)
         assert _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K) == _abi.SCHEDULE_AUTO
         # stream-K: the last whole wave and the partial one are shared
         sched, ws = _plan(4096, 4096, 4096)
