@@ -293,6 +293,15 @@ __device__ __forceinline__ void box_read_row(const uint8_t* buf, int lane,
 __device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
                                               const SkCombine& cb, int c,
                                               uint8_t* buf, int lane) {
+  if (cb.nseg == 2 && cb.stash) {
+    // Two segments, the other's already in shared memory: a + b == b + a
+    // exactly, so adding it to this segment's sums gives the k-order sum.
+    float v[32];
+    box_read_row(cb.stash + c * EPI_BOX_BYTES, lane, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + v[i]);
+    return true;
+  }
   float acc[32];
 #pragma unroll 1
   for (int s = 0; s < cb.nseg; ++s) {

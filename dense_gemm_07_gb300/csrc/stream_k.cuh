@@ -47,7 +47,7 @@ struct PairSchedule {
 
 // How the last, partial wave is shared.
 enum PairScheduleMode {
-  kScheduleAuto = 0,     // column split; stream-K only for few tiles, long K
+  kScheduleAuto = 0,     // the estimated fastest (pair_schedule_cost)
   kScheduleStreamK = 1,  // stream-K wherever it applies
   kScheduleNoSplitK = 2  // never stream-K (column split only)
 };
@@ -59,10 +59,8 @@ constexpr int kSkSliceK = 64;
 // range at least half a tile long, which bounds it by 3; whole-wave
 // schedules and aligned halves give 2).
 constexpr int kSkMaxSeg = 3;
-// Shortest k extent (in slices) worth splitting at all, and the shortest
-// one worth splitting when no whole wave follows to hide the combining.
+// Shortest k extent (in slices) worth splitting at all.
 constexpr int kSkMinSlices = 8;
-constexpr int kSkMinSlicesExposed = 96;
 
 __host__ __device__ inline int64_t sk_total(const PairSchedule& s) {
   return static_cast<int64_t>(s.sk_tiles) * s.num_kb;
@@ -173,12 +171,30 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 //     shared by all P pairs after W - 1 whole waves (at least a tile's worth
 //     each, so a tile has at most two segments);
 //   - W == 0: each tile is halved over 2T pairs (if 2T <= P);
-//   kScheduleAuto, with at least kSkMinSlicesExposed k-slices and 2T <= P:
-//     each tile of the last wave is halved along K over 2T pairs, after the
-//     W whole waves.  Combining the halves costs about as much as 30-40
-//     k-slices, so shorter K keeps the column split.
+//   halving (kScheduleAuto only): each tile of the last wave is halved along
+//     K over 2T pairs (2T <= P), after the W whole waves;
+//   kScheduleAuto takes whichever of these (or the plain or column-split
+//     last wave) has the lowest estimated time, pair_schedule_cost().
 // A last wave more than 85 % full, or fewer than kSkMinSlices k-slices, is
 // never split along K.
+// Estimated time of a schedule in units of one k-slice of one pair (about
+// 0.3 us on a GB300), for W whole waves of P pairs, a last wave of T tiles
+// and kb k-slices per tile.  Measured on the paired kernel: a 256 x 128
+// unit takes as long as a whole tile (operand delivery, not the MMA, paces
+// it), so the column split saves only epilogue time; adding the two halves
+// of a tile costs about 43 slices after its main loop; a stream-K run over
+// the last whole wave and the partial one costs about 25 slices more (its
+// early segments write partial sums beside the running main loops).
+enum PairScheduleKind { kPlainTail = 0, kColumnTail = 1, kHalvedTail = 2, kStreamKTail = 3 };
+inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb) {
+  switch (kind) {
+    case kPlainTail: return (W + 1) * kb + 16;
+    case kColumnTail: return (W + 1) * kb + 8;
+    case kHalvedTail: return W * kb + (kb + 1) / 2 + 43;
+    default: return (W - 1) * kb + ((P + T) * kb + P - 1) / P + 68;
+  }
+}
+
 inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
                                   int max_pairs, int mode) {
   PairSchedule s;
@@ -205,9 +221,22 @@ inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
   const bool sk_ok = tiles > 0 && tail > 0 && s.num_kb >= kSkMinSlices &&
                      20 * tail <= 17 * P;
   if (mode == kScheduleNoSplitK || !sk_ok) return column_split();
-  if (mode == kScheduleAuto && s.num_kb < kSkMinSlicesExposed) return column_split();
+  bool full_sk = waves >= 1 && mode == kScheduleStreamK;
+  if (mode == kScheduleAuto) {
+    // The simpler schedule unless a split along K is estimated to save more
+    // than 8 slices (about 2.5 us).
+    const int64_t kb = s.num_kb;
+    const int64_t base = pair_schedule_cost(col_split ? kColumnTail : kPlainTail, waves, tail, P, kb);
+    const int64_t halved = 2 * tail <= P ? pair_schedule_cost(kHalvedTail, waves, tail, P, kb)
+                                         : INT64_MAX;
+    const int64_t streamk = waves >= 1 ? pair_schedule_cost(kStreamKTail, waves, tail, P, kb)
+                                       : INT64_MAX;
+    const int64_t best_k = halved < streamk ? halved : streamk;
+    if (best_k + 8 >= base) return column_split();
+    full_sk = streamk < halved;
+  }
   int64_t sk_tiles = 0, sk_pairs = 0;
-  if (waves >= 1 && mode == kScheduleStreamK) {
+  if (full_sk) {
     sk_tiles = P + tail;
     sk_pairs = P;
   } else {

@@ -306,10 +306,11 @@ typedef struct gemm_plan {
  * How the BF16 paired-SM kernel (M > 128) shares out a partial last wave of
  * 256 x 256 tiles ("GEMM Optimization", section "L2 Cache and Wave Analysis":
  * a partial last wave leaves SMs idle).
- *   GEMM_SCHEDULE_AUTO: a last wave that fills at most half of the SM pairs
- *       is split: when K has at least 96 64-deep slices, each of its tiles
- *       is halved along K over two pairs (a tile's two halves are added in
- *       k order); otherwise its tiles run as 256 x 128 units.  Default.
+ *   GEMM_SCHEDULE_AUTO: the estimated fastest of running the last wave as
+ *       it is, as 256 x 128 units (when it fills at most half of the SM
+ *       pairs), with each of its tiles halved along K over two pairs, or
+ *       as GEMM_SCHEDULE_STREAM_K; a split along K is taken only when it is
+ *       estimated to save more than about 2.5 us.  Default.
  *   GEMM_SCHEDULE_STREAM_K: wherever it applies (a last wave at most 85 %
  *       full, K at least 8 slices), the last wave's tiles -- and, after one
  *       or more whole waves, also the last whole wave's -- are cut into

@@ -180,14 +180,15 @@ def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
     _check("bf16", M, N, K, 24, inputs.INT3, exact=True, rows=rows)
 
 
-@pytest.mark.parametrize("shape", [(2560, 2048, 6200),    # 76 whole tiles, 4 halved along K
-                                   (2600, 2100, 6150)])   # ragged edges and K
-def test_bf16_auto_tail_halves_after_whole_waves_exact(shape):
-    # automatic schedule: a whole wave, then the last wave's tiles each
-    # halved along K over two pairs; sampled rows cover the halved tiles
+@pytest.mark.parametrize("shape,dp,sk,skp", [
+    ((2560, 2048, 6200), 0, 80, 76),     # one wave + 4 tiles: all 80 shared as k runs
+    ((2600, 2100, 6150), 76, 23, 46)])   # one wave, then 23 tiles halved; ragged
+def test_bf16_auto_k_splits_after_whole_waves_exact(shape, dp, sk, skp):
+    # automatic schedule after a whole wave: stream-K over every tile, or
+    # the last wave's tiles halved along K; sampled rows cover the split tiles
     M, N, K = shape
     s, plan = g7.plan("bf16", M, N, K)
-    assert plan.dp_tiles == 76 and plan.sk_pairs == 2 * plan.sk_tiles > 0
+    assert (plan.dp_tiles, plan.sk_tiles, plan.sk_pairs) == (dp, sk, skp)
     a, b = inputs.make_pair(M, N, K, 27, inputs.INT3, dtype=torch.bfloat16)
     c = g7.gemm_bf16_f32acc(a.to(DEV), b.to(DEV))
     torch.cuda.synchronize()

@@ -141,14 +141,20 @@ def test_schedule_setting_and_plans(lib):
         sched, ws = _plan(512, 1024, 8192)
         assert sched == (0, 8, 16, 16) and ws >= 16 * 4 * 128 * 1024
         # whole waves, then a last wave of 28 tiles with 128 k-slices: each
-        # tail tile halved along K over 56 pairs; 64 k-slices keep the
-        # column split
+        # tail tile halved along K over 56 pairs (64 k-slices keep the
+        # column split, above)
         assert _plan(4096, 4096, 8192) == ((228, 28, 56, 76), 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8)
         assert _plan(8192, 8192, 8192)[0] == (988, 36, 72, 76)
         assert _plan(4096, 4096, 6144)[0] == (228, 28, 56, 76)
-        assert _plan(4096, 4096, 6080)[0] == (256, 0, 0, 76)   # 95 k-slices
+        assert _plan(2560, 2560, 8192)[0] == (76, 24, 48, 76)
+        # one whole wave and a small last wave: every tile shared (stream-K)
+        assert _plan(2560, 2048, 6200)[0] == (0, 80, 76, 76)
+        assert _plan(2304, 2304, 8192)[0] == (0, 81, 76, 76)
+        # ... but with 64 k-slices the gain is within the margin
+        assert _plan(2560, 2048, 4096)[0] == (80, 0, 0, 76)
         # a last wave of 52 tiles is more than half the pairs: no split
         assert _plan(2048, 4096, 11008) == ((128, 0, 0, 76), 0)
+        assert _plan(2048, 11008, 4096) == ((344, 0, 0, 76), 0)
         assert _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K) == _abi.SCHEDULE_AUTO
         # stream-K: the last whole wave and the partial one are shared
         sched, ws = _plan(4096, 4096, 4096)
