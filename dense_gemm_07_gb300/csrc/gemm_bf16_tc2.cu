@@ -352,7 +352,8 @@ __device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
 // cb set, each chunk is first combined with the other segments' partial
 // sums (loaded into the same box); tmOut is C's map, or the workspace's
 // when a segment leaves its partial sums (identity epilogue, M = N = the
-// workspace's extent).  W: the unit's width.  False: a wait ran out.
+// workspace's extent).  With `reduce`, the boxes are added to tmOut's
+// elements instead of stored.  W: the unit's width.  False: a wait ran out.
 template <int W>
 __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
                                                const CUtensorMap* tmOut,
@@ -361,7 +362,8 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
                                                int& chunk, const float* C,
                                                int64_t ldc,
                                                const EpiParams& epi,
-                                               const SkCombine* cb) {
+                                               const SkCombine* cb,
+                                               bool reduce = false) {
 #pragma unroll 1
   for (int c = 0; c < W / 32; ++c) {
     // Boxes wholly outside C are skipped (warp-uniform test); every other
@@ -405,7 +407,10 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
     __syncwarp();
     // partial boxes are clipped by the copy engine
     if (lane == 0) {
-      tma_store_2d(tmOut, buf, n0 + c * 32, row0);
+      if (reduce)
+        tma_reduce_add_2d(tmOut, buf, n0 + c * 32, row0);
+      else
+        tma_store_2d(tmOut, buf, n0 + c * 32, row0);
       bulk_commit();
     }
   }
@@ -619,14 +624,21 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              static_cast<uint32_t>(acc * BN);
       const int row0 = row - lane;
 
-      int ready_slot = -1;  // >= 0: partial sums left in this slot
+      int ready_slot = -1;  // >= 0: this segment's flag goes up after its stores
       SkCombine cb;
       const SkCombine* cbp = nullptr;
+      bool reduce_c = false;  // add this segment into C (the other one is there)
       bool good = true;
       if (w.k0 != 0 || w.k1 != sched.num_kb) {
         // A stream-K segment: take a ticket; the last of the tile's
         // segments finishes it, the others leave their partial sums.
         const SkTile st = sk_tile(sched, w.tile);
+        // Two segments, C open to TMA and no term besides alpha * A.B: the
+        // first to finish stores its share straight into C and the second
+        // adds its own with a TMA reduction.  a + b == b + a, so the bits do
+        // not depend on which finishes first.
+        const bool direct = tma_c && st.nseg == 2 && epi.beta == 0.0f &&
+                            epi.bias == nullptr && epi.act == 0;
         int ticket = 0;
         if (lane == 0)
           ticket = sk_take_ticket(sk_ticket(sk_sync, sched, w.tile, rank, q), sk_tag);
@@ -635,10 +647,12 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           good = false;
         } else if (ticket + 1 < st.nseg) {
           ready_slot = sk_slot(sched, pair, w.tile);
-          good = store_unit_tma<BN>(taddr, &tmW, ebuf,
-                                    sk_row(pair, ready_slot, rank, q), 0,
-                                    0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
-                                    epi_identity(), nullptr);
+          good = direct ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
+                                             chunk, C, ldc, epi, nullptr)
+                        : store_unit_tma<BN>(taddr, &tmW, ebuf,
+                                             sk_row(pair, ready_slot, rank, q), 0,
+                                             0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
+                                             epi_identity(), nullptr);
         } else {
           cb.tmW = &tmW;
           cb.sched = &sched;
@@ -680,7 +694,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           got = __shfl_sync(0xffffffffu, got, 0);
           good = got != 0;
-          if (good && last_unit && st.nseg == 2) {
+          reduce_c = direct;
+          if (good && !direct && last_unit && st.nseg == 2) {
             // This CTA's operand ring is idle: every MMA of the pair has
             // completed (this unit's accumulator is full) and no copy is
             // left to issue.  Load the other segment's 8 boxes at once into
@@ -700,7 +715,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             good = __shfl_sync(0xffffffffu, ld, 0) != 0;
             cb.stash = stash;
           }
-          cbp = &cb;
+          if (!direct) cbp = &cb;
         }
       }
       if (good && ready_slot < 0) {
@@ -714,7 +729,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                     ebuf, lane, chunk);
         } else {
           good = tma_c ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N,
-                                            lane, chunk, C, ldc, epi, cbp)
+                                            lane, chunk, C, ldc, epi, cbp, reduce_c)
                        : store_unit_rows<BN>(taddr, C, ldc, row0, n0, M, N,
                                              epi, cbp, ebuf, lane, chunk);
         }
@@ -728,8 +743,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       if (lane == 0) {
         mbar_arrive_cluster(map_to_rank(smem_u32(&ctl->acc_empty[acc]), 0));
         if (ready_slot >= 0) {
-          // The partial sums are in global memory (copies complete) before
-          // the flag says so.
+          // The segment's sums are in global memory (copies complete)
+          // before the flag says so.
           bulk_wait_all();
           fence_proxy_async_global();
           __threadfence();

@@ -179,21 +179,28 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 // never split along K.
 // Estimated time of a schedule in units of one k-slice of one pair (about
 // 0.3 us on a GB300), for W whole waves of P pairs, a last wave of T tiles
-// and kb k-slices per tile.  Measured on the paired kernel: a 256 x 128
-// unit takes as long as a whole tile (operand delivery, not the MMA, paces
-// it), so the column split saves only epilogue time; adding the two halves
-// of a tile costs about 43 slices after its main loop; a stream-K run over
-// the last whole wave and the partial one costs about 25 slices more (its
-// early segments write partial sums beside the running main loops).
+// and kb k-slices per tile, fitted to measurements of the paired kernel: a
+// 256 x 128 unit takes as long as a whole tile (operand delivery, not the
+// MMA, paces it), so the column split saves only epilogue time; finishing
+// a tile halved along K costs about 44 slices after its main loop; a
+// stream-K run over the last whole wave and the partial one costs 30 +
+// 0.3 kb slices (its pairs work on different k of different tiles at once,
+// so fewer operand reads are shared in L2).
 enum PairScheduleKind { kPlainTail = 0, kColumnTail = 1, kHalvedTail = 2, kStreamKTail = 3 };
 inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb) {
   switch (kind) {
     case kPlainTail: return (W + 1) * kb + 16;
     case kColumnTail: return (W + 1) * kb + 8;
-    case kHalvedTail: return W * kb + (kb + 1) / 2 + 43;
-    default: return (W - 1) * kb + ((P + T) * kb + P - 1) / P + 68;
+    case kHalvedTail: return W * kb + (kb + 1) / 2 + 44;
+    default: return (W - 1) * kb + ((P + T) * kb + P - 1) / P + 30 + (3 * kb) / 10;
   }
 }
+
+// Operands larger than this (bytes of A and B) are not shared out as
+// stream-K runs by the automatic schedule: with pairs at different k, L2 no
+// longer holds what they read (2048 x 4096 x 11008, 135 MB: 138 against
+// 116 us for whole tiles).
+constexpr int64_t kSkAutoMaxOperandBytes = 96ll << 20;
 
 inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
                                   int max_pairs, int mode) {
@@ -229,8 +236,10 @@ inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
     const int64_t base = pair_schedule_cost(col_split ? kColumnTail : kPlainTail, waves, tail, P, kb);
     const int64_t halved = 2 * tail <= P ? pair_schedule_cost(kHalvedTail, waves, tail, P, kb)
                                          : INT64_MAX;
-    const int64_t streamk = waves >= 1 ? pair_schedule_cost(kStreamKTail, waves, tail, P, kb)
-                                       : INT64_MAX;
+    const bool fits = 2 * (M * K + K * N) <= kSkAutoMaxOperandBytes;
+    const int64_t streamk = waves >= 1 && fits
+                                ? pair_schedule_cost(kStreamKTail, waves, tail, P, kb)
+                                : INT64_MAX;
     const int64_t best_k = halved < streamk ? halved : streamk;
     if (best_k + 8 >= base) return column_split();
     full_sk = streamk < halved;

@@ -182,7 +182,8 @@ def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
 
 @pytest.mark.parametrize("shape,dp,sk,skp", [
     ((2560, 2048, 6200), 0, 80, 76),     # one wave + 4 tiles: all 80 shared as k runs
-    ((2600, 2100, 6150), 76, 23, 46)])   # one wave, then 23 tiles halved; ragged
+    ((2600, 2100, 6150), 0, 99, 76),     # the same with ragged edges and K
+    ((2560, 2560, 8192), 76, 24, 48)])   # one wave, then 24 tiles halved along K
 def test_bf16_auto_k_splits_after_whole_waves_exact(shape, dp, sk, skp):
     # automatic schedule after a whole wave: stream-K over every tile, or
     # the last wave's tiles halved along K; sampled rows cover the split tiles

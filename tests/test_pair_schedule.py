@@ -150,8 +150,10 @@ def test_schedule_setting_and_plans(lib):
         # one whole wave and a small last wave: every tile shared (stream-K)
         assert _plan(2560, 2048, 6200)[0] == (0, 80, 76, 76)
         assert _plan(2304, 2304, 8192)[0] == (0, 81, 76, 76)
-        # ... but with 64 k-slices the gain is within the margin
-        assert _plan(2560, 2048, 4096)[0] == (80, 0, 0, 76)
+        assert _plan(2560, 2048, 4096)[0] == (0, 80, 76, 76)
+        # a last whole wave and a small partial one, but 32 k-slices: the
+        # column split
+        assert _plan(4096, 4096, 2048)[0] == (256, 0, 0, 76)
         # a last wave of 52 tiles is more than half the pairs: no split
         assert _plan(2048, 4096, 11008) == ((128, 0, 0, 76), 0)
         assert _plan(2048, 11008, 4096) == ((344, 0, 0, 76), 0)
