@@ -635,6 +635,18 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   return s;
 }
 
+// Rows of the largest block of whole tile rows, within [lo, hi] of M, whose
+// tiles fill whole waves of `slots` resident blocks; 0 if there is none.
+int64_t whole_wave_rows(int64_t M, int64_t N, int tile_m, int tile_n, int64_t slots,
+                        double lo, double hi) {
+  if (slots <= 0) return 0;
+  const int64_t tm = (M + tile_m - 1) / tile_m, tn = (N + tile_n - 1) / tile_n;
+  for (int64_t r = static_cast<int64_t>(hi * static_cast<double>(tm));
+       r >= 1 && static_cast<double>(r) >= lo * static_cast<double>(tm); --r)
+    if ((r * tn) % slots == 0 && r * tile_m < M) return r * tile_m;
+  return 0;
+}
+
 // Host-buffer variant: stage through pool memory and overlap the copies with
 // the GEMM.  A is split into `chunks` row blocks; each block's GEMM runs on
 // the caller's stream as soon as its rows (and B) have arrived, and each
@@ -648,11 +660,16 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
 // C := A_k B_k + C): its first GEMM starts once one piece of the operands
 // has arrived.  The first rows' sums are then added in that order.  This
 // pays when the GEMM, not the link, takes the time (FP32).
+//
+// With `head_rows` > 0 there are two blocks, rows [0, head_rows) and the
+// rest: a head block that is a whole number of waves of resident tiles
+// keeps the block GEMMs from adding partial waves of their own.
 template <typename T, typename Run>
 gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
                        int64_t lda, const T* B, int64_t ldb, float* C,
                        int64_t ldc, cudaStream_t stream, int max_chunks,
-                       int64_t min_chunk_rows, int max_parts, Run run) {
+                       int64_t min_chunk_rows, int max_parts, int64_t head_rows,
+                       Run run) {
   gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (s != GEMM_OK || M == 0 || N == 0) return s;
   DeviceState* d = nullptr;
@@ -666,6 +683,8 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   if (chunks < 1 || K == 0) chunks = 1;
   constexpr int kMaxChunks = 8;
   if (chunks > kMaxChunks) chunks = kMaxChunks;
+  if (head_rows <= 0 || head_rows >= M || K == 0) head_rows = 0;
+  if (head_rows > 0) chunks = 2;
   constexpr int kParts = 8;          // at most this many pieces of K
   constexpr int64_t kMinPartK = 512;
   int k_parts = max_parts < kParts ? max_parts : kParts;
@@ -703,6 +722,7 @@ gemm_status_t run_host(int64_t M, int64_t N, int64_t K, const T* A,
   // on whole 128-row tiles where the rows allow
   auto row_at = [&](int64_t i) -> int64_t {
     if (i >= chunks) return M;
+    if (head_rows > 0) return i == 0 ? 0 : head_rows;
     const int64_t r = M * i / chunks;
     const int64_t q = (r + 64) / 128 * 128;
     return q > 0 && q < M ? q : r;
@@ -986,9 +1006,14 @@ gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t K,
 gemm_status_t gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* A,
                             int64_t lda, const float* B, int64_t ldb, float* C,
                             int64_t ldc, void* stream) {
+  // A head block of whole waves of 128 x 128 tiles, 30-60 % of the rows, if
+  // one exists (4096 x 4096: 2432 rows, two waves of 304 tiles).
+  const int64_t head =
+      M >= 2048 && N > 0 ? whole_wave_rows(M, N, kF32TileM, kF32TileN, f32_slots(), 0.3, 0.6)
+                         : 0;
   return run_host<float>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      /*max_chunks=*/3, /*min_chunk_rows=*/1024, /*max_parts=*/4,
+      /*max_chunks=*/3, /*min_chunk_rows=*/1024, /*max_parts=*/4, head,
       [](int64_t m, int64_t n, int64_t k, const float* a, int64_t la, const float* b,
          int64_t lb, float* c, int64_t lc, const EpiParams& e, cudaStream_t st) {
         return run_f32(m, n, k, a, la, b, lb, c, lc, st, e);
@@ -1001,7 +1026,7 @@ gemm_status_t gemm_bf16_f32acc_host(int64_t M, int64_t N, int64_t K,
                                     int64_t ldc, void* stream) {
   return run_host<uint16_t>(
       M, N, K, A, lda, B, ldb, C, ldc, static_cast<cudaStream_t>(stream),
-      /*max_chunks=*/4, /*min_chunk_rows=*/512, /*max_parts=*/1,
+      /*max_chunks=*/4, /*min_chunk_rows=*/512, /*max_parts=*/1, /*head_rows=*/0,
       [](int64_t m, int64_t n, int64_t k, const uint16_t* a, int64_t la,
          const uint16_t* b, int64_t lb, float* c, int64_t lc, const EpiParams& e,
          cudaStream_t st) { return run_bf16(m, n, k, a, la, b, lb, c, lc, st, e); });

@@ -199,7 +199,9 @@ GEMM07_API gemm_status_t gemm_f32_ladder(int rung, int64_t M, int64_t N, int64_t
  * call stages A and B in device buffers from the library's memory pool,
  * runs the GEMM and copies C back, and returns once C is in host memory
  * (it synchronises `stream`).  A is split into row blocks (up to 3 for
- * FP32, 4 for BF16, boundaries on whole 128-row tiles); uploads run on a
+ * FP32, 4 for BF16, boundaries on whole 128-row tiles; for FP32, when a
+ * block of 30-60 % of the rows fills whole waves of the GPU's resident
+ * 128 x 128 tiles, that block and the rest); uploads run on a
  * library-owned upload stream, each block's product is computed on
  * `stream` as soon as its operands arrive, and each block of C is copied
  * back on a library-owned download stream while the next block computes,

@@ -405,6 +405,21 @@ def test_host_buffer_variant_k_pieces(kind, shape):
     assert g7.gemm_get_device_status() == 0
 
 
+@pytest.mark.parametrize("shape", [(4096, 2048, 2304), (4096, 2048, 640)])
+def test_f32_host_whole_wave_head_block(shape):
+    # FP32 host variant with a head block of whole waves: 2432 rows (19 tile
+    # rows x 16 tile columns = two waves of 304 resident blocks), then the
+    # other 1664 rows; with K = 2304 the head block goes up and accumulates
+    # in four K pieces
+    M, N, K = shape
+    a, b = inputs.make_pair(M, N, K, 31, inputs.INT4, dtype=torch.float32)
+    c = g7.gemm_f32_host(a.pin_memory(), b.pin_memory())
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), np.arange(2400, 2470), [M - 1]]))
+    c_ref, _ = oracle_ref("f32", a, b, rows=rows, with_abs=False)
+    assert_within("f32", c.numpy()[rows], c_ref, None, exact=True)
+    assert g7.gemm_get_device_status() == 0
+
+
 def test_streams_are_respected():
     a, b = inputs.make_pair(1024, 1024, 1024, 15, inputs.INT3, dtype=torch.bfloat16)
     s = torch.cuda.Stream()
