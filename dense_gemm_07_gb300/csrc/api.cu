@@ -161,11 +161,12 @@ gemm_status_t plan_f32(int64_t M, int64_t N, int64_t K, const void* A,
     return GEMM_OK;
   }
   p->path = GEMM_PATH_F32_SIMT;
-  p->tile_m = kF32TileM;
-  p->tile_n = kF32TileN;
+  const bool small = f32_small_problem(M, N, K);
+  p->tile_m = small ? kF32SmallTile : kF32TileM;
+  p->tile_n = small ? kF32SmallTile : kF32TileN;
   p->tile_k = kF32TileK;
   p->stages = 2;
-  p->tiles = ((M + kF32TileM - 1) / kF32TileM) * ((N + kF32TileN - 1) / kF32TileN);
+  p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
   return GEMM_OK;
 }

@@ -361,6 +361,151 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   }
 }
 
+// ------------------------------------------------------ small problems
+//
+// At most 16 tiles of 128 x 128 leave most SMs idle and each block a long
+// serial K loop.  Small problems therefore run as 64 x 64 tiles, every tile
+// split into `split` ranges of k-slices (a range may be a single slice), so
+// that the blocks fill the GPU; the ranges are added in order by the last
+// block of each tile, as for the wave tail above.  256 threads as 16 x 16,
+// each a 4 x 4 patch (rows 4ty.., columns 4tx..); per k one 16-byte read of
+// the transposed A slice and one of B; a 2-deep cp.async ring; plain FMAs.
+constexpr int SB = kF32SmallTile;   // 64
+constexpr int S_STRIDE = SB + 4;    // transposed A rows, padded
+struct SmallStage {
+  float a[BK][S_STRIDE];
+  float b[BK][SB];
+};
+
+template <bool VEC_B>
+__global__ void __launch_bounds__(THREADS)
+gemm_f32_small_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda,
+                      const float* __restrict__ B, int64_t ldb, float* __restrict__ C,
+                      int64_t ldc, int tiles_n, int split, int vec_c,
+                      float* __restrict__ ws, unsigned int* __restrict__ counters,
+                      EpiParams epi) {
+  __shared__ __align__(16) SmallStage st[2];
+  __shared__ int last_block;
+  const int tile = blockIdx.x / split;
+  const int piece = blockIdx.x % split;
+  const int m0 = (tile / tiles_n) * SB, n0 = (tile % tiles_n) * SB;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int nk_all = (K + BK - 1) / BK;
+  const int kt0 = static_cast<int>(static_cast<int64_t>(nk_all) * piece / split);
+  const int kt1 = static_cast<int>(static_cast<int64_t>(nk_all) * (piece + 1) / split);
+  // copy plan: A element (row tid / 32 + 8i, k tid % 32); B 16-byte groups
+  // (row tid / 16 + 16j, columns 4 (tid % 16)..), or single elements (row
+  // tid / 64 + 4j, column tid % 64)
+  const int ak = tid & 31, ar = tid >> 5;
+  auto load = [&](int buf, int kt) {
+    const uint32_t sa = smem_addr(&st[buf]);
+    const int k0 = kt * BK;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = ar + 8 * i, gm = m0 + r, gk = k0 + ak;
+      const bool ok = gm < M && gk < K;
+      cp_async4(sa + static_cast<uint32_t>((ak * S_STRIDE + r) * 4),
+                ok ? A + static_cast<int64_t>(gm) * lda + gk : A, ok ? 4u : 0u);
+    }
+    const uint32_t sb = sa + static_cast<uint32_t>(offsetof(SmallStage, b));
+    if (VEC_B) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = (tid >> 4) + 16 * j, c = (tid & 15) * 4, gk = k0 + r, gn = n0 + c;
+        const uint32_t bytes =
+            gk < K && gn < N ? (N - gn >= 4 ? 16u : static_cast<uint32_t>(N - gn) * 4u) : 0u;
+        cp_async16(sb + static_cast<uint32_t>((r * SB + c) * 4),
+                   bytes ? B + static_cast<int64_t>(gk) * ldb + gn : B, bytes);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = (tid >> 6) + 4 * j, c = tid & 63, gk = k0 + r, gn = n0 + c;
+        const bool ok = gk < K && gn < N;
+        cp_async4(sb + static_cast<uint32_t>((r * SB + c) * 4),
+                  ok ? B + static_cast<int64_t>(gk) * ldb + gn : B, ok ? 4u : 0u);
+      }
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  if (kt0 < kt1) load(0, kt0);
+  cp_async_commit();
+  for (int kt = kt0; kt < kt1; ++kt) {
+    const int buf = (kt - kt0) & 1;
+    if (kt + 1 < kt1) load(buf ^ 1, kt + 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // this thread's copies of slice kt landed
+    __syncthreads();     // everyone's
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&st[buf].a[k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&st[buf].b[k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();     // slice kt consumed before its buffer is refilled
+  }
+  cp_async_wait<0>();
+  const int col = n0 + tx * 4;
+  if (split > 1) {
+    float* tile_ws = ws + static_cast<int64_t>(tile) * split * (SB * SB);
+    float* mine = tile_ws + piece * (SB * SB);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      __stcg(reinterpret_cast<float4*>(mine + (ty * 4 + i) * SB + tx * 4),
+             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+      last_block = atomicAdd(&counters[tile], 1u) == static_cast<unsigned>(split - 1);
+    __syncthreads();
+    if (!last_block) return;
+    __threadfence();
+    // ranges added in order 0, 1, ..., split - 1; each range's four loads
+    // of this thread are in flight together
+    float4 sum[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      sum[i] = __ldcg(reinterpret_cast<const float4*>(tile_ws + (ty * 4 + i) * SB + tx * 4));
+#pragma unroll 1
+    for (int q = 1; q < split; ++q) {
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = __ldcg(reinterpret_cast<const float4*>(tile_ws + q * (SB * SB) +
+                                                     (ty * 4 + i) * SB + tx * 4));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sum[i].x += v[i].x;
+        sum[i].y += v[i].y;
+        sum[i].z += v[i].z;
+        sum[i].w += v[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int gm = m0 + ty * 4 + i;
+      if (gm < M) store4(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c, sum[i], epi);
+    }
+    if (tid == 0) counters[tile] = 0;  // leave the counter as found
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm < M)
+      store4(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c,
+             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]), epi);
+  }
+}
+
 template <bool VEC_B>
 cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int64_t lda, const float* B, int64_t ldb, float* C,
@@ -410,6 +555,24 @@ int64_t f32_slots() {
 
 F32Plan f32_plan(int M, int N, int K, int64_t slots) {
   F32Plan p;
+  if (f32_small_problem(M, N, K)) {
+    // every 64 x 64 tile split into ranges of k-slices, about two blocks
+    // per SM in all
+    p.small = true;
+    p.tiles_m = (M + SB - 1) / SB;
+    p.tiles_n = (N + SB - 1) / SB;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int nk = (K + BK - 1) / BK;
+    int split = slots > 0 ? static_cast<int>(slots / tiles) : 1;
+    if (split > 16) split = 16;
+    if (split > nk) split = nk;
+    p.split = split < 1 ? 1 : split;
+    p.tail = tiles;
+    p.workspace_bytes =
+        p.split > 1 ? static_cast<int64_t>(tiles) * p.split * SB * SB * 4 : 0;
+    p.counter_bytes = p.split > 1 ? static_cast<int64_t>(tiles) * 4 : 0;
+    return p;
+  }
   p.tiles_m = (M + BM - 1) / BM;
   p.tiles_n = (N + BN - 1) / BN;
   const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
@@ -457,6 +620,17 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
   if (f32_slots() <= 0) return cudaErrorInvalidDeviceFunction;
   const int vc = vec_c ? 1 : 0;
   cudaError_t e = cudaSuccess;
+  if (p.small) {
+    const int blocks = p.tiles_m * p.tiles_n * p.split;
+    if (vec_b)
+      gemm_f32_small_kernel<true><<<blocks, THREADS, 0, stream>>>(
+          M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
+    else
+      gemm_f32_small_kernel<false><<<blocks, THREADS, 0, stream>>>(
+          M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
+    note_launches(1);
+    return cudaGetLastError();
+  }
   if (p.full > 0) {
     e = vec_b ? launch_part<true>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
                                   p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,

@@ -112,6 +112,11 @@ def test_plan_paths():
     assert _path("bf16", 16, 100, 64)[1].split_k == 1      # one k slice only
     path, p = _path("f32", 4096, 4096, 4096)
     assert path == "f32_simt" and p.tiles == 32 * 32
+    # small problems: 64 x 64 tiles (split along K on the device)
+    path, p = _path("f32", 256, 256, 256)
+    assert path == "f32_simt" and (p.tile_m, p.tile_n, p.tiles) == (64, 64, 16)
+    assert _path("f32", 512, 512, 512)[1].tile_m == 128     # 2^27 multiply-adds
+    assert _path("f32", 2048, 300, 100)[1].tile_m == 128    # 48 tiles of 128 x 128
     # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
     path, p = _path("bf16", 127, 1000, 3001)
     assert path == "bf16_skinny" and p.pack_a == 1 and p.pack_b == 0
