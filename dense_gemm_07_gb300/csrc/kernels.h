@@ -31,12 +31,12 @@ struct F32Plan {
   int64_t workspace_bytes = 0, counter_bytes = 0;
   bool small = false;  // 64 x 64 tiles (f32_small_problem), all split `split` ways
 };
-// Small problems (at most 16 tiles of 128 x 128 and 2^26 multiply-adds) run
+// Small problems (at most 16 tiles of 128 x 128 and 2^29 multiply-adds) run
 // as 64 x 64 tiles split along K, so that they spread over the SMs.
 constexpr int kF32SmallTile = 64;
 inline bool f32_small_problem(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ((M + kF32TileM - 1) / kF32TileM) * ((N + kF32TileN - 1) / kF32TileN);
-  return tiles <= 16 && M * N * K <= (int64_t(1) << 26);
+  return tiles <= 16 && M * N * K <= (int64_t(1) << 29);
 }
 // Resident blocks of the FP32 kernel on the current device (0: cannot run).
 int64_t f32_slots();

@@ -115,7 +115,8 @@ def test_plan_paths():
     # small problems: 64 x 64 tiles (split along K on the device)
     path, p = _path("f32", 256, 256, 256)
     assert path == "f32_simt" and (p.tile_m, p.tile_n, p.tiles) == (64, 64, 16)
-    assert _path("f32", 512, 512, 512)[1].tile_m == 128     # 2^27 multiply-adds
+    assert _path("f32", 512, 512, 2048)[1].tile_m == 64     # 2^29 multiply-adds
+    assert _path("f32", 512, 512, 4096)[1].tile_m == 128    # 2^30
     assert _path("f32", 2048, 300, 100)[1].tile_m == 128    # 48 tiles of 128 x 128
     # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
     path, p = _path("bf16", 127, 1000, 3001)
