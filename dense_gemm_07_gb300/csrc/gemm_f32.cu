@@ -584,8 +584,10 @@ F32Plan f32_plan(int M, int N, int K, int64_t slots) {
     // Split the tiles of the last, partial wave along K so that its blocks
     // fill the resident slots: choose the split with the lowest estimated
     // time in units of one tile's main loop, rounds x (1/split + a per-round
-    // overhead for the pipeline fill) plus the last block's reading of the
-    // split partial tiles (about 1/15 of a k-slice each), at most 16 ranges.
+    // overhead for the pipeline fill, 1/50 of a tile) plus the last block's
+    // reading of the split partial tiles (about 1/15 of a k-slice each), at
+    // most 16 ranges.  A last wave with fewer tiles than resident slots is
+    // split too, since an SM holding one block runs it slower than two.
     // Ranges keep at least 4 k-slices, unless the split tiles then still
     // fit in one round of resident blocks (a short K with few tiles, e.g.
     // 256^3: 4 tiles of 8 slices, spreads over more SMs).
@@ -596,7 +598,7 @@ F32Plan f32_plan(int M, int N, int K, int64_t slots) {
     for (int s = 1; s <= max_split; ++s) {
       const int64_t rounds = (static_cast<int64_t>(p.tail) * s + slots - 1) / slots;
       if (s > long_split && rounds > 1) break;
-      const double cost = static_cast<double>(rounds) * (1.0 / s + 0.04) +
+      const double cost = static_cast<double>(rounds) * (1.0 / s + 0.02) +
                           (s > 1 ? reduce_per_range * s : 0.0);
       if (cost < best - 1e-9) {
         best = cost;
