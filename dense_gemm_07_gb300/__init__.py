@@ -113,7 +113,7 @@ def _gemm_ex(fn_name, dtype, A, B, out, alpha, beta, bias, activation, stream):
     if beta != 0.0 and out is None:
         raise ValueError("beta != 0 reads C: pass its prior contents as `out`")
     M, N, K, out = _operands(A, B, dtype, out, "cuda")
-    acts = {"none": abi.ACT_NONE, "relu": abi.ACT_RELU}
+    acts = {"none": abi.ACT_NONE, "relu": abi.ACT_RELU, "gelu": abi.ACT_GELU}
     if activation not in acts:
         raise ValueError(f"activation must be one of {sorted(acts)}")
     if bias is not None:

@@ -46,6 +46,7 @@ class GemmEpilogue(ctypes.Structure):
 
 ACT_NONE = 0
 ACT_RELU = 1
+ACT_GELU = 2
 
 
 # (name, restype, argtypes)

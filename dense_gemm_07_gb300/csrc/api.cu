@@ -227,7 +227,8 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
 gemm_status_t to_epi(const gemm_epilogue_t* e, EpiParams* out) {
   *out = epi_identity();
   if (e == nullptr) return GEMM_OK;
-  if (e->activation != GEMM_ACT_NONE && e->activation != GEMM_ACT_RELU)
+  if (e->activation != GEMM_ACT_NONE && e->activation != GEMM_ACT_RELU &&
+      e->activation != GEMM_ACT_GELU)
     return GEMM_ERR_INVALID_ARG;
   out->alpha = e->alpha;
   out->beta = e->beta;

@@ -15,7 +15,7 @@ struct EpiParams {
   float alpha;
   float beta;          // 0: the prior contents of C are not read
   const float* bias;   // N floats (device) or nullptr
-  int act;             // 0 identity, 1 ReLU
+  int act;             // 0 identity, 1 ReLU, 2 GELU
 };
 
 __host__ __device__ inline EpiParams epi_identity() {
@@ -28,6 +28,8 @@ __device__ __forceinline__ float epi_apply(const EpiParams& e, float acc,
   if (e.beta != 0.0f) v = fmaf(e.beta, c_old, v);
   if (e.bias != nullptr) v += bias;
   if (e.act == 1) v = fmaxf(v, 0.0f);
+  // GELU: x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), with CUDA's erff
+  if (e.act == 2) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
   return v;
 }
 

@@ -124,7 +124,9 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc(int64_t M, int64_t N, int64_t K,
  */
 typedef enum gemm_activation {
     GEMM_ACT_NONE = 0,
-    GEMM_ACT_RELU = 1      /* max(x, 0) */
+    GEMM_ACT_RELU = 1,     /* max(x, 0) */
+    GEMM_ACT_GELU = 2      /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), FP32 erff;
+                              the element-wise GELU of "GEMM Optimization" */
 } gemm_activation_t;
 
 typedef struct gemm_epilogue {

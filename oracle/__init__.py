@@ -136,7 +136,7 @@ def gemm_epilogue(AB: np.ndarray, alpha: float = 1.0, beta: float = 0.0,
     """act(alpha * AB + beta * C0 + bias) in double; AB from gemm_f32/gemm_bf16.
 
     C0 (FP32, M x N) None means C is not read; bias (FP32, N) None means no
-    bias; act 0 = identity, 1 = ReLU.
+    bias; act 0 = identity, 1 = ReLU, 2 = GELU (x * Phi(x), erf form).
     """
     lib = _load()
     AB = np.ascontiguousarray(AB, dtype=np.float64)

@@ -119,14 +119,17 @@ int oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
  *   out[i][j] = act(alpha * AB[i][j] + beta * C0[i][j] + bias[j])
  * in double.  AB is the oracle's product (ld_ab), C0 the prior contents of
  * C as FP32 (NULL: treated as zero, i.e. not read), bias N floats or NULL,
- * act 0 = identity, 1 = max(x, 0).  Returns 0, or -1 on a bad argument.
+ * act 0 = identity, 1 = max(x, 0), 2 = GELU, x * Phi(x) with Phi the
+ * standard normal distribution function, 0.5 x (1 + erf(x / sqrt(2)))
+ * (the activation named among a transformer's element-wise operations in
+ * "GEMM Optimization").  Returns 0, or -1 on a bad argument.
  */
 int oracle_gemm_epilogue(int64_t M, int64_t N, const double *AB, int64_t ld_ab,
                          double alpha, double beta, const float *C0,
                          int64_t ld_c0, const float *bias, int act, double *out,
                          int64_t ld_out)
 {
-    if (M < 0 || N < 0 || act < 0 || act > 1) return -1;
+    if (M < 0 || N < 0 || act < 0 || act > 2) return -1;
     if (M == 0 || N == 0) return 0;
     if (AB == NULL || out == NULL || ld_ab < N || ld_out < N) return -1;
     if (C0 != NULL && ld_c0 < N) return -1;
@@ -136,6 +139,7 @@ int oracle_gemm_epilogue(int64_t M, int64_t N, const double *AB, int64_t ld_ab,
             if (C0 != NULL) v += beta * (double)C0[i * ld_c0 + j];
             if (bias != NULL) v += (double)bias[j];
             if (act == 1 && v < 0.0) v = 0.0;
+            if (act == 2) v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
             out[i * ld_out + j] = v;
         }
     }

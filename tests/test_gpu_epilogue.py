@@ -114,3 +114,40 @@ def test_unknown_activation_rejected():
     st = torch.cuda.current_stream().cuda_stream
     assert _abi.gemm_f32_ex(4, 4, 4, a.data_ptr(), 4, a.data_ptr(), 4, c.data_ptr(), 4,
                             epi, st) == _abi.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind,M,N,K,schedule", [
+    ("f32", 700, 900, 1000, None), ("f32", 200, 190, 300, None),
+    ("bf16", 700, 900, 1000, None), ("bf16", 300, 258, 200, None),
+    ("bf16", 48, 1000, 777, None), ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K)])
+def test_epilogue_gelu(kind, M, N, K, schedule):
+    # GELU after alpha, beta and the bias on every path.  Bound: GELU's slope
+    # is at most 1.13, so the pre-activation bound grows by that factor; the
+    # FP32 erff and the final products add a few units in the last place of
+    # |v|.
+    dtype = torch.float32 if kind == "f32" else torch.bfloat16
+    dist = inputs.NORMAL if kind == "bf16" else inputs.UNIFORM
+    a, b = inputs.make_pair(M, N, K, 52, dist, dtype=dtype)
+    g = torch.Generator().manual_seed(1052)
+    c0 = torch.randn((M, N), generator=g).float()
+    bias = torch.randn((N,), generator=g).float()
+    out = c0.to(DEV).clone()
+    fn = g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex
+    prev = _abi.gemm_set_bf16_schedule(schedule) if schedule is not None else None
+    try:
+        fn(a.to(DEV), b.to(DEV), out=out, alpha=0.5, beta=0.75, bias=bias.to(DEV),
+           activation="gelu")
+        torch.cuda.synchronize()
+    finally:
+        if prev is not None:
+            _abi.gemm_set_bf16_schedule(prev)
+    assert g7.gemm_get_device_status() == 0
+    ab, s = oracle_ref(kind, a, b)
+    pre = oracle.gemm_epilogue(ab, alpha=0.5, beta=0.75, C0=c0.numpy(), bias=bias.numpy())
+    want = oracle.gemm_epilogue(ab, alpha=0.5, beta=0.75, C0=c0.numpy(), bias=bias.numpy(),
+                                act=2)
+    got = out.cpu().numpy().astype(np.float64)
+    scale = 0.5 * s + 0.75 * np.abs(c0.numpy()) + np.abs(bias.numpy())[None, :]
+    lim = 1.13 * (RTOL[kind] * scale + ATOL[kind]) + 1e-6 * np.abs(pre) + 1e-6
+    err = np.abs(got - want)
+    assert np.all(err <= lim), float(np.max(err - lim))

@@ -341,8 +341,30 @@ def test_epilogue_beta_without_c_and_zero_product(oracle_mod):
     assert np.array_equal(oracle_mod.gemm_epilogue(AB, bias=bias), np.tile(bias, (3, 1)))
 
 
+def test_epilogue_gelu_special_values(oracle_mod):
+    # GELU(x) = x * Phi(x): values of the standard normal distribution
+    # function from its tables, Phi(1) = 0.8413447460685429,
+    # Phi(2) = 0.9772498680518208, Phi(-1) = 0.15865525393145707
+    x = np.array([[0.0, 1.0, 2.0, -1.0, 10.0, -10.0]])
+    g = oracle_mod.gemm_epilogue(x, act=2)[0]
+    want = [0.0, 0.8413447460685429, 2 * 0.9772498680518208, -0.15865525393145707, 10.0, 0.0]
+    assert np.allclose(g, want, rtol=1e-15, atol=1e-20)
+    # Phi(x) + Phi(-x) = 1, so GELU(x) - GELU(-x) = x
+    t = np.linspace(-6, 6, 97)[None, :]
+    d = oracle_mod.gemm_epilogue(t, act=2) - oracle_mod.gemm_epilogue(-t, act=2)
+    assert np.allclose(d, t, rtol=1e-14, atol=1e-15)
+    # applied after alpha, beta and the bias, like ReLU
+    AB = np.array([[1.0, -2.0]])
+    C0 = np.array([[3.0, 1.0]], dtype=np.float32)
+    bias = np.array([-1.0, 4.0], dtype=np.float32)
+    pre = oracle_mod.gemm_epilogue(AB, alpha=2.0, beta=-1.0, C0=C0, bias=bias)
+    assert np.array_equal(pre, [[-2.0, -1.0]])
+    got = oracle_mod.gemm_epilogue(AB, alpha=2.0, beta=-1.0, C0=C0, bias=bias, act=2)
+    assert np.allclose(got, [[-2 * (1 - 0.9772498680518208), -0.15865525393145707]], rtol=1e-14)
+
+
 def test_epilogue_rejects_bad_arguments(oracle_mod):
     with pytest.raises(ValueError):
-        oracle_mod.gemm_epilogue(np.zeros((2, 3)), act=2)
+        oracle_mod.gemm_epilogue(np.zeros((2, 3)), act=3)
     with pytest.raises(ValueError):
         oracle_mod.gemm_epilogue(np.zeros((2, 3)), bias=np.zeros(2, np.float32))
