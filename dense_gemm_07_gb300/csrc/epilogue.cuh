@@ -22,6 +22,11 @@ __host__ __device__ inline EpiParams epi_identity() {
   return EpiParams{1.0f, 0.0f, nullptr, 0};
 }
 
+// kGelu = false compiles the GELU case out: the main kernels are built
+// twice, and the copy without it is used for every other activation (the
+// erff code, even unused, changes the register allocation of the main loops
+// around it).
+template <bool kGelu = true>
 __device__ __forceinline__ float epi_apply(const EpiParams& e, float acc,
                                            float c_old, float bias) {
   float v = e.alpha * acc;
@@ -29,8 +34,10 @@ __device__ __forceinline__ float epi_apply(const EpiParams& e, float acc,
   if (e.bias != nullptr) v += bias;
   if (e.act == 1) v = fmaxf(v, 0.0f);
   // GELU: x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), with CUDA's erff
-  if (e.act == 2) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  if (kGelu && e.act == 2) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
   return v;
 }
+
+constexpr int kActGelu = 2;
 
 }  // namespace g07

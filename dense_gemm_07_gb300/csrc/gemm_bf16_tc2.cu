@@ -354,7 +354,7 @@ __device__ __forceinline__ bool combine_chunk(uint32_t (&r)[32],
 // when a segment leaves its partial sums (identity epilogue, M = N = the
 // workspace's extent).  With `reduce`, the boxes are added to tmOut's
 // elements instead of stored.  W: the unit's width.  False: a wait ran out.
-template <int W>
+template <int W, bool GELU>
 __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
                                                const CUtensorMap* tmOut,
                                                uint8_t* ebuf, int row0, int n0,
@@ -392,7 +392,7 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const bool in = gn + j + e < N;
-          r[j + e] = __float_as_uint(epi_apply(
+          r[j + e] = __float_as_uint(epi_apply<GELU>(
               epi, __uint_as_float(r[j + e]), o[e],
               (epi.bias != nullptr && in) ? epi.bias[gn + j + e] : 0.0f));
         }
@@ -426,7 +426,7 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
 // of C and of the bias are coalesced the same way).  With cb set, each chunk
 // is first combined with the other segments' partial sums, loaded through
 // the same box.  False: a wait ran out.
-template <int W>
+template <int W, bool GELU>
 __device__ __forceinline__ bool store_unit_rows(uint32_t taddr, float* C,
                                                 int64_t ldc, int row0, int n0,
                                                 int M, int N,
@@ -467,7 +467,7 @@ __device__ __forceinline__ bool store_unit_rows(uint32_t taddr, float* C,
         const float v = *reinterpret_cast<const float*>(
             buf + rr * 128 + (((group ^ static_cast<uint32_t>(rr & 7)) << 4) | in_group));
         float* dst = cp + static_cast<int64_t>(rr) * ldc;
-        *dst = plain ? v : epi_apply(epi, v, epi.beta != 0.0f ? *dst : 0.0f, bias);
+        *dst = plain ? v : epi_apply<GELU>(epi, v, epi.beta != 0.0f ? *dst : 0.0f, bias);
       }
     }
     // every lane has read the box before it is written again, by this
@@ -478,6 +478,9 @@ __device__ __forceinline__ bool store_unit_rows(uint32_t taddr, float* C,
   return true;
 }
 
+// GELU: whether the GELU activation is compiled in (epi_apply); the copy
+// without it serves every other epilogue.
+template <bool GELU>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -647,9 +650,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           good = false;
         } else if (ticket + 1 < st.nseg) {
           ready_slot = sk_slot(sched, pair, w.tile);
-          good = direct ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
+          good = direct ? store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
                                              chunk, C, ldc, epi, nullptr)
-                        : store_unit_tma<BN>(taddr, &tmW, ebuf,
+                        : store_unit_tma<BN, GELU>(taddr, &tmW, ebuf,
                                              sk_row(pair, ready_slot, rank, q), 0,
                                              0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
                                              epi_identity(), nullptr);
@@ -722,15 +725,15 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         if (w.width != BN) {
           // a column-split unit of the last wave (never a stream-K segment)
           if (tma_c)
-            store_unit_tma<BN / 2>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
+            store_unit_tma<BN / 2, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
                                    chunk, C, ldc, epi, nullptr);
           else
-            store_unit_rows<BN / 2>(taddr, C, ldc, row0, n0, M, N, epi, nullptr,
+            store_unit_rows<BN / 2, GELU>(taddr, C, ldc, row0, n0, M, N, epi, nullptr,
                                     ebuf, lane, chunk);
         } else {
-          good = tma_c ? store_unit_tma<BN>(taddr, &tmC, ebuf, row0, n0, M, N,
+          good = tma_c ? store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N,
                                             lane, chunk, C, ldc, epi, cbp, reduce_c)
-                       : store_unit_rows<BN>(taddr, C, ldc, row0, n0, M, N,
+                       : store_unit_rows<BN, GELU>(taddr, C, ldc, row0, n0, M, N,
                                              epi, cbp, ebuf, lane, chunk);
         }
       }
@@ -785,7 +788,10 @@ int pair_max_active(cudaStream_t stream) {
   LaunchInfo& li = g_info[dev];
   if (!li.ready) {
     const size_t smem = pair_smem_bytes();
-    if (cudaFuncSetAttribute(gemm_bf16_pair_kernel,
+    if (cudaFuncSetAttribute(gemm_bf16_pair_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_bf16_pair_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return 0;
@@ -802,7 +808,7 @@ int pair_max_active(cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_pair_kernel, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_pair_kernel<false>, &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -839,10 +845,14 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
   cfg.numAttrs = 1;
   CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
-  const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, gemm_bf16_pair_kernel, tmA, tmB, tmC ? *tmC : unused,
-      tmW ? *tmW : unused, C, ldc, M, N, sched, sk_sync, sk_tag, tmC ? 1 : 0,
-      status, epi);
+  const cudaError_t e =
+      epi.act == kActGelu
+          ? cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel<true>, tmA, tmB,
+                               tmC ? *tmC : unused, tmW ? *tmW : unused, C, ldc, M, N,
+                               sched, sk_sync, sk_tag, tmC ? 1 : 0, status, epi)
+          : cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel<false>, tmA, tmB,
+                               tmC ? *tmC : unused, tmW ? *tmW : unused, C, ldc, M, N,
+                               sched, sk_sync, sk_tag, tmC ? 1 : 0, status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -168,6 +168,8 @@ struct SliceLoader {
 
 // Guarded store of one 4-wide group of row `crow` at column gn, through the
 // epilogue (prior C and bias read only when the epilogue needs them).
+// GELU: whether the GELU activation is compiled in (epi_apply).
+template <bool GELU>
 __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
                                        float4 v, const EpiParams& epi) {
   float e[4] = {v.x, v.y, v.z, v.w};
@@ -177,14 +179,14 @@ __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
     const float o[4] = {old.x, old.y, old.z, old.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      e[j] = epi_apply(epi, e[j], o[j], epi.bias ? epi.bias[gn + j] : 0.0f);
+      e[j] = epi_apply<GELU>(epi, e[j], o[j], epi.bias ? epi.bias[gn + j] : 0.0f);
     *reinterpret_cast<float4*>(crow + gn) = make_float4(e[0], e[1], e[2], e[3]);
   } else {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       if (gn + j < N)
-        crow[gn + j] = epi_apply(epi, e[j], epi.beta != 0.0f ? crow[gn + j] : 0.0f,
-                                 epi.bias ? epi.bias[gn + j] : 0.0f);
+        crow[gn + j] = epi_apply<GELU>(epi, e[j], epi.beta != 0.0f ? crow[gn + j] : 0.0f,
+                                       epi.bias ? epi.bias[gn + j] : 0.0f);
   }
 }
 
@@ -193,6 +195,7 @@ __device__ __forceinline__ void store4(float* crow, int gn, int N, int vec_c,
 // rows at a time: per range, the 8 float4 loads of those rows are issued
 // together before they are added, so each range costs one L2 round trip
 // rather than one per row.
+template <bool GELU>
 __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
                                            float* C, int64_t ldc, int M, int N,
                                            int m0, int n0, int row_a, int col_b,
@@ -232,7 +235,8 @@ __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
       if (gm >= M) continue;
       float* crow = C + static_cast<int64_t>(gm) * ldc;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) store4(crow, n0 + col_b + 32 * h, N, vec_c, sum[i][h], epi);
+      for (int h = 0; h < 2; ++h)
+        store4<GELU>(crow, n0 + col_b + 32 * h, N, vec_c, sum[i][h], epi);
     }
   }
 }
@@ -244,7 +248,7 @@ __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
 // (split x 128 x 128 floats per tile); the last of its blocks to finish (per
 // `counters`, zero at launch) adds the partials in range order 0, 1, ... and
 // writes C, so the result does not depend on which block finishes last.
-template <bool VEC_B>
+template <bool VEC_B, bool GELU>
 __global__ void __launch_bounds__(THREADS, 2)
 gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
                          int64_t lda, const float* __restrict__ B, int64_t ldb,
@@ -340,7 +344,7 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     __syncthreads();
     if (last_block) {
       __threadfence();
-      reduce_ranges(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c, epi);
+      reduce_ranges<GELU>(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c, epi);
       if (tid == 0) counters[local_tile] = 0;  // leave the counter as found
     }
     return;
@@ -354,7 +358,7 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     float* crow = C + static_cast<int64_t>(gm) * ldc;
 #pragma unroll
     for (int h = 0; h < JP / 2; ++h)
-      store4(crow, n0 + col_b + 32 * h, N, vec_c,
+      store4<GELU>(crow, n0 + col_b + 32 * h, N, vec_c,
              make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
                          acc[i][2 * h + 1].y),
              epi);
@@ -492,7 +496,7 @@ gemm_f32_small_kernel(int M, int N, int K, const float* __restrict__ A, int64_t 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int gm = m0 + ty * 4 + i;
-      if (gm < M) store4(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c, sum[i], epi);
+      if (gm < M) store4<true>(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c, sum[i], epi);
     }
     if (tid == 0) counters[tile] = 0;  // leave the counter as found
     return;
@@ -501,11 +505,12 @@ gemm_f32_small_kernel(int M, int N, int K, const float* __restrict__ A, int64_t 
   for (int i = 0; i < 4; ++i) {
     const int gm = m0 + ty * 4 + i;
     if (gm < M)
-      store4(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c,
-             make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]), epi);
+      store4<true>(C + static_cast<int64_t>(gm) * ldc, col, N, vec_c,
+                   make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]), epi);
   }
 }
 
+// The kernel copy with GELU compiled in only for that activation.
 template <bool VEC_B>
 cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int64_t lda, const float* B, int64_t ldb, float* C,
@@ -513,16 +518,21 @@ cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int split, int vec_c, float* ws, unsigned int* counters,
                         const EpiParams& epi, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<BN>);
-  gemm_f32_regblock_kernel<VEC_B><<<blocks, THREADS, smem, stream>>>(
-      M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
-      counters, epi);
+  if (epi.act == kActGelu)
+    gemm_f32_regblock_kernel<VEC_B, true><<<blocks, THREADS, smem, stream>>>(
+        M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
+        counters, epi);
+  else
+    gemm_f32_regblock_kernel<VEC_B, false><<<blocks, THREADS, smem, stream>>>(
+        M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
+        counters, epi);
   note_launches(1);
   return cudaGetLastError();
 }
 
-template <bool VEC_B>
+template <bool VEC_B, bool GELU>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_f32_regblock_kernel<VEC_B>,
+  return cudaFuncSetAttribute(gemm_f32_regblock_kernel<VEC_B, GELU>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(STAGES * sizeof(F32Stage<BN>)));
 }
@@ -537,12 +547,15 @@ int64_t f32_slots() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!g_attr_set[dev]) {
-    if (set_smem_attr<true>() != cudaSuccess || set_smem_attr<false>() != cudaSuccess)
+    if (set_smem_attr<true, false>() != cudaSuccess ||
+        set_smem_attr<false, false>() != cudaSuccess ||
+        set_smem_attr<true, true>() != cudaSuccess ||
+        set_smem_attr<false, true>() != cudaSuccess)
       return 0;
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, gemm_f32_regblock_kernel<true>, THREADS,
+            &per_sm, gemm_f32_regblock_kernel<true, false>, THREADS,
             STAGES * sizeof(F32Stage<BN>)) != cudaSuccess) {
       cudaGetLastError();
       return 0;
