@@ -64,7 +64,9 @@ __device__ __forceinline__ void raise_abort(volatile int* abort,
   atomicOr(status, 1u);
 }
 
-template <int NM>
+// GELU: whether the GELU activation is compiled in (epi_apply); the copy
+// without it serves every other epilogue.
+template <int NM, bool GELU>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -237,7 +239,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
           if (q < cs) sum += v[i][q];
         if (m < rows && n < N) {
           float* p = C + static_cast<int64_t>(m) * ldc + n;
-          *p = epi_apply(epi, sum, epi.beta != 0.0f ? *p : 0.0f,
+          *p = epi_apply<GELU>(epi, sum, epi.beta != 0.0f ? *p : 0.0f,
                          epi.bias ? epi.bias[n] : 0.0f);
         }
       }
@@ -264,14 +266,16 @@ cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
   using S = SkinnyShape<NM>;
   const size_t smem = 1024 + static_cast<size_t>(S::STAGES) * S::STAGE_BYTES +
                       sizeof(SkinnyControl<S::STAGES>);
+  auto kernel = epi.act == kActGelu ? gemm_bf16_skinny_kernel<NM, true>
+                                     : gemm_bf16_skinny_kernel<NM, false>;
   if (!g_attr_done[dev][slot]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_skinny_kernel<NM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_bf16_skinny_kernel<NM>,
-                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+    for (auto k : {gemm_bf16_skinny_kernel<NM, false>, gemm_bf16_skinny_kernel<NM, true>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     g_attr_done[dev][slot] = 1;
   }
   const int tiles = (N + TILE_N - 1) / TILE_N;
@@ -287,8 +291,8 @@ cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel<NM>, tmA,
-                                           tmB, C, ldc, M, N, K, cs, status, epi);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, C, ldc, M, N, K, cs,
+                                           status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
