@@ -67,15 +67,18 @@ def load_peaks():
                 "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
-def kernel_hash(path):
-    """Hash of a kernel source's code: comments and blank space removed, so
-    that editing a comment does not invalidate a profile of the code."""
-    with open(path) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", " ", text)
-    text = " ".join(text.split())
-    return hashlib.sha256(text.encode()).hexdigest()[:16]
+def kernel_hash(*paths):
+    """Hash of the code of a kernel's sources: comments and blank space
+    removed, so that editing a comment does not invalidate a profile of the
+    code."""
+    parts = []
+    for path in paths:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        parts.append(" ".join(text.split()))
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel_file):
@@ -88,8 +91,12 @@ def ncu_traffic(kernel_file):
     except (OSError, ValueError):
         return None
     entry = d.get(os.path.basename(kernel_file))
-    src = os.path.join(ROOT, "dense_gemm_07_gb300", "csrc", os.path.basename(kernel_file))
-    if not entry or entry.get("source_sha256_16") != kernel_hash(src):
+    if not entry:
+        return None
+    # the kernel file, and the headers that decide its work where listed
+    srcs = [os.path.join(ROOT, "dense_gemm_07_gb300", "csrc", f)
+            for f in entry.get("sources", [os.path.basename(kernel_file)])]
+    if entry.get("source_sha256_16") != kernel_hash(*srcs):
         return None
     return entry.get("dram_bytes_per_launch_full_size")
 

@@ -85,6 +85,11 @@ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// C can take the TMA-store epilogue (FP32 rows of whole 16-byte groups).
+bool tma_store_ok(const void* C, int64_t N, int64_t ldc) {
+  return aligned16(C) && ldc % 4 == 0 && N % 4 == 0;
+}
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
@@ -213,7 +218,8 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
   if (pair) {
-    const PairSchedule ps = pair_schedule(M, N, K, 76, g_schedule.load());
+    const PairSchedule ps =
+        pair_schedule(M, N, K, 76, g_schedule.load(), tma_store_ok(C, N, ldc));
     p->dp_tiles = ps.dp_tiles;
     p->sk_tiles = ps.sk_tiles;
     p->sk_pairs = ps.sk_pairs;
@@ -380,10 +386,6 @@ gemm_status_t make_operand_maps(CUtensorMap* tmA, CUtensorMap* tmB,
 // bytes apart, and N a multiple of 4: the copy engine clips the inner
 // dimension of a store in 16-byte units, so a row that ends mid-unit would
 // be written past column N-1.
-bool tma_store_ok(const float* C, int64_t N, int64_t ldc) {
-  return aligned16(C) && ldc % 4 == 0 && N % 4 == 0;
-}
-
 // FP32 map of C for the TMA-store epilogue: 32 x 32 boxes, 128-byte swizzle.
 gemm_status_t make_map_c(CUtensorMap* map, const float* C, int64_t M,
                          int64_t N, int64_t ldc) {
@@ -579,7 +581,10 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   const int max_pairs =
       !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   PairSchedule ps;
-  if (max_pairs > 0) ps = pair_schedule(M, N, K, max_pairs, g_schedule.load());
+  if (max_pairs > 0)
+    ps = pair_schedule(M, N, K, max_pairs, g_schedule.load(),
+                       tma_store_ok(C, N, ldc) && epi.beta == 0.0f && epi.bias == nullptr &&
+                           epi.act == 0);
   const int64_t pack_ws = pack_bytes(M, N, K, plan.pack_a, plan.pack_b);
   void* ws = nullptr;
   bool fresh = false, owned = false;
@@ -904,7 +909,8 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   if (max_pairs > 0) {
     // Stream-K only when its scratch fits after the packed operands.
-    PairSchedule ps = pair_schedule(M, N, K, max_pairs, g_schedule.load());
+    PairSchedule ps =
+        pair_schedule(M, N, K, max_pairs, g_schedule.load(), tma_store_ok(C, N, ldc));
     if (pack_ws + sk_bytes(ps) > kNoallocScratchBytes)
       ps = pair_schedule(M, N, K, max_pairs, kScheduleNoSplitK);
     float* sk_ws = nullptr;

@@ -20,7 +20,11 @@
 // their partial sums to a workspace and raise a ready flag; the last one
 // adds all segments in k order (its own from tensor memory) and applies the
 // output step.  No warp waits for work that has not started: a flag is only
-// awaited after its writer has taken its ticket.  Partial sums move by the
+// awaited after its writer has taken its ticket.  A tile of two segments
+// whose output step is alpha * A.B into a C open to TMA is finished in C
+// itself instead: the pair holding its first segment clears the tile's rows
+// of C when the kernel starts, and each segment adds its sums there with
+// TMA reductions as soon as it is done.  Partial sums move by the
 // copy engine; when the finishing unit is the pair's last, its operand ring
 // is idle and each warp loads its 32 x 256 partial sums there in one batch.
 //
@@ -605,6 +609,47 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t part_uses = 0;
     WorkIter wi;
     wi.init(sched, pair);
+    // Tiles cut into two segments, with C open to TMA and no term besides
+    // alpha * A.B, are finished directly in C: each segment adds its sums
+    // there with TMA reductions, so those rows of C must read zero first.
+    // The pair holding a tile's first segment clears its rows of the tile
+    // before its first unit and raises its ready flag; the other segment's
+    // warp waits for that flag before it adds.  (0 + a) + b == (0 + b) + a,
+    // so the bits do not depend on which segment finishes first, and neither
+    // waits for the other's MMAs.
+    const bool direct_ok = tma_c && epi.beta == 0.0f && epi.bias == nullptr && epi.act == 0;
+    if (direct_ok && pair < sched.sk_pairs) {
+      const int64_t I = sk_total(sched);
+      const int64_t b0 = sk_begin(pair, sched.sk_pairs, I);
+      const int64_t b1 = sk_begin(pair + 1, sched.sk_pairs, I);
+      // A first segment of a two-segment tile ends this pair's range.
+      const int tile = sched.dp_tiles + static_cast<int>((b1 > b0 ? b1 - 1 : b0) / sched.num_kb);
+      const SkTile st = b1 > b0 ? sk_tile(sched, tile) : SkTile{-1, 0};
+      if (st.q_first == pair && st.nseg == 2) {
+        const TileCoord tc = tile_order(tile, sched.tiles_m, sched.tiles_n, GROUP);
+        const int row0 = tc.m * PAIR_M + static_cast<int>(rank) * CTA_M + q * 32;
+        const int n0 = tc.n * BN;
+        uint4* zrow = reinterpret_cast<uint4*>(ebuf + lane * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zrow[j] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (row0 < M)
+            for (int c = 0; c < BN / 32; ++c)
+              if (n0 + c * 32 < N) tma_store_2d(&tmC, ebuf, n0 + c * 32, row0);
+          bulk_commit();
+          // The zeros are in C (and the box is free again) before the flag
+          // says so.
+          bulk_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+          st_release_gpu_u64(sk_ready(sk_sync, sched, pair, sk_slot(sched, pair, tile), rank, q),
+                             sk_tag);
+        }
+        __syncwarp();
+      }
+    }
     WorkUnit w;
     for (int t = 0; wi.next(sched, num_pairs, w); ++t) {
       const int acc = t % NUM_ACC;
@@ -632,16 +677,28 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const SkCombine* cbp = nullptr;
       bool reduce_c = false;  // add this segment into C (the other one is there)
       bool good = true;
-      if (w.k0 != 0 || w.k1 != sched.num_kb) {
+      const bool segment = w.k0 != 0 || w.k1 != sched.num_kb;
+      const SkTile st = segment ? sk_tile(sched, w.tile) : SkTile{pair, 1};
+      if (segment && direct_ok && st.nseg == 2) {
+        // A segment finished directly in C (above): add it once the tile's
+        // rows of C have been cleared.
+        int got = 1;
+        if (lane == 0 && pair != st.q_first) {
+          unsigned long long* f =
+              sk_ready(sk_sync, sched, st.q_first, sk_slot(sched, st.q_first, w.tile), rank, q);
+          got = sk_wait_ready(f, sk_tag, abort, tmo) ? 1 : 0;
+          // the flag was read by this thread; C will be updated by the
+          // copy engine
+          fence_proxy_async_global();
+          // the only reader of this flag puts it back to zero for a replay
+          // of this launch with the same tag
+          if (got) *f = 0ull;
+        }
+        good = __shfl_sync(0xffffffffu, got, 0) != 0;
+        reduce_c = true;
+      } else if (segment) {
         // A stream-K segment: take a ticket; the last of the tile's
         // segments finishes it, the others leave their partial sums.
-        const SkTile st = sk_tile(sched, w.tile);
-        // Two segments, C open to TMA and no term besides alpha * A.B: the
-        // first to finish stores its share straight into C and the second
-        // adds its own with a TMA reduction.  a + b == b + a, so the bits do
-        // not depend on which finishes first.
-        const bool direct = tma_c && st.nseg == 2 && epi.beta == 0.0f &&
-                            epi.bias == nullptr && epi.act == 0;
         int ticket = 0;
         if (lane == 0)
           ticket = sk_take_ticket(sk_ticket(sk_sync, sched, w.tile, rank, q), sk_tag);
@@ -650,12 +707,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           good = false;
         } else if (ticket + 1 < st.nseg) {
           ready_slot = sk_slot(sched, pair, w.tile);
-          good = direct ? store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
-                                             chunk, C, ldc, epi, nullptr)
-                        : store_unit_tma<BN, GELU>(taddr, &tmW, ebuf,
-                                             sk_row(pair, ready_slot, rank, q), 0,
-                                             0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
-                                             epi_identity(), nullptr);
+          good = store_unit_tma<BN, GELU>(taddr, &tmW, ebuf, sk_row(pair, ready_slot, rank, q),
+                                          0, 0x7FFFFFFF, BN, lane, chunk, nullptr, 0,
+                                          epi_identity(), nullptr);
         } else {
           cb.tmW = &tmW;
           cb.sched = &sched;
@@ -697,8 +751,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           got = __shfl_sync(0xffffffffu, got, 0);
           good = got != 0;
-          reduce_c = direct;
-          if (good && !direct && last_unit && st.nseg == 2) {
+          if (good && last_unit && st.nseg == 2) {
             // This CTA's operand ring is idle: every MMA of the pair has
             // completed (this unit's accumulator is full) and no copy is
             // left to issue.  Load the other segment's 8 boxes at once into
@@ -718,7 +771,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             good = __shfl_sync(0xffffffffu, ld, 0) != 0;
             cb.stash = stash;
           }
-          if (!direct) cbp = &cb;
+          cbp = &cb;
         }
       }
       if (good && ready_slot < 0) {

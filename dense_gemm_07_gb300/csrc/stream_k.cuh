@@ -181,18 +181,24 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 // 0.3 us on a GB300), for W whole waves of P pairs, a last wave of T tiles
 // and kb k-slices per tile, fitted to measurements of the paired kernel: a
 // 256 x 128 unit takes as long as a whole tile (operand delivery, not the
-// MMA, paces it), so the column split saves only epilogue time; finishing
-// a tile halved along K costs about 44 slices after its main loop; a
-// stream-K run over the last whole wave and the partial one costs 30 +
-// 0.3 kb slices (its pairs work on different k of different tiles at once,
-// so fewer operand reads are shared in L2).
+// MMA, paces it), so the column split saves only epilogue time.  Finishing
+// a tile halved along K costs about 24 slices after its main loop when the
+// halves are added in C itself (in_c: two segments, a plain alpha * A.B
+// output step and a C open to TMA), 54 when they meet in the partial-sum
+// workspace; a stream-K run over the last whole wave and the partial one
+// costs 30 + 0.3 kb slices, or 65 + kb / 4 through the workspace (its pairs
+// work on different k of different tiles at once, so fewer operand reads
+// are shared in L2).
 enum PairScheduleKind { kPlainTail = 0, kColumnTail = 1, kHalvedTail = 2, kStreamKTail = 3 };
-inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb) {
+inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb,
+                                  bool in_c) {
   switch (kind) {
     case kPlainTail: return (W + 1) * kb + 16;
     case kColumnTail: return (W + 1) * kb + 8;
-    case kHalvedTail: return W * kb + (kb + 1) / 2 + 44;
-    default: return (W - 1) * kb + ((P + T) * kb + P - 1) / P + 30 + (3 * kb) / 10;
+    case kHalvedTail: return W * kb + (kb + 1) / 2 + (in_c ? 24 : 54);
+    default:
+      return (W - 1) * kb + ((P + T) * kb + P - 1) / P +
+             (in_c ? 30 + (3 * kb) / 10 : 65 + kb / 4);
   }
 }
 
@@ -202,8 +208,11 @@ inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int
 // 116 us for whole tiles).
 constexpr int64_t kSkAutoMaxOperandBytes = 96ll << 20;
 
+// in_c: tiles cut into two segments can be finished in C itself (C open to
+// TMA stores and an output step of alpha * A.B alone); it only changes
+// the automatic choice.
 inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
-                                  int max_pairs, int mode) {
+                                  int max_pairs, int mode, bool in_c = true) {
   PairSchedule s;
   s.tiles_m = static_cast<int>((M + 255) / 256);
   s.tiles_n = static_cast<int>((N + 255) / 256);
@@ -233,15 +242,16 @@ inline PairSchedule pair_schedule(int64_t M, int64_t N, int64_t K,
     // The simpler schedule unless a split along K is estimated to save more
     // than 8 slices (about 2.5 us).
     const int64_t kb = s.num_kb;
-    const int64_t base = pair_schedule_cost(col_split ? kColumnTail : kPlainTail, waves, tail, P, kb);
-    const int64_t halved = 2 * tail <= P ? pair_schedule_cost(kHalvedTail, waves, tail, P, kb)
-                                         : INT64_MAX;
+    const int64_t base =
+        pair_schedule_cost(col_split ? kColumnTail : kPlainTail, waves, tail, P, kb, in_c);
+    const int64_t halved =
+        2 * tail <= P ? pair_schedule_cost(kHalvedTail, waves, tail, P, kb, in_c) : INT64_MAX;
     const bool fits = 2 * (M * K + K * N) <= kSkAutoMaxOperandBytes;
     const int64_t streamk = waves >= 1 && fits
-                                ? pair_schedule_cost(kStreamKTail, waves, tail, P, kb)
+                                ? pair_schedule_cost(kStreamKTail, waves, tail, P, kb, in_c)
                                 : INT64_MAX;
     const int64_t best_k = halved < streamk ? halved : streamk;
-    if (best_k + 8 >= base) return column_split();
+    if (best_k >= base - 8) return column_split();
     full_sk = streamk < halved;
   }
   int64_t sk_tiles = 0, sk_pairs = 0;

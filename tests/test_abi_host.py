@@ -96,9 +96,12 @@ def test_plan_paths():
     assert _path("bf16", 5, 5, 0)[0] == "zero_fill"
     assert _path("f32", 5, 5, 0)[0] == "zero_fill"
     path, p = _path("bf16", 4096, 4096, 4096)
-    assert path == "bf16_tma" and p.tiles == 16 * 16 and p.workspace_bytes == 0
-    # three whole waves on 76 pairs, the last 28 tiles as 56 half-width units
-    assert (p.dp_tiles, p.sk_tiles, p.sk_pairs, p.pairs) == (256, 0, 0, 76)
+    # three whole waves on 76 pairs, then each of the last 28 tiles halved
+    # along K over two pairs (scratch: partial-sum slots and flags, which
+    # the halves need only when they cannot be added in C itself)
+    assert path == "bf16_tma" and p.tiles == 16 * 16
+    assert p.workspace_bytes == 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8
+    assert (p.dp_tiles, p.sk_tiles, p.sk_pairs, p.pairs) == (228, 28, 56, 76)
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
     path, p = _path("bf16", 129, 4096, 4096)
     assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (256, 256, 6)

@@ -59,7 +59,7 @@ PATHS = [
     ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + TMA stores
     ("bf16", 2560, 2302, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + row stores
     ("bf16", 512, 1024, 8192, None),   # tiles halved along K; alpha-only: finished in C
-    ("bf16", 2560, 2048, 4096, None),  # automatic stream-K runs after a whole wave
+    ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K),  # stream-K over every tile
     ("bf16", 48, 1000, 777, None),   # small M, cluster reduction
     ("f32", 200, 190, 300, None),    # FP32 small problem: 64 x 64 tiles split along K
     ("f32", 640, 520, 2000, None),   # FP32, one partial wave split along K

@@ -182,8 +182,11 @@ def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
 
 @pytest.mark.parametrize("shape,dp,sk,skp", [
     ((2560, 2048, 6200), 0, 80, 76),     # one wave + 4 tiles: all 80 shared as k runs
-    ((2600, 2100, 6150), 0, 99, 76),     # the same with ragged edges and K
-    ((2560, 2560, 8192), 76, 24, 48)])   # one wave, then 24 tiles halved along K
+    ((2530, 2040, 6150), 0, 80, 76),     # the same with ragged edges and K
+    ((2530, 2030, 6150), 0, 80, 76),     # and N % 4 != 0: row stores, partial sums
+    ((2600, 2100, 6150), 76, 23, 46),    # one wave, then 23 ragged tiles halved along K
+    ((2560, 2560, 8192), 76, 24, 48),    # one wave, then 24 tiles halved along K
+    ((4096, 4096, 4096), 228, 28, 56)])  # three waves, then 28 tiles halved along K
 def test_bf16_auto_k_splits_after_whole_waves_exact(shape, dp, sk, skp):
     # automatic schedule after a whole wave: stream-K over every tile, or
     # the last wave's tiles halved along K; sampled rows cover the split tiles
@@ -197,6 +200,21 @@ def test_bf16_auto_k_splits_after_whole_waves_exact(shape, dp, sk, skp):
     rows = np.unique(np.concatenate([np.arange(0, M, 173), np.arange(M - 300, M, 37), [M - 1]]))
     c_ref, _ = oracle_ref("bf16", a, b, rows=rows, with_abs=False)
     assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
+
+
+def test_bf16_halved_tail_deterministic_bits():
+    # 4096^3, automatic schedule: both halves of a split tile add into C
+    # (cleared first) in whichever order they finish; the bits never change
+    M = N = K = 4096
+    s, plan = g7.plan("bf16", M, N, K)
+    assert (plan.sk_tiles, plan.sk_pairs) == (28, 56)
+    a, b = inputs.make_pair(M, N, K, 26, inputs.NORMAL, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    first = g7.gemm_bf16_f32acc(a_d, b_d).clone()
+    for _ in range(5):
+        again = g7.gemm_bf16_f32acc(a_d, b_d)
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    assert g7.gemm_get_device_status() == 0
 
 
 @pytest.mark.parametrize("shape", [(2560, 2304, 1024), (4096, 4096, 1024)])

@@ -125,8 +125,8 @@ def test_work_is_balanced(lib, M, N, K, P, sched):
     assert max(costs) - min(costs) <= 2
 
 
-def _plan(M, N, K):
-    s, p = _abi.gemm_plan_bf16(M, N, K, 256, K, 256, N, 256, N)
+def _plan(M, N, K, c_addr=256):
+    s, p = _abi.gemm_plan_bf16(M, N, K, 256, K, 256, N, c_addr, N)
     assert s == 0
     return (p.dp_tiles, p.sk_tiles, p.sk_pairs, p.pairs), p.workspace_bytes
 
@@ -134,16 +134,20 @@ def _plan(M, N, K):
 def test_schedule_setting_and_plans(lib):
     prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_AUTO)
     try:
-        # automatic: the 28-tile last wave of 4096^3 runs as 56 half-width
-        # units, no scratch
-        assert _plan(4096, 4096, 4096) == ((256, 0, 0, 76), 0)
+        # automatic: 3 whole waves, then each tile of the 28-tile last wave
+        # of 4096^3 halved along K over 56 pairs (the halves are added in C)
+        ws_4096 = 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8
+        assert _plan(4096, 4096, 4096) == ((228, 28, 56, 76), ws_4096)
+        # C not open to TMA stores: the halves would meet in the partial-sum
+        # workspace, which costs more than the column split saves
+        assert _plan(4096, 4096, 4096, c_addr=260) == ((256, 0, 0, 76), 0)
+        assert _plan(2560, 2560, 4096, c_addr=260) == ((100, 0, 0, 76), 0)
         # few tiles and long K: each of the 8 tiles halved along K
         sched, ws = _plan(512, 1024, 8192)
         assert sched == (0, 8, 16, 16) and ws >= 16 * 4 * 128 * 1024
-        # whole waves, then a last wave of 28 tiles with 128 k-slices: each
-        # tail tile halved along K over 56 pairs (64 k-slices keep the
-        # column split, above)
-        assert _plan(4096, 4096, 8192) == ((228, 28, 56, 76), 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8)
+        assert _plan(4096, 4096, 8192) == ((228, 28, 56, 76), ws_4096)
+        assert _plan(5120, 5120, 4096)[0] == (380, 20, 40, 76)
+        assert _plan(2560, 2560, 4096)[0] == (76, 24, 48, 76)
         assert _plan(8192, 8192, 8192)[0] == (988, 36, 72, 76)
         assert _plan(4096, 4096, 6144)[0] == (228, 28, 56, 76)
         assert _plan(2560, 2560, 8192)[0] == (76, 24, 48, 76)
@@ -151,9 +155,10 @@ def test_schedule_setting_and_plans(lib):
         assert _plan(2560, 2048, 6200)[0] == (0, 80, 76, 76)
         assert _plan(2304, 2304, 8192)[0] == (0, 81, 76, 76)
         assert _plan(2560, 2048, 4096)[0] == (0, 80, 76, 76)
-        # a last whole wave and a small partial one, but 32 k-slices: the
-        # column split
+        # a last whole wave and a small partial one, but 32 or 48 k-slices:
+        # the column split
         assert _plan(4096, 4096, 2048)[0] == (256, 0, 0, 76)
+        assert _plan(4096, 4096, 3072)[0] == (256, 0, 0, 76)
         # a last wave of 52 tiles is more than half the pairs: no split
         assert _plan(2048, 4096, 11008) == ((128, 0, 0, 76), 0)
         assert _plan(2048, 11008, 4096) == ((344, 0, 0, 76), 0)
