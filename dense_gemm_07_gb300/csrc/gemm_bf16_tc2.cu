@@ -367,7 +367,8 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
                                                int64_t ldc,
                                                const EpiParams& epi,
                                                const SkCombine* cb,
-                                               bool reduce = false) {
+                                               bool reduce = false,
+                                               uint8_t* wide = nullptr) {
 #pragma unroll 1
   for (int c = 0; c < W / 32; ++c) {
     // Boxes wholly outside C are skipped (warp-uniform test); every other
@@ -376,8 +377,13 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
     if (row0 >= M || n0 + c * 32 >= N) continue;
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + c * 32, r);
-    uint8_t* buf = ebuf + (chunk++ & 1) * EPI_BOX_BYTES;
-    if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
+    uint8_t* buf;
+    if (wide) {
+      buf = wide + c * EPI_BOX_BYTES;  // a box per chunk: nothing to wait for
+    } else {
+      buf = ebuf + (chunk++ & 1) * EPI_BOX_BYTES;
+      if (lane == 0) bulk_wait_read<1>();  // the box's previous store has read it
+    }
     __syncwarp();
     tmem_ld_wait();
     if (cb && !combine_chunk(r, *cb, c, buf, lane)) return false;
@@ -420,6 +426,10 @@ __device__ __forceinline__ bool store_unit_tma(uint32_t taddr,
   }
   return true;
 }
+
+// (wide: W / 32 staging boxes of this warp's own, one per chunk, so no chunk
+// waits for an earlier store to have read its box; used for a pair's last
+// unit, whose operand ring is idle.)
 
 // Epilogue of one unit when C's layout does not allow TMA stores (a row
 // stride that is not a multiple of 16 bytes, or an unaligned base).  Per
@@ -657,46 +667,46 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       WorkIter peek = wi;
       WorkUnit after;
       const bool last_unit = !peek.next(sched, num_pairs, after);
-      int ok = 0;
-      if (lane == 0) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort, tmo) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) raise_abort(abort, peer_abort, status);
-        break;
-      }
-      tc_fence_after_sync();
+      // Everything that depends only on the unit is done while its MMAs
+      // run: coordinates, the split-tile lookup and, for a segment finished
+      // in C, the wait for the tile's cleared rows.
       const TileCoord tc = tile_order(w.tile, sched.tiles_m, sched.tiles_n, GROUP);
       const int m0 = tc.m * PAIR_M, n0 = tc.n * BN + w.n_off;
       const int row = m0 + static_cast<int>(rank) * CTA_M + q * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int row0 = row - lane;
+      const bool segment = w.k0 != 0 || w.k1 != sched.num_kb;
+      const SkTile st = segment ? sk_tile(sched, w.tile) : SkTile{pair, 1};
+      const bool in_c = segment && direct_ok && st.nseg == 2;
+      int ok = 1;
+      if (in_c && lane == 0 && pair != st.q_first) {
+        // A segment finished directly in C (above): it may add once the
+        // tile's rows of C have been cleared.
+        unsigned long long* f =
+            sk_ready(sk_sync, sched, st.q_first, sk_slot(sched, st.q_first, w.tile), rank, q);
+        ok = sk_wait_ready(f, sk_tag, abort, tmo) ? 1 : 0;
+        // the flag was read by this thread; C will be updated by the copy
+        // engine
+        fence_proxy_async_global();
+        // the only reader of this flag puts it back to zero for a replay of
+        // this launch with the same tag
+        if (ok) *f = 0ull;
+      }
+      if (lane == 0 && ok) ok = pair_wait(&ctl->acc_full[acc], acc_phase, abort, tmo) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) raise_abort(abort, peer_abort, status);
+        break;
+      }
+      tc_fence_after_sync();
 
       int ready_slot = -1;  // >= 0: this segment's flag goes up after its stores
       SkCombine cb;
       const SkCombine* cbp = nullptr;
-      bool reduce_c = false;  // add this segment into C (the other one is there)
+      bool reduce_c = in_c;  // add this segment into C (cleared at the start)
       bool good = true;
-      const bool segment = w.k0 != 0 || w.k1 != sched.num_kb;
-      const SkTile st = segment ? sk_tile(sched, w.tile) : SkTile{pair, 1};
-      if (segment && direct_ok && st.nseg == 2) {
-        // A segment finished directly in C (above): add it once the tile's
-        // rows of C have been cleared.
-        int got = 1;
-        if (lane == 0 && pair != st.q_first) {
-          unsigned long long* f =
-              sk_ready(sk_sync, sched, st.q_first, sk_slot(sched, st.q_first, w.tile), rank, q);
-          got = sk_wait_ready(f, sk_tag, abort, tmo) ? 1 : 0;
-          // the flag was read by this thread; C will be updated by the
-          // copy engine
-          fence_proxy_async_global();
-          // the only reader of this flag puts it back to zero for a replay
-          // of this launch with the same tag
-          if (got) *f = 0ull;
-        }
-        good = __shfl_sync(0xffffffffu, got, 0) != 0;
-        reduce_c = true;
-      } else if (segment) {
+      if (segment && !in_c) {
         // A stream-K segment: take a ticket; the last of the tile's
         // segments finishes it, the others leave their partial sums.
         int ticket = 0;
@@ -774,18 +784,23 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           cbp = &cb;
         }
       }
+      // The pair's last unit: its operand ring is idle (every MMA of the
+      // pair has completed and no copy is left to issue), so unless it holds
+      // the other segment's sums, this warp's quarter of it stages a box per
+      // chunk.
+      uint8_t* wide = last_unit && cbp == nullptr ? smem + q * (BN / 32) * EPI_BOX_BYTES : nullptr;
       if (good && ready_slot < 0) {
         if (w.width != BN) {
           // a column-split unit of the last wave (never a stream-K segment)
           if (tma_c)
             store_unit_tma<BN / 2, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
-                                   chunk, C, ldc, epi, nullptr);
+                                   chunk, C, ldc, epi, nullptr, false, wide);
           else
             store_unit_rows<BN / 2, GELU>(taddr, C, ldc, row0, n0, M, N, epi, nullptr,
                                     ebuf, lane, chunk);
         } else {
           good = tma_c ? store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N,
-                                            lane, chunk, C, ldc, epi, cbp, reduce_c)
+                                            lane, chunk, C, ldc, epi, cbp, reduce_c, wide)
                        : store_unit_rows<BN, GELU>(taddr, C, ldc, row0, n0, M, N,
                                              epi, cbp, ebuf, lane, chunk);
         }
