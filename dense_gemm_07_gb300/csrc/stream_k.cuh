@@ -88,7 +88,7 @@ struct WorkUnit {
 // Walks one pair's units: its data-parallel units, then its stream-K range.
 struct WorkIter {
   int next_dp;
-  int64_t it, end;
+  int64_t it, end;  // stream-K range [it, end) still to walk, from the end
 
   __host__ __device__ void init(const PairSchedule& s, int pair) {
     next_dp = pair;
@@ -119,17 +119,20 @@ struct WorkIter {
       }
       return true;
     }
-    if (it < end) {
-      const int64_t t = it / s.num_kb;
-      const int k0 = static_cast<int>(it - t * s.num_kb);
-      const int64_t left = end - it;
-      const int k1 = left < s.num_kb - k0 ? k0 + static_cast<int>(left) : s.num_kb;
+    if (end > it) {
+      // The range is walked from its end: its last tile first, from k = 0,
+      // so that the pairs start their runs in step along K (their first
+      // slices are shared in L2, as whole tiles' are) rather than each at
+      // its own depth.
+      const int64_t t = (end - 1) / s.num_kb;
+      const int64_t x0 = t * s.num_kb;
+      const int64_t lo = it > x0 ? it : x0;
       u.tile = s.dp_tiles + static_cast<int>(t);
-      u.k0 = k0;
-      u.k1 = k1;
+      u.k0 = static_cast<int>(lo - x0);
+      u.k1 = static_cast<int>(end - x0);
       u.n_off = 0;
       u.width = 256;
-      it += k1 - k0;
+      end = lo;
       return true;
     }
     return false;
@@ -186,9 +189,9 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 // halves are added in C itself (in_c: two segments, a plain alpha * A.B
 // output step and a C open to TMA), 54 when they meet in the partial-sum
 // workspace; a stream-K run over the last whole wave and the partial one
-// costs 30 + 0.3 kb slices, or 65 + kb / 4 through the workspace (its pairs
-// work on different k of different tiles at once, so fewer operand reads
-// are shared in L2).
+// costs 36 + kb / 8 slices, or 60 + kb / 5 through the workspace (its
+// pairs' runs end at different k, so fewer operand reads are shared in L2
+// near the end, and the shortest segments pay a tile's start-up).
 enum PairScheduleKind { kPlainTail = 0, kColumnTail = 1, kHalvedTail = 2, kStreamKTail = 3 };
 inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb,
                                   bool in_c) {
@@ -198,7 +201,7 @@ inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int
     case kHalvedTail: return W * kb + (kb + 1) / 2 + (in_c ? 24 : 54);
     default:
       return (W - 1) * kb + ((P + T) * kb + P - 1) / P +
-             (in_c ? 30 + (3 * kb) / 10 : 65 + kb / 4);
+             (in_c ? 36 + kb / 8 : 60 + kb / 5);
   }
 }
 
