@@ -185,23 +185,24 @@ __host__ __device__ inline int sk_slot(const PairSchedule& s, int q, int tile) {
 // and kb k-slices per tile, fitted to measurements of the paired kernel: a
 // 256 x 128 unit takes as long as a whole tile (operand delivery, not the
 // MMA, paces it), so the column split saves only epilogue time.  Finishing
-// a tile halved along K costs about 24 slices after its main loop when the
-// halves are added in C itself (in_c: two segments, a plain alpha * A.B
-// output step and a C open to TMA), 54 when they meet in the partial-sum
-// workspace; a stream-K run over the last whole wave and the partial one
-// costs 36 + kb / 8 slices, or 60 + kb / 5 through the workspace (its
-// pairs' runs end at different k, so fewer operand reads are shared in L2
-// near the end, and the shortest segments pay a tile's start-up).
+// a tile halved along K costs about 20 + kb / 16 slices after its main loop
+// when the halves are added in C itself (in_c: two segments, a plain
+// alpha * A.B output step and a C open to TMA), 58 when they meet in the
+// partial-sum workspace; a stream-K run over the last whole wave and the
+// partial one costs 38 + kb / 16 slices, or 75 + kb / 16 through the
+// workspace (its pairs' runs end at different k, so fewer operand reads are
+// shared in L2 near the end, and the shortest segments pay a tile's
+// start-up).
 enum PairScheduleKind { kPlainTail = 0, kColumnTail = 1, kHalvedTail = 2, kStreamKTail = 3 };
 inline int64_t pair_schedule_cost(int kind, int64_t W, int64_t T, int64_t P, int64_t kb,
                                   bool in_c) {
   switch (kind) {
     case kPlainTail: return (W + 1) * kb + 16;
     case kColumnTail: return (W + 1) * kb + 8;
-    case kHalvedTail: return W * kb + (kb + 1) / 2 + (in_c ? 24 : 54);
+    case kHalvedTail: return W * kb + (kb + 1) / 2 + (in_c ? 20 + kb / 16 : 58);
     default:
       return (W - 1) * kb + ((P + T) * kb + P - 1) / P +
-             (in_c ? 36 + kb / 8 : 60 + kb / 5);
+             (in_c ? 38 + kb / 16 : 75 + kb / 16);
   }
 }
 

@@ -184,8 +184,8 @@ def test_bf16_stream_k_after_whole_waves_sampled(stream_k):
     ((2560, 2048, 6200), 0, 80, 76),     # one wave + 4 tiles: all 80 shared as k runs
     ((2530, 2040, 6150), 0, 80, 76),     # the same with ragged edges and K
     ((2530, 2030, 6150), 0, 80, 76),     # and N % 4 != 0: row stores, partial sums
-    ((2600, 2100, 6150), 76, 23, 46),    # one wave, then 23 ragged tiles halved along K
-    ((2560, 2560, 8192), 76, 24, 48),    # one wave, then 24 tiles halved along K
+    ((2600, 2100, 4100), 76, 23, 46),    # one wave, then 23 ragged tiles halved along K
+    ((2560, 2560, 4096), 76, 24, 48),    # one wave, then 24 tiles halved along K
     ((4096, 4096, 4096), 228, 28, 56)])  # three waves, then 28 tiles halved along K
 def test_bf16_auto_k_splits_after_whole_waves_exact(shape, dp, sk, skp):
     # automatic schedule after a whole wave: stream-K over every tile, or

@@ -150,15 +150,17 @@ def test_schedule_setting_and_plans(lib):
         assert _plan(2560, 2560, 4096)[0] == (76, 24, 48, 76)
         assert _plan(8192, 8192, 8192)[0] == (988, 36, 72, 76)
         assert _plan(4096, 4096, 6144)[0] == (228, 28, 56, 76)
-        assert _plan(2560, 2560, 8192)[0] == (76, 24, 48, 76)
+        # one whole wave, a last wave of 24 and 128 k-slices: every tile shared
+        assert _plan(2560, 2560, 8192)[0] == (0, 100, 76, 76)
+        assert _plan(2816, 2816, 6144)[0] == (0, 121, 76, 76)
         # one whole wave and a small last wave: every tile shared (stream-K)
         assert _plan(2560, 2048, 6200)[0] == (0, 80, 76, 76)
         assert _plan(2304, 2304, 8192)[0] == (0, 81, 76, 76)
         assert _plan(2560, 2048, 4096)[0] == (0, 80, 76, 76)
-        # a last whole wave and a small partial one, but 32 or 48 k-slices:
-        # the column split
+        # a last whole wave and a small partial one, but 32 k-slices: the
+        # column split (48 k-slices: halved)
         assert _plan(4096, 4096, 2048)[0] == (256, 0, 0, 76)
-        assert _plan(4096, 4096, 3072)[0] == (256, 0, 0, 76)
+        assert _plan(4096, 4096, 3072)[0] == (228, 28, 56, 76)
         # a last wave of 52 tiles is more than half the pairs: no split
         assert _plan(2048, 4096, 11008) == ((128, 0, 0, 76), 0)
         assert _plan(2048, 11008, 4096) == ((344, 0, 0, 76), 0)
