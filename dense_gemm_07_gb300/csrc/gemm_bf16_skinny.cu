@@ -64,6 +64,21 @@ __device__ __forceinline__ void raise_abort(volatile int* abort,
   atomicOr(status, 1u);
 }
 
+// Arm stage `stage`'s "full" barrier and copy k-slice kb into it: the two
+// 64-column boxes of B's 128-column tile and the NM x 64 box of A.
+template <int NM>
+__device__ __forceinline__ void issue_stage(uint8_t* smem, uint64_t* full, int stage,
+                                            const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                            int n0, int kb) {
+  using S = SkinnyShape<NM>;
+  uint8_t* sb = smem + stage * S::STAGE_BYTES;
+  uint8_t* sa = sb + B_STAGE_BYTES;
+  mbar_arrive_expect_tx(&full[stage], S::STAGE_BYTES);
+  tma_load_2d(sb, tmB, &full[stage], n0, kb * BK);
+  tma_load_2d(sb + B_BOX_BYTES, tmB, &full[stage], n0 + 64, kb * BK);
+  tma_load_2d(sa, tmA, &full[stage], kb * BK, 0);
+}
+
 // GELU: whether the GELU activation is compiled in (epi_apply); the copy
 // without it serves every other epilogue.
 template <int NM, bool GELU>
@@ -103,6 +118,11 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    // The ring is empty, so its first stages need no slot to be freed: their
+    // copies go out now, while tensor memory is allocated and the block
+    // meets (the barriers were initialised by this thread).
+    const int pre = num_kb < STAGES ? num_kb : STAGES;
+    for (int i = 0; i < pre; ++i) issue_stage<NM>(smem, ctl->full, i, &tmA, &tmB, n0, kb_begin + i);
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, S::TMEM_COLS);
@@ -117,21 +137,18 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      // continue after the stages issued before the block barrier
+      const int pre = num_kb < STAGES ? num_kb : STAGES;
+      int stage = pre % STAGES;
+      uint32_t phase = pre == STAGES ? 1u : 0u;
       int last_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
-      for (int kb = kb_begin; kb < kb_end; ++kb) {
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = s < pre ? 0 : -1;
+      for (int kb = kb_begin + pre; kb < kb_end; ++kb) {
         if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort, tmo)) {
           raise_abort(abort, status);
           break;
         }
-        uint8_t* sb = smem + stage * S::STAGE_BYTES;
-        uint8_t* sa = sb + B_STAGE_BYTES;
-        mbar_arrive_expect_tx(&ctl->full[stage], S::STAGE_BYTES);
-        tma_load_2d(sb, &tmB, &ctl->full[stage], n0, kb * BK);
-        tma_load_2d(sb + B_BOX_BYTES, &tmB, &ctl->full[stage], n0 + 64, kb * BK);
-        tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, 0);
+        issue_stage<NM>(smem, ctl->full, stage, &tmA, &tmB, n0, kb);
         last_phase[stage] = static_cast<int>(phase);
         if (++stage == STAGES) {
           stage = 0;
