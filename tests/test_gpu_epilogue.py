@@ -151,3 +151,34 @@ def test_epilogue_gelu(kind, M, N, K, schedule):
     lim = 1.13 * (RTOL[kind] * scale + ATOL[kind]) + 1e-6 * np.abs(pre) + 1e-6
     err = np.abs(got - want)
     assert np.all(err <= lim), float(np.max(err - lim))
+
+
+@pytest.mark.parametrize("epi", [(2.0, -1.0, True, "relu"), (1.0, 0.0, False, "none")],
+                         ids=["workspace", "in_c"])
+def test_epilogue_halved_after_whole_waves_sampled(epi):
+    # 2560 x 2560 x 8192: one whole wave of 76 tiles, then the last 24 halved
+    # along K over 48 pairs.  With beta, a bias and ReLU the halves meet in
+    # the partial-sum workspace; the plain product adds them in C itself.
+    # Sampled rows cover the halved tiles (rows 1024..2559).
+    M, N, K = 2560, 2560, 8192
+    alpha, beta, use_bias, act = epi
+    a, b = inputs.make_pair(M, N, K, 56, inputs.INT3, dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(1056)
+    c0 = torch.randint(-5, 6, (M, N), generator=g).float()
+    bias = torch.randint(-4, 5, (N,), generator=g).float() if use_bias else None
+    out = c0.to(DEV).clone()
+    g7.gemm_bf16_f32acc_ex(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
+                           bias=bias.to(DEV) if bias is not None else None,
+                           activation=act)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    rows = np.unique(np.concatenate([np.arange(0, M, 211), np.arange(1024, 2048, 97),
+                                     np.arange(2048, M, 41), [M - 1]]))
+    ab, _ = oracle_ref("bf16", a, b, rows=rows, with_abs=False)
+    want = oracle.gemm_epilogue(ab, alpha=alpha, beta=beta,
+                                C0=c0.numpy()[rows] if beta != 0 else None,
+                                bias=bias.numpy() if bias is not None else None,
+                                act=1 if act == "relu" else 0)
+    got = out.cpu().numpy().astype(np.float64)[rows]
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {tuple(bad[0])}"
