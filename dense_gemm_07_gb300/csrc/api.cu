@@ -198,7 +198,8 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->workspace_bytes = pack_bytes(M, N, K, p->pack_a, p->pack_b);
   if (M <= kSkinnyMaxM) {
     // Small M: 128-column tiles of C, K split over a cluster (the split is
-    // reported for the 152 SMs of a GB300; launches use the device's count).
+    // reported for the 152 SMs of a GB300; launches use the device's count
+    // and lower the split until every cluster is resident at once).
     p->path = GEMM_PATH_BF16_SKINNY;
     p->tile_m = skinny_rows(static_cast<int>(M));
     p->tile_n = kSkinnyTileN;
@@ -618,7 +619,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                           skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
   if (s == GEMM_OK && skinny) {
     s = from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
-                                          skinny_split(n, k, d->sms), d->status,
+                                          skinny_split_resident(m, n, k, d->sms), d->status,
                                           epi, stream));
   } else if (s == GEMM_OK) {
     const bool vec_c = aligned16(C) && ldc % 4 == 0;
@@ -904,7 +905,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   if (s != GEMM_OK) return s;
   if (skinny)
     return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
-                                             skinny_split(n, k, d->sms),
+                                             skinny_split_resident(m, n, k, d->sms),
                                              d->status, epi_identity(), stream));
   const bool vec_c = aligned16(C) && ldc % 4 == 0;
   if (max_pairs > 0) {

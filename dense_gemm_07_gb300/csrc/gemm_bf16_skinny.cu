@@ -21,6 +21,7 @@
 //     consecutive columns).  The sum order is fixed, so results are
 //     deterministic; no global workspace and no second kernel are needed.
 // Every mbarrier wait is bounded as in the other tensor-core kernels.
+#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -273,28 +274,75 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
-int g_attr_done[64][4];
+std::atomic<int> g_attr_done[64][4];
+// Clusters of c CTAs that can be resident at once, per device, row class
+// and c (0: not asked yet).
+std::atomic<int> g_max_clusters[64][4][9];
+
+template <int NM>
+size_t skinny_smem_bytes() {
+  using S = SkinnyShape<NM>;
+  return 1024 + static_cast<size_t>(S::STAGES) * S::STAGE_BYTES + sizeof(SkinnyControl<S::STAGES>);
+}
+
+template <int NM>
+cudaError_t set_attrs_nm(int dev, int slot) {
+  if (g_attr_done[dev][slot].load()) return cudaSuccess;
+  const size_t smem = skinny_smem_bytes<NM>();
+  for (auto k : {gemm_bf16_skinny_kernel<NM, false>, gemm_bf16_skinny_kernel<NM, true>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  g_attr_done[dev][slot].store(1);
+  return cudaSuccess;
+}
+
+// How many clusters of cs CTAs fit on the device at once.  A cluster must
+// sit within one GPC, so this can be less than the SM count / cs (clusters
+// of 4 reach only 144 of a GB300's 152 SMs).  -1: the query failed.
+template <int NM>
+int max_clusters_nm(int cs, int dev, int slot) {
+  const int known = g_max_clusters[dev][slot][cs].load();
+  if (known != 0) return known;
+  if (set_attrs_nm<NM>(dev, slot) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = skinny_smem_bytes<NM>();
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_skinny_kernel<NM, false>, &cfg) !=
+          cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    return -1;
+  }
+  g_max_clusters[dev][slot][cs].store(n);
+  return n;
+}
 
 template <int NM>
 cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
                       int64_t ldc, int M, int N, int K, int cs,
                       unsigned int* status, const EpiParams& epi,
                       cudaStream_t stream, int dev, int slot) {
-  using S = SkinnyShape<NM>;
-  const size_t smem = 1024 + static_cast<size_t>(S::STAGES) * S::STAGE_BYTES +
-                      sizeof(SkinnyControl<S::STAGES>);
+  const size_t smem = skinny_smem_bytes<NM>();
   auto kernel = epi.act == kActGelu ? gemm_bf16_skinny_kernel<NM, true>
                                      : gemm_bf16_skinny_kernel<NM, false>;
-  if (!g_attr_done[dev][slot]) {
-    for (auto k : {gemm_bf16_skinny_kernel<NM, false>, gemm_bf16_skinny_kernel<NM, true>}) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
-    g_attr_done[dev][slot] = 1;
-  }
+  const cudaError_t ea = set_attrs_nm<NM>(dev, slot);
+  if (ea != cudaSuccess) return ea;
   const int tiles = (N + TILE_N - 1) / TILE_N;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -325,6 +373,31 @@ int skinny_split(int N, int K, int sms) {
   if (cs > 8) cs = 8;
   if (cs > kb) cs = kb;
   return cs < 1 ? 1 : cs;
+}
+
+int skinny_split_resident(int M, int N, int K, int sms) {
+  int cs = skinny_split(N, K, sms);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return cs;
+  }
+  const int tiles = (N + TILE_N - 1) / TILE_N;
+  // The largest split whose clusters all fit at once: one that does not
+  // leaves some clusters for a second round, about doubling the time
+  // (16 x 4864 x 4096 in clusters of 4: 24.1 us against 17.2 us for
+  // N = 4096).
+  for (; cs > 1; --cs) {
+    int fit = 0;
+    switch (skinny_rows(M)) {
+      case 16: fit = max_clusters_nm<16>(cs, dev, 0); break;
+      case 32: fit = max_clusters_nm<32>(cs, dev, 1); break;
+      case 64: fit = max_clusters_nm<64>(cs, dev, 2); break;
+      default: fit = max_clusters_nm<128>(cs, dev, 3); break;
+    }
+    if (fit < 0 || tiles <= fit) break;
+  }
+  return cs;
 }
 
 cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,

@@ -99,6 +99,9 @@ constexpr int kSkinnyTileN = 128;
 int skinny_rows(int M);
 // CTAs per cluster (k split) for an N x K problem on `sms` SMs (1..8).
 int skinny_split(int N, int K, int sms);
+// The same, lowered until every cluster of the launch fits on the current
+// device at once (checked with the occupancy calculator; host code).
+int skinny_split_resident(int M, int N, int K, int sms);
 // tmA: box {64, skinny_rows(M)}; tmB: the usual box {64, 64}.
 cudaError_t launch_gemm_bf16_skinny(const CUtensorMap& tmA,
                                     const CUtensorMap& tmB, float* C,
