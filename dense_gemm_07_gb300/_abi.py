@@ -26,7 +26,7 @@ GEMM_ERR_SCRATCH_TOO_SMALL = 7
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 PATHS = {0: "none", 1: "zero_fill", 2: "f32_simt", 3: "bf16_tma",
-         4: "bf16_packed", 5: "bf16_skinny"}
+         4: "bf16_packed", 5: "bf16_skinny", 6: "bf16_gemv"}
 
 
 class GemmPlan(ctypes.Structure):

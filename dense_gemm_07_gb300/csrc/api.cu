@@ -35,7 +35,8 @@ enum ScratchUse {
   kScratchStreamK = 0,  // BF16 stream-K partial sums + tagged sync words
   kScratchSplitK = 1,   // FP32 split-K counters (kept zero) + partial sums
   kScratchPack = 2,     // BF16 operands copied to aligned rows
-  kScratchUses = 3
+  kScratchGemv = 3,     // BF16 M = 1: counters (kept zero) + partial sums
+  kScratchUses = 4
 };
 struct StreamScratch {
   cudaStream_t stream = nullptr;
@@ -91,6 +92,17 @@ bool tma_store_ok(const void* C, int64_t N, int64_t ldc) {
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// M = 1: counters of the column blocks at the start of the scratch block, a
+// fixed area so that every call finds them zero whatever its size (each
+// launch's last range puts its counter back); partial sums after it.
+// Beyond 16384 column blocks the rows are not split.
+constexpr int64_t kGemvCounterBytes = 65536;
+int gemv_ranges_capped(int64_t N, int64_t K, int sms) {
+  const int64_t blocks = (N + kGemvCols - 1) / kGemvCols;
+  if (blocks * 4 > kGemvCounterBytes) return 1;
+  return gemv_ranges(static_cast<int>(N), static_cast<int>(K), sms);
+}
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
                          int64_t lda, const void* B, int64_t ldb,
@@ -192,10 +204,26 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   }
   // The tensor-memory accelerator reads an operand in place when its base is
   // 16-byte aligned and its row stride is a multiple of 16 bytes (8 BF16).
-  p->pack_a = (aligned16(A) && lda % 8 == 0) ? 0 : 1;
+  // (one row of A has no row stride to speak of: only its base counts)
+  p->pack_a = (aligned16(A) && (lda % 8 == 0 || M == 1)) ? 0 : 1;
   p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
   p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
   p->workspace_bytes = pack_bytes(M, N, K, p->pack_a, p->pack_b);
+  if (M == 1) {
+    // One row of A: B streamed through shared memory, products on the CUDA
+    // cores (the row ranges are reported for the 152 SMs of a GB300;
+    // launches use the device's count).
+    p->path = GEMM_PATH_BF16_GEMV;
+    p->tile_m = 1;
+    p->tile_n = kGemvCols;
+    p->tile_k = kGemvRows;
+    p->stages = kGemvStages;
+    p->split_k = gemv_ranges_capped(N, K, 152);
+    p->tiles = ((N + kGemvCols - 1) / kGemvCols) * p->split_k;
+    if (p->split_k > 1)
+      p->workspace_bytes += kGemvCounterBytes + gemv_workspace_bytes(static_cast<int>(N), p->split_k);
+    return GEMM_OK;
+  }
   if (M <= kSkinnyMaxM) {
     // Small M: 128-column tiles of C, K split over a cluster (the split is
     // reported for the 152 SMs of a GB300; launches use the device's count
@@ -347,7 +375,8 @@ gemm_status_t encoder(EncodeTiledFn* fn) {
 gemm_status_t make_map_typed(CUtensorMap* map, CUtensorMapDataType type,
                              int64_t elem_bytes, const void* base, int64_t inner,
                              int64_t outer, int64_t ld, uint32_t box_inner,
-                             uint32_t box_outer) {
+                             uint32_t box_outer,
+                             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = nullptr;
   gemm_status_t s = encoder(&enc);
   if (s != GEMM_OK) return s;
@@ -358,8 +387,7 @@ gemm_status_t make_map_typed(CUtensorMap* map, CUtensorMapDataType type,
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, type, 2,
                          const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INTERNAL;
@@ -378,7 +406,9 @@ gemm_status_t make_operand_maps(CUtensorMap* tmA, CUtensorMap* tmB,
                                 const uint16_t* a, int64_t lda,
                                 const uint16_t* b, int64_t ldb, int64_t M,
                                 int64_t N, int64_t K, uint32_t a_rows) {
-  gemm_status_t s = make_map(tmA, a, K, M, lda, kTcTileK, a_rows);
+  // A single row is read in place whatever its stride (boxes cover rows the
+  // map holds as out of range, which read 0), so any 16-byte multiple will do.
+  gemm_status_t s = make_map(tmA, a, K, M, M == 1 ? round_up(lda, 8) : lda, kTcTileK, a_rows);
   if (s == GEMM_OK) s = make_map(tmB, b, N, K, ldb, 64, kTcTileK);
   return s;
 }
@@ -562,6 +592,38 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   return s;
 }
 
+// M = 1 on operands the copy engine can read in place (after any copy):
+// unswizzled maps of B (256 x 16 boxes) and of A's row (16-element boxes),
+// the counters and partial sums, the launch.
+gemm_status_t run_gemv(DeviceState* d, const uint16_t* a, int64_t lda, const uint16_t* b,
+                       int64_t ldb, float* C, int64_t N, int64_t K, const EpiParams& epi,
+                       cudaStream_t stream) {
+  const int n = static_cast<int>(N), k = static_cast<int>(K);
+  const int ranges = gemv_ranges_capped(N, K, d->sms);
+  CUtensorMap tmA, tmB;
+  gemm_status_t s = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, K, 1,
+                                   round_up(lda, 8), kGemvRows, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (s == GEMM_OK)
+    s = make_map_typed(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b, N, K, ldb, 256, kGemvRows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (s != GEMM_OK) return s;
+  void* ws = nullptr;
+  bool fresh = false, owned = false;
+  if (ranges > 1) {
+    s = call_scratch(d, stream, kScratchGemv,
+                     kGemvCounterBytes + gemv_workspace_bytes(n, ranges), &ws, &fresh, &owned);
+    if (s != GEMM_OK) return s;
+    if (fresh) s = from_cuda(cudaMemsetAsync(ws, 0, kGemvCounterBytes, stream));
+  }
+  if (s == GEMM_OK)
+    s = from_cuda(launch_gemm_bf16_gemv(
+        tmA, tmB, C, n, k, ranges,
+        ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kGemvCounterBytes) : nullptr,
+        static_cast<unsigned int*>(ws), d->status, epi, stream));
+  if (owned) pool_free(ws, stream);
+  return s;
+}
+
 gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                        int64_t lda, const uint16_t* B, int64_t ldb, float* C,
                        int64_t ldc, cudaStream_t stream,
@@ -613,6 +675,12 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (s == GEMM_OK)
     s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
                                 &b_op, &ldb_op, stream));
+  if (plan.path == GEMM_PATH_BF16_GEMV) {
+    if (s == GEMM_OK) s = run_gemv(d, a_op, lda_op, b_op, ldb_op, C, N, K, epi, stream);
+    if (owned) pool_free(ws, stream);
+    if (sk_owned) pool_free(sk, stream);
+    return s;
+  }
   CUtensorMap tmA, tmB;
   if (s == GEMM_OK)
     s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
@@ -896,7 +964,10 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
                               &b_op, &ldb_op, stream));
   CUtensorMap tmA, tmB;
-  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
+  // M = 1 runs on the small-M kernel here: its cluster reduction needs no
+  // counters, which the shared fixed scratch could not keep zero.
+  const bool skinny =
+      plan.path == GEMM_PATH_BF16_SKINNY || plan.path == GEMM_PATH_BF16_GEMV;
   const int max_pairs =
       !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
   if (s == GEMM_OK)

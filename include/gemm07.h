@@ -281,9 +281,14 @@ typedef enum gemm_path {
     GEMM_PATH_F32_SIMT = 2,     /* gemm_f32 register-blocked kernel         */
     GEMM_PATH_BF16_TMA = 3,     /* tcgen05 kernel reading the operands      */
     GEMM_PATH_BF16_PACKED = 4,  /* operands copied to aligned workspace first */
-    GEMM_PATH_BF16_SKINNY = 5   /* M <= 128: 128-column tiles, K split over a
-                                   cluster, B streamed once (A/B may also be
-                                   copied first: see pack_a / pack_b) */
+    GEMM_PATH_BF16_SKINNY = 5,  /* 2 <= M <= 128: 128-column tiles, K split
+                                   over a cluster, B streamed once (A/B may
+                                   also be copied first: see pack_a / pack_b) */
+    GEMM_PATH_BF16_GEMV = 6     /* M == 1: B streamed through shared memory in
+                                   1024-column blocks, FP32 products on the
+                                   CUDA cores, rows split into split_k ranges
+                                   added in range order (the no-allocation
+                                   entry point uses GEMM_PATH_BF16_SKINNY) */
 } gemm_path_t;
 
 typedef struct gemm_plan {

@@ -109,7 +109,15 @@ def test_plan_paths():
     path, p = _path("bf16", 16, 4096, 4096)
     assert path == "bf16_skinny" and (p.tile_m, p.tile_n, p.split_k) == (16, 128, 4)
     assert p.tiles == 32 * 4
-    assert _path("bf16", 1, 4096, 4096)[1].tile_m == 16
+    # M = 1: 1024-column blocks of B, rows split into 38 ranges (4 x 38 = 152
+    # blocks), partial sums in scratch after a fixed 64 KB of counters
+    path, p = _path("bf16", 1, 4096, 4096)
+    assert path == "bf16_gemv" and (p.tile_m, p.tile_n, p.tile_k, p.split_k) == (1, 1024, 16, 38)
+    assert p.tiles == 4 * 38 and p.workspace_bytes == 65536 + 4 * 38 * 1024 * 4
+    # one 16-row stage: a single range, no scratch
+    path, p = _path("bf16", 1, 1000, 16)
+    assert path == "bf16_gemv" and p.split_k == 1 and p.workspace_bytes == 0
+    assert _path("bf16", 2, 4096, 4096)[1].tile_m == 16
     assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
     assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
     assert _path("bf16", 16, 100, 64)[1].split_k == 1      # one k slice only

@@ -61,6 +61,8 @@ PATHS = [
     ("bf16", 512, 1024, 8192, None),   # tiles halved along K; alpha-only: finished in C
     ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K),  # stream-K over every tile
     ("bf16", 48, 1000, 777, None),   # small M, cluster reduction
+    ("bf16", 1, 4096, 4096, None),   # M = 1: range sums added by the last range
+    ("bf16", 1, 1000, 40, None),     # M = 1, one range: finished in place
     ("f32", 200, 190, 300, None),    # FP32 small problem: 64 x 64 tiles split along K
     ("f32", 640, 520, 2000, None),   # FP32, one partial wave split along K
     ("f32", 2560, 2048, 640, None),  # FP32, whole waves + split tail
@@ -119,7 +121,8 @@ def test_unknown_activation_rejected():
 @pytest.mark.parametrize("kind,M,N,K,schedule", [
     ("f32", 700, 900, 1000, None), ("f32", 200, 190, 300, None),
     ("bf16", 700, 900, 1000, None), ("bf16", 300, 258, 200, None),
-    ("bf16", 48, 1000, 777, None), ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K)])
+    ("bf16", 48, 1000, 777, None), ("bf16", 1, 3000, 3001, None),
+    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K)])
 def test_epilogue_gelu(kind, M, N, K, schedule):
     # GELU after alpha, beta and the bias on every path.  Bound: GELU's slope
     # is at most 1.13, so the pre-activation bound grows by that factor; the

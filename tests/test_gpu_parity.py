@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import dense_gemm_07_gb300 as g7
+from dense_gemm_07_gb300 import _abi
 from dense_gemm_07_gb300 import inputs
 from gemm_check import (assert_guards_intact, assert_within, guarded_output,
                         oracle_ref)
@@ -263,6 +264,34 @@ def test_bf16_boundary_sweep_exact(M, N, K):
 @pytest.mark.parametrize("M", [1, 16])
 def test_bf16_skinny_exact(M):
     _check("bf16", M, 4096, 4096, 4, inputs.INT3, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 3001), (1, 3001, 1000),
+                                   (1, 127, 127), (1, 11008, 4096), (1, 4096, 11008),
+                                   (1, 4096, 1), (1, 4096, 16), (1, 4096, 17), (1, 1, 64),
+                                   (1, 256, 65536), (1, 1100, 40)])
+def test_bf16_vector_times_matrix_exact(shape):
+    # M = 1: B streamed in 1024-column blocks split into row ranges; ragged
+    # N (a partial or wholly out-of-range box), ragged K, B copied first
+    # (N = 3001, 127), K below one 16-row stage, long K (many ranges)
+    M, N, K = shape
+    s, plan = g7.plan("bf16", M, N, K)
+    assert _abi.PATHS[plan.path] == "bf16_gemv"
+    _check("bf16", M, N, K, 19, inputs.INT3, exact=True)
+
+
+def test_bf16_vector_times_matrix_general_values_and_bits():
+    # N(0,1) inputs within the BF16 bound; the range sums are added in a
+    # fixed order, so repeated calls give the same bits
+    a, b = inputs.make_pair(1, 4096, 11008, 20, inputs.NORMAL, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    first = g7.gemm_bf16_f32acc(a_d, b_d).clone()
+    for _ in range(3):
+        again = g7.gemm_bf16_f32acc(a_d, b_d)
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    c_ref, s_ref = oracle_ref("bf16", a, b)
+    assert_within("bf16", first.cpu().numpy(), c_ref, s_ref)
+    assert g7.gemm_get_device_status() == 0
 
 
 @pytest.mark.parametrize("shape", [(2, 300, 1000), (17, 1000, 777), (33, 257, 4096),
