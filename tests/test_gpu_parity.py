@@ -523,14 +523,14 @@ def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
         assert_within("bf16", c.cpu().numpy()[rows], c_ref, None, exact=True)
 
 
-@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed"])
+@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed", "bf16_gemv"])
 def test_capture_on_fresh_stream_then_replay(case):
     # Captured on a stream the library has never seen: its scratch is then
     # allocated inside the graph (owned by it) rather than kept, and every
     # replay on new operand values is exact.
     kind = "f32" if case.startswith("f32") else "bf16"
     M, N, K = {"f32_split_k": (2560, 2048, 640), "bf16_stream_k": (2560, 2304, 1024),
-               "bf16_packed": (700, 500, 333)}[case]
+               "bf16_packed": (700, 500, 333), "bf16_gemv": (1, 4096, 4096)}[case]
     dtype = _dtype(kind)
     fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
     a, b = inputs.make_pair(M, N, K, 35, inputs.INT3, dtype=dtype)

@@ -109,3 +109,17 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     assert _noalloc(a, b, c) == _abi.GEMM_ERR_SCRATCH_TOO_SMALL
     torch.cuda.synchronize()
     assert torch.all(c == 7.0)   # nothing was enqueued
+
+
+def test_noalloc_single_row_exact():
+    # M = 1 runs on the small-M kernel here; A's single row of 3001 elements
+    # (not a multiple of 16 bytes) is read in place, only B is copied
+    M, N, K = 1, 1000, 3001
+    a, b = inputs.make_pair(M, N, K, 23, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), c_ref)
