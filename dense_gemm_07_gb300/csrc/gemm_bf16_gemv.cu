@@ -22,6 +22,7 @@
 //     launches) adds them in range order 0, 1, ..., applies the output step
 //     and writes C, so the result does not depend on timing.
 // Every mbarrier wait is bounded as in the tensor-core kernels.
+#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -229,7 +230,7 @@ size_t gemv_smem_bytes() {
   return 1024 + static_cast<size_t>(STAGES) * STAGE_STRIDE + sizeof(GemvControl);
 }
 
-int g_gemv_attr[64];
+std::atomic<int> g_gemv_attr[64];
 
 }  // namespace
 
@@ -258,13 +259,13 @@ cudaError_t launch_gemm_bf16_gemv(const CUtensorMap& tmA, const CUtensorMap& tmB
   if (ranges < 1 || (ranges > 1 && (ws == nullptr || counters == nullptr)))
     return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes();
-  if (!g_gemv_attr[dev]) {
+  if (!g_gemv_attr[dev].load()) {
     for (auto k : {gemm_bf16_gemv_kernel<false>, gemm_bf16_gemv_kernel<true>}) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    g_gemv_attr[dev] = 1;
+    g_gemv_attr[dev].store(1);
   }
   const int blocks = (N + COLS - 1) / COLS;
   auto kernel = epi.act == kActGelu ? gemm_bf16_gemv_kernel<true> : gemm_bf16_gemv_kernel<false>;
