@@ -390,6 +390,28 @@ def test_leading_dims_and_misaligned_bases(kind):
         assert g7.abi.PATHS[p.path] == "bf16_packed" and p.pack_a and p.pack_b
 
 
+@pytest.mark.parametrize("a_off,b_off", [(1, 0), (0, 3), (8, 8)])
+def test_bf16_vector_times_matrix_misaligned_bases(a_off, b_off):
+    # M = 1 with A and/or B at element offsets: a base off 16 bytes is
+    # copied first; an aligned A with any stride is read in place
+    M, N, K = 1, 2000, 1000
+    a, b = inputs.make_pair(M, N, K, 14, inputs.INT3, dtype=torch.bfloat16)
+    a_buf = torch.zeros((M, K + 16), dtype=a.dtype, device=DEV)
+    b_buf = torch.zeros((K, N + 16), dtype=b.dtype, device=DEV)
+    a_buf[:, a_off:K + a_off] = a.to(DEV)
+    b_buf[:, b_off:N + b_off] = b.to(DEV)
+    a_v, b_v = a_buf[:, a_off:K + a_off], b_buf[:, b_off:N + b_off]
+    s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
+                   b_v.data_ptr(), b_v.stride(0), 16, N)
+    assert g7.abi.PATHS[p.path] == "bf16_gemv"
+    assert (p.pack_a, p.pack_b) == (a_off % 8 != 0, b_off % 8 != 0)
+    c = g7.gemm_bf16_f32acc(a_v, b_v)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
+
+
 @pytest.mark.parametrize("kind", ["f32", "bf16"])
 def test_deterministic_bits(kind):
     a, b = inputs.make_pair(512, 768, 1000, 13, inputs.NORMAL, dtype=_dtype(kind))
