@@ -20,11 +20,11 @@
 //     out-of-range elements (the ": 0.0f" of the guarded tiled kernel); one
 //     barrier per slice;
 //   * stores are guarded on both row < M and col < N;
-//   * wave tail: tiles are launched in whole waves of resident blocks; the
-//     tiles of a last, partial wave are split along K (split-K, "A06",
-//     section 3) into ranges computed by separate blocks, whose partial sums
-//     are added in a fixed order by the last block to finish, so the tail
-//     keeps every SM busy and results stay deterministic.
+//   * wave tail: tiles fill whole waves of resident blocks; the tiles of a
+//     last, partial wave are split along K (split-K, "A06", section 3) into
+//     ranges computed by separate blocks of the same launch, whose partial
+//     sums are added in a fixed order by the last block to finish, so the
+//     tail keeps every SM busy and results stay deterministic.
 //
 // Thread layout: 8 warps as 4 (M) x 2 (N), each warp a 32 x 64 sub-tile;
 // lane (ly = lane/8, lx = lane%8) owns rows {4ly..4ly+3, 16+4ly..16+4ly+3}
@@ -241,13 +241,15 @@ __device__ __noinline__ void reduce_ranges(const float* tile_ws, int split,
   }
 }
 
-// One launch computes tiles first .. first + gridDim.x / split - 1 of the
-// grouped order; with split > 1 each tile's k-slices are cut into `split`
-// contiguous ranges, one per block (split-K), block b taking range b % split
-// of tile first + b / split.  A split tile's partial sums go to `ws`
-// (split x 128 x 128 floats per tile); the last of its blocks to finish (per
-// `counters`, zero at launch) adds the partials in range order 0, 1, ... and
-// writes C, so the result does not depend on which block finishes last.
+// One launch computes every tile of the grouped order: blocks 0 .. first - 1
+// compute tiles 0 .. first - 1 whole; the blocks after them cut each of the
+// following tiles' k-slices into `split` contiguous ranges (split-K), block
+// first + b taking range b % split of tile first + b / split.  Blocks are
+// dispatched in index order, so the split blocks fill the SMs as the last
+// whole wave drains.  A split tile's partial sums go to `ws` (split x 128 x
+// 128 floats per tile); the last of its blocks to finish (per `counters`,
+// zero at launch) adds the partials in range order 0, 1, ... and writes C,
+// so the result does not depend on which block finishes last.
 template <bool VEC_B, bool GELU>
 __global__ void __launch_bounds__(THREADS, 2)
 gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
@@ -262,9 +264,14 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   F32Stage<TN>* stage = reinterpret_cast<F32Stage<TN>*>(smem_raw);
   __shared__ int last_block;
 
-  const int local_tile = blockIdx.x / split;
-  const int piece = blockIdx.x % split;
-  const TileCoord tc = tile_order(first + local_tile, tiles_m, tiles_n, kF32Group);
+  // blocks [0, first): whole tiles 0 .. first - 1; then `split` blocks per
+  // tile for tiles first, first + 1, ...
+  const bool split_blk = static_cast<int>(blockIdx.x) >= first;
+  const int bx = static_cast<int>(blockIdx.x) - (split_blk ? first : 0);
+  const int sp = split_blk ? split : 1;
+  const int local_tile = bx / sp;
+  const int piece = bx % sp;
+  const TileCoord tc = tile_order((split_blk ? first : 0) + local_tile, tiles_m, tiles_n, kF32Group);
   const int m0 = tc.m * BM;
   const int n0 = tc.n * BN;
   const int tid = threadIdx.x;
@@ -281,8 +288,8 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
     for (int j = 0; j < JP; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
   const int nk_all = (K + BK - 1) / BK;
-  const int kt_begin = static_cast<int>(static_cast<int64_t>(nk_all) * piece / split);
-  const int kt_end = static_cast<int>(static_cast<int64_t>(nk_all) * (piece + 1) / split);
+  const int kt_begin = static_cast<int>(static_cast<int64_t>(nk_all) * piece / sp);
+  const int kt_end = static_cast<int>(static_cast<int64_t>(nk_all) * (piece + 1) / sp);
   const int nk = kt_end - kt_begin;
   SliceLoader<TN, VEC_B> loader(A, lda, B, ldb, M, N, K, m0, n0, kt_begin, tid);
   const uint32_t stage0 = smem_addr(stage);
@@ -324,7 +331,7 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   }
   cp_async_wait<0>();
 
-  if (split > 1) {
+  if (sp > 1) {
     // Park this range's partial tile, then count the tile's finished ranges.
     float* tile_ws = ws + static_cast<int64_t>(local_tile) * split * (BM * BN);
     float* mine = tile_ws + piece * (BM * BN);
@@ -625,8 +632,8 @@ F32Plan f32_plan(int M, int N, int K, int64_t slots) {
   return p;
 }
 
-// Whole waves of tiles first; then the tiles of the last, partial wave,
-// split along K as planned (two launches on the stream).
+// Whole waves of tiles first, then the tiles of the last, partial wave split
+// along K as planned, all in one launch.
 cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             const float* B, int64_t ldb, float* C, int64_t ldc,
                             bool vec_b, bool vec_c, const F32Plan& p, float* ws,
@@ -646,22 +653,14 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
     note_launches(1);
     return cudaGetLastError();
   }
-  if (p.full > 0) {
-    e = vec_b ? launch_part<true>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
-                                  p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
-                                  nullptr, epi, stream)
-              : launch_part<false>(p.full, M, N, K, A, lda, B, ldb, C, ldc,
-                                   p.tiles_m, p.tiles_n, 0, 1, vc, nullptr,
-                                   nullptr, epi, stream);
-    if (e != cudaSuccess) return e;
-  }
-  if (p.tail > 0) {
-    const int blocks = p.tail * p.split;
+  {
+    const int blocks = p.full + p.tail * (p.tail > 0 ? p.split : 1);
+    const int sp = p.tail > 0 ? p.split : 1;
     e = vec_b ? launch_part<true>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
-                                  p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
+                                  p.tiles_m, p.tiles_n, p.full, sp, vc, ws,
                                   counters, epi, stream)
               : launch_part<false>(blocks, M, N, K, A, lda, B, ldb, C, ldc,
-                                   p.tiles_m, p.tiles_n, p.full, p.split, vc, ws,
+                                   p.tiles_m, p.tiles_n, p.full, sp, vc, ws,
                                    counters, epi, stream);
   }
   return e;
