@@ -105,6 +105,9 @@ gemm_bf16_gemv_kernel(const __grid_constant__ CUtensorMap tmA,
   const int g_end = static_cast<int>(static_cast<int64_t>(groups) * (rg + 1) / ranges);
   const int num_g = g_end - g_begin;
   const int pre = num_g < STAGES ? num_g : STAGES;
+  // Test fault (gemm_debug_inject mode 1): the first stage is never copied,
+  // so the consumers' wait for it runs out and the block unwinds.
+  const bool skip_first = status[1] == 1u;
 
   if (tid == CONSUMERS) {
     for (int s = 0; s < STAGES; ++s) {
@@ -117,7 +120,8 @@ gemm_bf16_gemv_kernel(const __grid_constant__ CUtensorMap tmA,
     tma_prefetch_desc(&tmB);
     // The ring is empty: its first stages go out at once.
     for (int i = 0; i < pre; ++i)
-      issue_stage(smem, ctl->full, i, &tmA, &tmB, n0, (g_begin + i) * ROWS);
+      if (!(skip_first && i == 0))
+        issue_stage(smem, ctl->full, i, &tmA, &tmB, n0, (g_begin + i) * ROWS);
   }
   __syncthreads();
   const uint64_t tmo = wait_limit_ns(status);
@@ -129,7 +133,7 @@ gemm_bf16_gemv_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = pre % STAGES;
       uint32_t phase = pre == STAGES ? 1u : 0u;
       int last_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = s < pre ? 0 : -1;
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = s < pre && !(skip_first && s == 0) ? 0 : -1;
       for (int g = pre; g < num_g; ++g) {
         if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort, tmo)) {
           raise_abort(abort, status);

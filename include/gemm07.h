@@ -239,10 +239,11 @@ GEMM07_API gemm_status_t gemm_get_device_status(void *stream);
  *   wait_ns: limit of every bounded wait inside the tensor-core kernels
  *            (0 restores the default of 2 s).
  *   mode 0:  normal operation.
- *   mode 1:  BF16 GEMMs on the paired-SM path withhold the copy of their
- *            first k-slice, so a bounded wait runs out: the kernels unwind,
- *            return, and gemm_get_device_status() reports GEMM_ERR_TIMEOUT
- *            (C is then incomplete).  Nothing faults, traps or hangs.
+ *   mode 1:  BF16 GEMMs on the paired-SM path and with M == 1 withhold the
+ *            copy of their first k-slice (first stage), so a bounded wait
+ *            runs out: the kernels unwind, return, and
+ *            gemm_get_device_status() reports GEMM_ERR_TIMEOUT (C is then
+ *            incomplete).  Nothing faults, traps or hangs.
  * Returns GEMM_ERR_INVALID_ARG for an unknown mode.  Not for production use.
  */
 GEMM07_API gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns);
