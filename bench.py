@@ -12,6 +12,15 @@ events.  Each GEMM is timed with CUDA events on the stream it is launched on;
 ms_per_step is the sum of the two kernels' event times, value = FLOPs of the
 step / ms_per_step.
 
+After the timed region:
+  * "parity": every element of the last timed step's two outputs, and of the
+    host-buffer calls' outputs, against the FP64 oracle on the same inputs
+    (max of |C - C_ref| / (rtol*S + atol); at most 1 passes).  The oracle run
+    is timed as well and reported as "cpu_baseline";
+  * "configs": the other workload configurations (FP32 256^3, the
+    linear-layer shapes, boundary and skinny shapes), one call each under the
+    same protocol, with their roofline fractions.
+
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
 """
@@ -51,6 +60,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-ladder", action="store_true")
+    p.add_argument("--no-configs", action="store_true")
+    p.add_argument("--config-reps", type=int, default=20)
     return p.parse_args()
 
 
@@ -171,9 +182,11 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def cpu_sample_baseline(rows_each=4096):
-    """The oracle as it stands, on the first `rows_each` rows of each of the
-    step's two GEMMs (same seeded inputs), on this host's cores."""
+def oracle_products():
+    """The oracle as it stands on both GEMMs of the step (same seeded inputs,
+    all 4096 rows), timed on this host's cores.  It returns C and S =
+    sum_k |A_ik B_kj| for each GEMM: the products the timed outputs are
+    compared with element by element, and the CPU baseline."""
     import oracle
     from dense_gemm_07_gb300 import inputs
     import torch
@@ -181,18 +194,100 @@ def cpu_sample_baseline(rows_each=4096):
     oracle.build()
     a16, b16 = inputs.make_pair(SIZE, SIZE, SIZE, 2, inputs.NORMAL, dtype=torch.bfloat16)
     a32, b32 = inputs.make_pair(SIZE, SIZE, SIZE, 1, inputs.UNIFORM, dtype=torch.float32)
-    a16b, b16b = inputs.bf16_bits(a16[:rows_each].contiguous()), inputs.bf16_bits(b16)
-    a32n, b32n = a32[:rows_each].contiguous().numpy(), b32.numpy()
+    a16b, b16b = inputs.bf16_bits(a16), inputs.bf16_bits(b16)
+    a32n, b32n = a32.numpy(), b32.numpy()
     t0 = time.perf_counter()
-    oracle.gemm_bf16(a16b, b16b)
-    oracle.gemm_f32(a32n, b32n)
+    ref16 = oracle.gemm_bf16(a16b, b16b, with_abs=True)
+    ref32 = oracle.gemm_f32(a32n, b32n, with_abs=True)
     dt = time.perf_counter() - t0
-    flops = 2 * 2.0 * rows_each * SIZE * SIZE
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
-            "kind": "oracle", "seconds": dt,
-            "sample": (f"first {rows_each} of 4096 rows of both step GEMMs "
-                       f"(BF16 4096^3 and FP32 4096^3), FP64 triple loop, "
-                       f"OpenMP over rows")}
+    flops = 2 * 2.0 * SIZE * SIZE * SIZE
+    cpu = {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+           "kind": "oracle", "seconds": dt,
+           "sample": ("all 4096 rows of both step GEMMs (BF16 4096^3 and FP32 "
+                      "4096^3): FP64 triple loop, OpenMP over rows, computing C "
+                      "and S = sum|a*b| (the error scale); value counts 2MNK "
+                      "per GEMM")}
+    # The small configuration (FP32 256^3, U[-1,1), seed 0) on one thread.
+    a1, b1 = inputs.make_pair(256, 256, 256, 0, inputs.UNIFORM, dtype=torch.float32)
+    threads = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.gemm_f32(a1.numpy(), b1.numpy())
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(threads)
+    cpu["fp32_256_single_thread"] = {"seconds": dt1,
+                                     "gflops": 2.0 * 256 ** 3 / dt1 / 1e9,
+                                     "cores": 1}
+    return {"bf16": ref16, "f32": ref32}, cpu
+
+
+# Elementwise acceptance bound |C - C_ref| <= RTOL * S + ATOL, S = sum_k
+# |A_ik B_kj| (FP32 path 1e-5 / 1e-7; BF16 inputs with FP32 accumulation
+# 4e-3 / 1e-6, the oracle run on the BF16-rounded inputs).
+PARITY_TOL = {"bf16": (4e-3, 1e-6), "f32": (1e-5, 1e-7)}
+
+
+def parity_ratio(kind, c_gpu, ref):
+    """max over all elements of |C - C_ref| / (rtol * S + atol); <= 1 passes.
+    A non-finite output counts as infinitely far."""
+    import numpy as np
+
+    c_ref, s_ref = ref
+    rtol, atol = PARITY_TOL[kind]
+    c = np.asarray(c_gpu, dtype=np.float64)
+    if c.shape != c_ref.shape or not np.all(np.isfinite(c)):
+        return float("inf")
+    return float(np.max(np.abs(c - c_ref) / (rtol * s_ref + atol)))
+
+
+def config_figures(g7, roofline, peaks, sms, reps=20):
+    """Time the other workload configurations of the pages (one call each,
+    the same protocol as the 4096^3 step: L2 flushed before every call, CUDA
+    events on the calling stream), with TFLOP/s, GB/s of the algorithmic
+    minimum bytes and the fraction of min(peak, intensity x HBM)."""
+    import torch
+    from dense_gemm_07_gb300 import config_table, inputs
+
+    want = {("C1a", 256, 256, 256), ("C1b", 256, 256, 256),
+            ("C2", 4096, 4096, 4096), ("C3", 4096, 4096, 4096),
+            ("C4", 2048, 4096, 4096), ("C4", 2048, 11008, 4096),
+            ("C4", 2048, 4096, 11008),
+            ("C5a", 127, 127, 127), ("C5a", 1000, 1000, 1000),
+            ("C5a", 3001, 3001, 3001), ("C5a", 3001, 3001, 127),
+            ("C5b", 1, 4096, 4096), ("C5c", 16, 4096, 4096)}
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    fp32_peak = roofline.fp32_simt_peak(sms, float(peaks.get("sm_max_mhz", 2070.0))) / 1e12
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = []
+    for name, kind, (M, N, K), dist, dist_b, seed in config_table.configs():
+        if (name, M, N, K) not in want:
+            continue
+        dtype = torch.float32 if kind == "f32" else torch.bfloat16
+        x, y = inputs.make_pair(M, N, K, seed, dist, dist_b, dtype=dtype)
+        X, Y = x.to(dev), y.to(dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
+        mean, best = config_table.time_call(lambda: fn(X, Y, out=C), reps, flush)
+        eb = 4 if kind == "f32" else 2
+        flops = roofline.gemm_flops(M, N, K)
+        nbytes = roofline.min_bytes(M, N, K, eb, 4)
+        peak = fp32_peak if kind == "f32" else bf16_peak
+        roof_tf = min(peak, roofline.intensity(M, N, K, eb, 4) * hbm / 1e3)
+        hbm_bound = roof_tf < peak
+        tf = flops / (mean * 1e-6) / 1e12
+        e = {"cfg": name, "kind": kind, "M": M, "N": N, "K": K, "us": mean,
+             "us_best": best, "tflops": tf, "gbs": nbytes / (mean * 1e-6) / 1e9,
+             "bound": "hbm" if hbm_bound else ("alu" if kind == "f32" else "tensor"),
+             "roofline_tflops": roof_tf, "frac": tf / roof_tf}
+        out.append(e)
+    return {"reps": reps, "timing": "CUDA events around one call, L2 flushed "
+            "(256 MiB write) before each, queued behind a short spin; mean of "
+            "reps (us), TFLOP/s and GB/s of algorithmic bytes from the mean",
+            "entries": out}
 
 
 def ladder_context(g7, roofline, A32, B32, C32, flush, stream, sms, sm_mhz, hbm_gbs):
@@ -379,6 +474,8 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     status = g7.gemm_get_device_status()
+    # the last timed step's outputs, for the comparison with the oracle
+    c16_out, c32_out = C16.cpu().numpy(), C32.cpu().numpy()
 
     t_bf16 = [e[0].elapsed_time(e[1]) for e in events]   # ms
     t_f32 = [e[2].elapsed_time(e[3]) for e in events]
@@ -412,6 +509,7 @@ def main():
 
     # End to end through the host-buffer C-ABI entry points.
     e2e = None
+    e2e_out = None
     if args.e2e_steps > 0:
         h_a16, h_b16 = a16.pin_memory(), b16.pin_memory()
         h_a32, h_b32 = a32.pin_memory(), b32.pin_memory()
@@ -431,6 +529,7 @@ def main():
         e2e_s = replicas.max_over_ranks([e2e_s], dev)[0]
         h2d = (h_a16.numel() + h_b16.numel()) * 2 + (h_a32.numel() + h_b32.numel()) * 4
         d2h = (h_c16.numel() + h_c32.numel()) * 4
+        e2e_out = (h_c16.numpy().copy(), h_c32.numpy().copy())
         e2e = {"value": replicas.whole_job_rate(world, 2 * flops_one, e2e_s) / 1e12,
                "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -442,9 +541,30 @@ def main():
         ladder = ladder_context(g7, roofline, A32, B32, C32, flush, stream, sms,
                                 sm_max, hbm)
 
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = config_figures(g7, roofline, peaks, sms, reps=args.config_reps)
+
+    # Every element of both timed outputs (and of the host-buffer calls'
+    # outputs) against the FP64 oracle on the same inputs; the oracle run is
+    # also the CPU baseline.
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_sample_baseline()
+    parity = None
+    if rank == 0:
+        refs, cpu_run = oracle_products()
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_run
+        parity = {"bf16": parity_ratio("bf16", c16_out, refs["bf16"]),
+                  "f32": parity_ratio("f32", c32_out, refs["f32"])}
+        if e2e_out is not None:
+            parity["e2e_bf16"] = parity_ratio("bf16", e2e_out[0], refs["bf16"])
+            parity["e2e_f32"] = parity_ratio("f32", e2e_out[1], refs["f32"])
+        parity.update({
+            "rows": SIZE, "elements_per_output": SIZE * SIZE,
+            "ok": all(v <= 1.0 for v in parity.values()),
+            "measure": "max over every element of |C - C_ref| / (rtol*S + atol), "
+                       "S = sum|a*b|; bf16 rtol 4e-3 atol 1e-6, f32 rtol 1e-5 "
+                       "atol 1e-7; <= 1 passes"})
 
     if rank == 0:
         line = {
@@ -459,6 +579,8 @@ def main():
             },
             "roofline": dominant,
             "cpu_baseline": cpu,
+            "parity": parity,
+            "configs": configs,
             "ladder_fp32_4096": ladder,
             "e2e": e2e,
             "gpu_launches": launches,

@@ -17,12 +17,13 @@ _lock = threading.Lock()
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = 1
-GEMM_ERR_UNSUPPORTED_DEVICE = 2
-GEMM_ERR_LAUNCH = 3
-GEMM_ERR_TIMEOUT = 4
-GEMM_ERR_NO_MEMORY = 5
+GEMM_ERR_MISALIGNED = 2          # reserved, never returned
+GEMM_ERR_UNSUPPORTED_DEVICE = 3
+GEMM_ERR_LAUNCH = 4
+GEMM_ERR_TIMEOUT = 5
 GEMM_ERR_INTERNAL = 6
-GEMM_ERR_SCRATCH_TOO_SMALL = 7
+GEMM_ERR_NO_MEMORY = 7
+GEMM_ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 PATHS = {0: "none", 1: "zero_fill", 2: "f32_simt", 3: "bf16_tma",

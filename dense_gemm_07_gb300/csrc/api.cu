@@ -239,22 +239,19 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   }
   // 256 x 256 tiles on SM pairs (the work sharing is reported for the 76
   // pairs of a 152-SM GB300; launches use the device's resident count).
-  const bool pair = M > kTcTileM;
-  p->tile_m = pair ? kPairTileM : kTcTileM;
-  p->tile_n = pair ? kPairTileN : kTcTileN;
-  p->tile_k = pair ? kPairTileK : kTcTileK;
-  p->stages = pair ? kPairStages : kTcStages;
+  p->tile_m = kPairTileM;
+  p->tile_n = kPairTileN;
+  p->tile_k = kPairTileK;
+  p->stages = kPairStages;
   p->tiles = ((M + p->tile_m - 1) / p->tile_m) * ((N + p->tile_n - 1) / p->tile_n);
   if (p->tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
-  if (pair) {
-    const PairSchedule ps =
-        pair_schedule(M, N, K, 76, g_schedule.load(), tma_store_ok(C, N, ldc));
-    p->dp_tiles = ps.dp_tiles;
-    p->sk_tiles = ps.sk_tiles;
-    p->sk_pairs = ps.sk_pairs;
-    p->pairs = ps.pairs;
-    p->workspace_bytes += sk_bytes(ps);
-  }
+  const PairSchedule ps =
+      pair_schedule(M, N, K, 76, g_schedule.load(), tma_store_ok(C, N, ldc));
+  p->dp_tiles = ps.dp_tiles;
+  p->sk_tiles = ps.sk_tiles;
+  p->sk_pairs = ps.sk_pairs;
+  p->pairs = ps.pairs;
+  p->workspace_bytes += sk_bytes(ps);
   return GEMM_OK;
 }
 
@@ -641,8 +638,11 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   const int m = static_cast<int>(M), n = static_cast<int>(N),
             k = static_cast<int>(K);
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
-  const int max_pairs =
-      !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
+  const bool paired = !skinny && plan.path != GEMM_PATH_BF16_GEMV;
+  const int max_pairs = paired ? pair_max_active(stream) : 0;
+  // The paired-SM kernel is the only kernel for M > 128: a device on which
+  // no pair of its CTAs can be resident cannot run this GEMM.
+  if (paired && max_pairs <= 0) return GEMM_ERR_LAUNCH;
   PairSchedule ps;
   if (max_pairs > 0)
     ps = pair_schedule(M, N, K, max_pairs, g_schedule.load(),
@@ -690,21 +690,12 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                                           skinny_split_resident(m, n, k, d->sms), d->status,
                                           epi, stream));
   } else if (s == GEMM_OK) {
-    const bool vec_c = aligned16(C) && ldc % 4 == 0;
-    if (max_pairs > 0) {
-      CUtensorMap tmC;
-      const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
-      const unsigned long long tag = ps.sk_tiles > 0 ? next_launch_tag(d) : 0;
-      s = from_cuda(launch_gemm_bf16_pair(
-          tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
-          ldc, m, n, ps, sk_sync, tag, d->status, epi, stream));
-    } else {
-      const int64_t tiles = ((M + kTcTileM - 1) / kTcTileM) *
-                            ((N + kTcTileN - 1) / kTcTileN);
-      const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
-      s = from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
-                                        d->status, epi, stream));
-    }
+    CUtensorMap tmC;
+    const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
+    const unsigned long long tag = ps.sk_tiles > 0 ? next_launch_tag(d) : 0;
+    s = from_cuda(launch_gemm_bf16_pair(
+        tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
+        ldc, m, n, ps, sk_sync, tag, d->status, epi, stream));
   }
   if (owned) pool_free(ws, stream);
   if (sk_owned) pool_free(sk, stream);
@@ -968,8 +959,8 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   // counters, which the shared fixed scratch could not keep zero.
   const bool skinny =
       plan.path == GEMM_PATH_BF16_SKINNY || plan.path == GEMM_PATH_BF16_GEMV;
-  const int max_pairs =
-      !skinny && plan.tile_m == kPairTileM ? pair_max_active(stream) : 0;
+  const int max_pairs = skinny ? 0 : pair_max_active(stream);
+  if (!skinny && max_pairs <= 0) return GEMM_ERR_LAUNCH;
   if (s == GEMM_OK)
     s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
                           skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
@@ -978,36 +969,28 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
     return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                              skinny_split_resident(m, n, k, d->sms),
                                              d->status, epi_identity(), stream));
-  const bool vec_c = aligned16(C) && ldc % 4 == 0;
-  if (max_pairs > 0) {
-    // Stream-K only when its scratch fits after the packed operands.
-    PairSchedule ps =
-        pair_schedule(M, N, K, max_pairs, g_schedule.load(), tma_store_ok(C, N, ldc));
-    if (pack_ws + sk_bytes(ps) > kNoallocScratchBytes)
-      ps = pair_schedule(M, N, K, max_pairs, kScheduleNoSplitK);
-    float* sk_ws = nullptr;
-    unsigned long long* sk_sync = nullptr;
-    CUtensorMap tmW;
-    unsigned long long tag = 0;
-    if (ps.sk_tiles > 0) {
-      sk_ws = reinterpret_cast<float*>(d->scratch + pack_ws);
-      sk_sync = reinterpret_cast<unsigned long long*>(
-          d->scratch + pack_ws + round_up(sk_partial_bytes(ps), 256));
-      s = make_map_partials(&tmW, sk_ws, ps);
-      if (s != GEMM_OK) return s;
-      tag = next_noalloc_tag(d);
-    }
-    CUtensorMap tmC;
-    const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
-    return from_cuda(launch_gemm_bf16_pair(
-        tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
-        ldc, m, n, ps, sk_sync, tag, d->status, epi_identity(), stream));
+  // Stream-K only when its scratch fits after the packed operands.
+  PairSchedule ps =
+      pair_schedule(M, N, K, max_pairs, g_schedule.load(), tma_store_ok(C, N, ldc));
+  if (pack_ws + sk_bytes(ps) > kNoallocScratchBytes)
+    ps = pair_schedule(M, N, K, max_pairs, kScheduleNoSplitK);
+  float* sk_ws = nullptr;
+  unsigned long long* sk_sync = nullptr;
+  CUtensorMap tmW;
+  unsigned long long tag = 0;
+  if (ps.sk_tiles > 0) {
+    sk_ws = reinterpret_cast<float*>(d->scratch + pack_ws);
+    sk_sync = reinterpret_cast<unsigned long long*>(
+        d->scratch + pack_ws + round_up(sk_partial_bytes(ps), 256));
+    s = make_map_partials(&tmW, sk_ws, ps);
+    if (s != GEMM_OK) return s;
+    tag = next_noalloc_tag(d);
   }
-  const int64_t tiles =
-      ((M + kTcTileM - 1) / kTcTileM) * ((N + kTcTileN - 1) / kTcTileN);
-  const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
-  return from_cuda(launch_gemm_bf16_tc(tmA, tmB, C, ldc, m, n, k, vec_c, grid,
-                                       d->status, epi_identity(), stream));
+  CUtensorMap tmC;
+  const bool tma_c = tma_store_ok(C, N, ldc) && make_map_c(&tmC, C, M, N, ldc) == GEMM_OK;
+  return from_cuda(launch_gemm_bf16_pair(
+      tmA, tmB, tma_c ? &tmC : nullptr, ps.sk_tiles > 0 ? &tmW : nullptr, C,
+      ldc, m, n, ps, sk_sync, tag, d->status, epi_identity(), stream));
 }
 
 }  // namespace
@@ -1116,6 +1099,7 @@ const char* gemm_status_string(gemm_status_t status) {
   switch (status) {
     case GEMM_OK: return "success";
     case GEMM_ERR_INVALID_ARG: return "invalid argument (size, leading dimension or pointer)";
+    case GEMM_ERR_MISALIGNED: return "misaligned operand (reserved: not returned by this library)";
     case GEMM_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3 (sm_103a) is current";
     case GEMM_ERR_LAUNCH: return "a CUDA call or kernel launch failed";
     case GEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out; the output is incomplete";
@@ -1168,7 +1152,7 @@ void gemm_shutdown(void) {
   cudaGetLastError();
 }
 
-int gemm_abi_version(void) { return 2; }
+int gemm_abi_version(void) { return 3; }
 
 int gemm_set_bf16_schedule(int schedule) {
   if (schedule < GEMM_SCHEDULE_AUTO || schedule > GEMM_SCHEDULE_COLUMN_SPLIT)

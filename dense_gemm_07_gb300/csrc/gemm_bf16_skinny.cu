@@ -107,6 +107,10 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
   const int kb_begin = static_cast<int>(static_cast<int64_t>(num_kb_total) * rank / cs);
   const int kb_end = static_cast<int>(static_cast<int64_t>(num_kb_total) * (rank + 1) / cs);
   const int num_kb = kb_end - kb_begin;
+  // Test fault (gemm_debug_inject mode 1): no CTA copies its first stage,
+  // so the MMA issuer's wait for it runs out; every role unwinds and the
+  // cluster still meets at its final barrier.
+  const bool skip_first = status[1] == 1u;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -123,7 +127,9 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
     // copies go out now, while tensor memory is allocated and the block
     // meets (the barriers were initialised by this thread).
     const int pre = num_kb < STAGES ? num_kb : STAGES;
-    for (int i = 0; i < pre; ++i) issue_stage<NM>(smem, ctl->full, i, &tmA, &tmB, n0, kb_begin + i);
+    for (int i = 0; i < pre; ++i)
+      if (!(skip_first && i == 0))
+        issue_stage<NM>(smem, ctl->full, i, &tmA, &tmB, n0, kb_begin + i);
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, S::TMEM_COLS);
@@ -143,7 +149,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = pre % STAGES;
       uint32_t phase = pre == STAGES ? 1u : 0u;
       int last_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = s < pre ? 0 : -1;
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = s < pre && !(skip_first && s == 0) ? 0 : -1;
       for (int kb = kb_begin + pre; kb < kb_end; ++kb) {
         if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort, tmo)) {
           raise_abort(abort, status);

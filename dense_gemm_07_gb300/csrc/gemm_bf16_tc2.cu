@@ -1,11 +1,11 @@
 // gemm_bf16_tc2.cu -- BF16 x BF16 -> FP32 GEMM on pairs of SMs.
 //
-// Same method as gemm_bf16_tc.cu (the tensor-core rung of "GEMM, step by
-// step", section "Concept": BF16 inputs, FP32 sums, large tiles, neighbouring
-// blocks on the same rows/columns; multi-stage prefetch as in "GEMM
-// Optimization", section 5), with the output tile grown to 256 x 256 and
-// computed by two SMs together ("Production tensor-core kernels use larger
-// tiles", same section of "GEMM, step by step").
+// The tensor-core rung of "GEMM, step by step" (section "Concept": BF16
+// inputs, FP32 sums, large tiles, neighbouring blocks on the same
+// rows/columns; multi-stage prefetch as in "GEMM Optimization", section 5),
+// with the output tile grown to 256 x 256 and computed by two SMs together
+// ("Production tensor-core kernels use larger tiles", same section of "GEMM,
+// step by step").  This kernel serves every M > 128.
 //
 // Work sharing (stream_k.cuh): whole tiles round-robin over the resident
 // pairs while they fill whole waves.  A last wave that fills at most half of

@@ -47,21 +47,11 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             float* ws, unsigned int* counters,
                             const EpiParams& epi, cudaStream_t stream);
 
-// ---- BF16 tensor-core path (gemm_bf16_tc.cu)
+// ---- BF16 tensor-core path: shared tile constants.  One CTA of a pair
+// stages kTcTileM rows of A per k-slice of kTcTileK; M <= kTcTileM runs on
+// the small-M kernel, larger M on the paired-SM kernel.
 constexpr int kTcTileM = 128;
-constexpr int kTcTileN = 256;
 constexpr int kTcTileK = 64;
-constexpr int kTcStages = 4;
-constexpr int kTcGroup = 8;
-
-size_t tc_smem_bytes();
-
-// A and B described by tensor maps (K-major A box 64 x 128, N-major B box
-// 64 x 64, both 128-byte swizzled).  `grid` persistent CTAs walk the tiles.
-cudaError_t launch_gemm_bf16_tc(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                float* C, int64_t ldc, int M, int N, int K,
-                                bool vec_c, int grid, unsigned int* status,
-                                const EpiParams& epi, cudaStream_t stream);
 
 // ---- BF16 tensor-core path on SM pairs (gemm_bf16_tc2.cu): 256 x 256 tiles
 constexpr int kPairTileM = 256;

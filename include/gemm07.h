@@ -62,12 +62,14 @@ extern "C" {
 typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1,        /* negative size, short ld, null pointer */
-    GEMM_ERR_UNSUPPORTED_DEVICE = 2, /* no device, or not compute capability 10.3 */
-    GEMM_ERR_LAUNCH = 3,             /* a CUDA call or kernel launch failed */
-    GEMM_ERR_TIMEOUT = 4,            /* a device-side bounded wait ran out */
-    GEMM_ERR_NO_MEMORY = 5,          /* workspace or staging allocation failed */
-    GEMM_ERR_INTERNAL = 6,
-    GEMM_ERR_SCRATCH_TOO_SMALL = 7   /* gemm_bf16_f32acc_noalloc: request exceeds its fixed scratch */
+    GEMM_ERR_MISALIGNED = 2,         /* reserved, never returned: any alignment and
+                                        leading dimension is handled internally */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = 4,             /* a CUDA call or kernel launch failed */
+    GEMM_ERR_TIMEOUT = 5,            /* a device-side bounded wait ran out */
+    GEMM_ERR_INTERNAL = 6,           /* tensor-map encoding rejected a layout */
+    GEMM_ERR_NO_MEMORY = 7,          /* workspace or staging allocation failed */
+    GEMM_ERR_SCRATCH_TOO_SMALL = 8   /* gemm_bf16_f32acc_noalloc: request exceeds its fixed scratch */
 } gemm_status_t;
 
 /*
@@ -158,17 +160,27 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K,
  *   from calling cudaMalloc, and latency-critical loops where an allocation
  *   could synchronise the device or wait on the allocator.  This call never
  *   calls cudaMalloc, cudaFree, a pool or any other allocating routine.
- *   Scratch: when A or B has to be copied to an aligned layout first (base
- *   not 16-byte aligned, or lda/ldb not a multiple of 8), the copies go into
- *   one fixed array of GEMM07_NOALLOC_SCRATCH_BYTES that the library
- *   declares in device memory; every device that loads the library holds it
- *   until the process exits.  A request whose copies need more than that
- *   returns GEMM_ERR_SCRATCH_TOO_SMALL before anything is enqueued (aligned
- *   operands need no scratch and have no such limit).
+ *   Scratch: one fixed array of GEMM07_NOALLOC_SCRATCH_BYTES that the
+ *   library declares in device memory; every device that loads the library
+ *   holds it until the process exits.  A call may put in it, in this order:
+ *     1. the aligned copy of A, when A has to be copied (base not 16-byte
+ *        aligned, or lda not a multiple of 8);
+ *     2. the aligned copy of B, likewise;
+ *     3. for M > 128 when the schedule splits tiles along K over several SM
+ *        pairs (the default schedule does so at 4096 x 4096 x 4096, even
+ *        with aligned operands): the split tiles' partial sums and their
+ *        synchronisation words (tickets, ready and cleared flags).
+ *   A request whose copies (1 and 2) need more than the array returns
+ *   GEMM_ERR_SCRATCH_TOO_SMALL before anything is enqueued; when 3 does not
+ *   fit after them, the call runs without the K split instead.  M = 1 runs
+ *   on the small-M kernel here, which reduces through shared memory and
+ *   puts nothing in the array beyond 1 and 2.
  *   Sharing: every call on a device uses the same array and it keeps the
- *   last call's contents.  Calls whose kernels may overlap on the GPU (on
- *   different streams without ordering between them) race on it: order them
- *   on one stream or with events.
+ *   last call's contents.  ANY two calls whose kernels may overlap on the
+ *   GPU (on different streams without ordering between them) race on it,
+ *   whether or not their operands are aligned: the results can be wrong, or
+ *   a bounded wait can run out and gemm_get_device_status reports
+ *   GEMM_ERR_TIMEOUT.  Order the calls on one stream or with events.
  *   Set-up: the first call on each device looks up the array's device
  *   address (with that device current); later calls reuse it.
  */
@@ -183,8 +195,9 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc_noalloc(int64_t M, int64_t N, int64_t 
  * measuring the ladder of the pages on this GPU (not a production path):
  *   rung 0: one thread per output, coalesced mapping ("How a Matrix Multiply
  *           Runs on a GPU", "Level 0"), 0.25 FLOP/byte;
- *   rung 1: 32 x 32 shared-memory tiles, two barriers per tile, zero-filled
- *           edges ("Level 1"; "A06", section 3), 8 FLOP/byte;
+ *   rung 1: 32 x 32 shared-memory tiles, one output per thread, zero-filled
+ *           edges ("Level 1"; "A06", section 3), 8 FLOP/byte; double
+ *           buffered with one barrier per tile;
  *   rung 2: one-dimensional register tiling, 8 outputs per thread in one
  *           column ("GEMM" (inference-book), 1D register tiling).
  * Same operands, conventions and errors as gemm_f32; rung outside 0..2 or
@@ -239,9 +252,10 @@ GEMM07_API gemm_status_t gemm_get_device_status(void *stream);
  *   wait_ns: limit of every bounded wait inside the tensor-core kernels
  *            (0 restores the default of 2 s).
  *   mode 0:  normal operation.
- *   mode 1:  BF16 GEMMs on the paired-SM path and with M == 1 withhold the
- *            copy of their first k-slice (first stage), so a bounded wait
- *            runs out: the kernels unwind, return, and
+ *   mode 1:  BF16 GEMMs (paired-SM path, small-M cluster path and
+ *            M == 1) withhold the copy of their first k-slice (first
+ *            stage), so a bounded wait runs out: the kernels unwind, return,
+ *            and
  *            gemm_get_device_status() reports GEMM_ERR_TIMEOUT (C is then
  *            incomplete).  Nothing faults, traps or hangs.
  * Returns GEMM_ERR_INVALID_ARG for an unknown mode.  Not for production use.
@@ -251,7 +265,9 @@ GEMM07_API gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns);
 /* Releases per-device state held by the library (pools, status words). */
 GEMM07_API void gemm_shutdown(void);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 3 (status codes numbered as in the boundary
+ * definition: MISALIGNED = 2 reserved, UNSUPPORTED_DEVICE = 3, LAUNCH = 4,
+ * TIMEOUT = 5, INTERNAL = 6; NO_MEMORY = 7 and SCRATCH_TOO_SMALL = 8 added). */
 GEMM07_API int gemm_abi_version(void);
 
 /*

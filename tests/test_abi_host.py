@@ -44,12 +44,20 @@ def test_library_is_in_tree_and_for_sm103a():
 
 
 def test_abi_version(lib):
-    assert _abi.gemm_abi_version() == 2
+    assert _abi.gemm_abi_version() == 3
+
+
+def test_status_numbering_follows_the_boundary_table():
+    # the codes of the boundary's definition, then this library's additions
+    assert (_abi.GEMM_OK, _abi.GEMM_ERR_INVALID_ARG, _abi.GEMM_ERR_MISALIGNED,
+            _abi.GEMM_ERR_UNSUPPORTED_DEVICE, _abi.GEMM_ERR_LAUNCH,
+            _abi.GEMM_ERR_TIMEOUT, _abi.GEMM_ERR_INTERNAL) == (0, 1, 2, 3, 4, 5, 6)
+    assert (_abi.GEMM_ERR_NO_MEMORY, _abi.GEMM_ERR_SCRATCH_TOO_SMALL) == (7, 8)
 
 
 def test_status_strings(lib):
     seen = set()
-    for code in range(8):
+    for code in range(9):
         s = _abi.gemm_status_string(code)
         assert s and s not in seen
         seen.add(s)

@@ -1,7 +1,8 @@
 """Large sizes: outputs with more than 2^31 elements (64-bit element
 offsets in every store path) and very long K (k-slice indices and copy
-coordinates far from zero), compared with the oracle on sampled rows or with
-an exact closed form."""
+coordinates far from zero), compared with the oracle on sampled rows plus
+exact row and column sums over every element, or with an exact closed
+form."""
 import numpy as np
 import pytest
 import torch
@@ -28,7 +29,15 @@ def test_output_beyond_2_31_elements(kind):
     rows = np.array([0, 1, 127, 128, 35000, 67107, 67108, 67109, 68000, 69887,
                      69888, 69999])
     got = c[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    # Every element, through two properties of the exact product that hold at
+    # any size: its row sums equal A (B 1) and its column sums (1^T A) B.  The
+    # inputs are small integers, so every sum below is exact in FP64.
+    row_sums = c.sum(dim=1, dtype=torch.float64).cpu().numpy()
+    col_sums = c.sum(dim=0, dtype=torch.float64).cpu().numpy()
     del c
+    a64, b64 = a.to(torch.float64).numpy(), b.to(torch.float64).numpy()
+    assert np.array_equal(row_sums, a64 @ b64.sum(axis=1)), "row sums of C differ"
+    assert np.array_equal(col_sums, a64.sum(axis=0) @ b64), "column sums of C differ"
     c_ref, _ = oracle_ref(kind, a, b, rows=rows, with_abs=False)
     assert_within(kind, got, c_ref, None, exact=True, what=f"{kind} {M}x{N}x{K}")
 

@@ -8,10 +8,12 @@ allocation could synchronise the device.  For them the library offers one
 entry point whose operand copies go into a fixed scratch array declared in
 device memory instead of a memory pool.
 
-These tests call it through the C ABI and compare it with the ordinary
-(pool-using) entry point on shapes that need the copies, twice in a row, so
-that the second call runs on scratch left over from the first.  The file is
-named so that pytest collects it last.
+These tests call it through the C ABI, twice in a row on each input (the
+second call runs on scratch left over from the first), and check every
+element of each output against the FP64 oracle -- exactly on integer inputs,
+within the BF16 bound otherwise -- and against the ordinary (pool-using)
+entry point, within the same bound (bit for bit where both run the same
+schedule).  The file is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
@@ -51,7 +53,30 @@ CASES = [(300, 520, 333, 21, inputs.INT3, True),
          (257, 300, 200, 22, inputs.NORMAL, False)]
 
 
-def test_noalloc_matches_pooled_entry_point_two_calls_in_a_row():
+def _against_oracle_and_pooled(a, b, a_d, b_d, exact, what):
+    """Two no-allocation calls in a row, each compared in full with the
+    oracle and with the pooled entry point."""
+    M, K = a.shape
+    N = b.shape[1]
+    c_ref, s_ref = oracle_ref("bf16", a, b, with_abs=not exact)
+    pooled = g7.gemm_bf16_f32acc(a_d, b_d).cpu().numpy()
+    for call in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
+        torch.cuda.synchronize()
+        assert g7.gemm_get_device_status() == 0
+        got = out.cpu().numpy()
+        assert_within("bf16", got, c_ref, s_ref, exact=exact,
+                      what=f"{what}, call {call + 1} against the oracle")
+        if exact:
+            assert np.array_equal(got, pooled), f"{what}: differs from the pooled call"
+        else:
+            # the same bound, taken around the pooled entry point's output
+            assert_within("bf16", got, pooled.astype(np.float64), s_ref,
+                          what=f"{what}, call {call + 1} against the pooled call")
+
+
+def test_noalloc_copied_operands_two_calls_in_a_row():
     for (M, N, K, seed, dist, exact) in CASES:
         a, b = inputs.make_pair(M, N, K, seed, dist, dtype=torch.bfloat16)
         if exact:
@@ -61,41 +86,35 @@ def test_noalloc_matches_pooled_entry_point_two_calls_in_a_row():
         s, plan = g7.plan("bf16", M, N, K, a_d.data_ptr(), a_d.stride(0),
                           b_d.data_ptr(), b_d.stride(0), 16, N)
         assert s == 0 and plan.pack_a == 1, "case must exercise the scratch copies"
-        ref = g7.gemm_bf16_f32acc(a_d, b_d)
-        out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
-        assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
-        torch.cuda.synchronize()
-        assert g7.gemm_get_device_status() == 0
-        got, want = out.cpu().numpy(), ref.cpu().numpy()
-        if exact:
-            assert np.array_equal(got, want)
-        else:
-            _, s_ref = oracle_ref("bf16", a, b)
-            # same bound as the parity tests, measured against the pooled
-            # entry point's output
-            assert_within("bf16", got, want.astype(np.float64), s_ref,
-                          what="noalloc vs pooled entry point")
+        _against_oracle_and_pooled(a, b, a_d, b_d, exact, f"{M}x{N}x{K}")
 
 
-def test_noalloc_stream_k_matches_pooled_bitwise():
+@pytest.mark.parametrize("dist,exact", [(inputs.INT3, True), (inputs.NORMAL, False)])
+def test_noalloc_stream_k_two_calls_in_a_row(dist, exact):
     # 90 tiles shared as k-slice runs by 76 SM pairs: the partial sums
     # and the synchronisation words live in the fixed scratch array too
     M, N, K = 2560, 2304, 1024
-    a, b = inputs.make_pair(M, N, K, 26, inputs.NORMAL, dtype=torch.bfloat16)
+    a, b = inputs.make_pair(M, N, K, 26, dist, dtype=torch.bfloat16)
     a_d, b_d = a.to(DEV), b.to(DEV)
     prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)
     try:
         s, plan = g7.plan("bf16", M, N, K)
         assert s == 0 and plan.sk_tiles > 0
-        ref = g7.gemm_bf16_f32acc(a_d, b_d)
-        for _ in range(2):
-            out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
-            assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
-            torch.cuda.synchronize()
-            assert g7.gemm_get_device_status() == 0
-            assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+        _against_oracle_and_pooled(a, b, a_d, b_d, exact, "stream-K 2560x2304x1024")
     finally:
         _abi.gemm_set_bf16_schedule(prev)
+
+
+def test_noalloc_default_schedule_4096_aligned_operands():
+    # 4096^3 with aligned operands: no copies, but the default schedule halves
+    # the last wave's 28 tiles along K and their cleared flags live in the
+    # array
+    M = N = K = 4096
+    a, b = inputs.make_pair(M, N, K, 2, inputs.NORMAL, dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    s, plan = g7.plan("bf16", M, N, K)
+    assert s == 0 and plan.sk_tiles == 28 and plan.pack_a == 0 and plan.pack_b == 0
+    _against_oracle_and_pooled(a, b, a_d, b_d, False, "4096^3 default schedule")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
