@@ -93,14 +93,14 @@ bool tma_store_ok(const void* C, int64_t N, int64_t ldc) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// M = 1: counters of the column blocks at the start of the scratch block, a
+// M = 1: two counters per column block at the start of the scratch block, a
 // fixed area so that every call finds them zero whatever its size (each
-// launch's last range puts its counter back); partial sums after it.
-// Beyond 16384 column blocks the rows are not split.
+// launch's last range puts them back); partial sums after it.  Beyond 8192
+// column blocks the rows are not split.
 constexpr int64_t kGemvCounterBytes = 65536;
 int gemv_ranges_capped(int64_t N, int64_t K, int sms) {
   const int64_t blocks = (N + kGemvCols - 1) / kGemvCols;
-  if (blocks * 4 > kGemvCounterBytes) return 1;
+  if (blocks * 8 > kGemvCounterBytes) return 1;
   return gemv_ranges(static_cast<int>(N), static_cast<int>(K), sms);
 }
 

@@ -17,10 +17,14 @@
 //     matching elements of x per stage;
 //   * 8 consumer warps each own 4 columns per thread and add x[k] * B[k][n]
 //     in FP32, k increasing (BF16 products are exact in FP32);
-//   * with KS > 1 each range parks its 1024 sums in a workspace; the last
-//     range of a column block to finish (per a counter, zero between
-//     launches) adds them in range order 0, 1, ..., applies the output step
-//     and writes C, so the result does not depend on timing.
+//   * with KS > 1 each range publishes its 1024 sums to a workspace and
+//     counts itself in; the launch is cooperative (all blocks resident), so
+//     each range then waits, bounded, for the other ranges of its column
+//     block and finishes its own 1/KS slice of the columns: it adds that
+//     slice of every range's sums in range order 0, 1, ..., applies the
+//     output step and writes C.  The order is fixed, so the result does not
+//     depend on timing, and the final additions are spread over all KS SMs
+//     instead of one SM reading every range's sums.
 // Every mbarrier wait is bounded as in the tensor-core kernels.
 #include <atomic>
 #include <cstdint>
@@ -47,7 +51,6 @@ struct alignas(8) GemvControl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   int abort;
-  int last;
 };
 
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* status) {
@@ -192,42 +195,59 @@ gemm_bf16_gemv_kernel(const __grid_constant__ CUtensorMap tmA,
     if (tid < CONSUMERS) store_out<GELU>(C, n, N, acc, epi);
     return;
   }
-  // Park this range's sums, then count the column block's finished ranges.
+  // Publish this range's sums, then count the range in.
   if (tid < CONSUMERS)
     __stcg(reinterpret_cast<float4*>(ws + (static_cast<int64_t>(nb) * ranges + rg) * COLS) + tid,
            make_float4(acc[0], acc[1], acc[2], acc[3]));
   __threadfence();
   __syncthreads();
-  if (tid == 0) ctl->last = atomicAdd(&counters[nb], 1u) == static_cast<unsigned>(ranges - 1);
-  __syncthreads();
-  if (!ctl->last) return;
-  __threadfence();
-  if (tid < CONSUMERS) {
-    // The ranges' sums in range order.  Up to 40 loads go out before the
-    // first add (registers are plentiful here), so a column block's 38
-    // ranges at N = 4096 cost one L2 round trip rather than several.
-    constexpr int BATCH = 40;
-    const float4* part =
-        reinterpret_cast<const float4*>(ws + static_cast<int64_t>(nb) * ranges * COLS) + tid;
-    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int q0 = 0; q0 < ranges; q0 += BATCH) {
-      float4 v[BATCH];
-#pragma unroll
-      for (int i = 0; i < BATCH; ++i)
-        v[i] = q0 + i < ranges ? __ldcg(part + (q0 + i) * (COLS / 4))
-                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-      for (int i = 0; i < BATCH; ++i) {
-        sum.x += v[i].x;
-        sum.y += v[i].y;
-        sum.z += v[i].z;
-        sum.w += v[i].w;
-      }
-    }
-    const float v[4] = {sum.x, sum.y, sum.z, sum.w};
-    store_out<GELU>(C, n, N, v, epi);
+  unsigned int* arrived = counters + 2 * nb;
+  unsigned int* departed = arrived + 1;
+  if (tid == 0) {
+    atomicAdd(arrived, 1u);
+    // The launch is cooperative, so every range of this column block is
+    // resident: wait (bounded) until all of them have published.
+    if (!wait_count_gpu(arrived, static_cast<unsigned>(ranges), tmo)) raise_abort(abort, status);
   }
-  if (tid == 0) counters[nb] = 0u;  // clean for the next launch
+  __syncthreads();
+  // Each range then finishes its own slice of the block's columns: it loads
+  // that slice of every range's sums into the idle ring in one batch and
+  // adds them in range order 0, 1, ..., ranges - 1.
+  const int per = ((COLS + ranges - 1) / ranges + 3) & ~3;  // columns per slice
+  const int s0 = rg * per;
+  const int cols = s0 < COLS ? (per < COLS - s0 ? per : COLS - s0) : 0;
+  float* slice = reinterpret_cast<float*>(smem);             // [ranges][cols]
+  if (cols > 0) {
+    const int vec = cols / 4;
+    const float4* src =
+        reinterpret_cast<const float4*>(ws + static_cast<int64_t>(nb) * ranges * COLS + s0);
+    for (int i = tid; i < ranges * vec; i += THREADS)
+      reinterpret_cast<float4*>(slice)[i] = __ldcg(src + (i / vec) * (COLS / 4) + i % vec);
+  }
+  __syncthreads();
+  for (int c = tid; c < cols; c += THREADS) {
+    // in range order; eight terms are loaded before they are added
+    float sum = 0.0f;
+    int q = 0;
+    for (; q + 8 <= ranges; q += 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = slice[(q + i) * cols + c];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
+    }
+    for (; q < ranges; ++q) sum += slice[q * cols + c];
+    const int nn = n0 + s0 + c;
+    if (nn < N)
+      C[nn] = epi_apply<GELU>(epi, sum, epi.beta != 0.0f ? C[nn] : 0.0f,
+                              epi.bias ? epi.bias[nn] : 0.0f);
+  }
+  // Count the range out; the last one leaves both counters at zero for the
+  // next launch (every range has passed its wait by then).
+  if (tid == 0 && atomicAdd(departed, 1u) == static_cast<unsigned>(ranges - 1)) {
+    *arrived = 0u;
+    *departed = 0u;
+  }
 }
 
 size_t gemv_smem_bytes() {
@@ -273,9 +293,20 @@ cudaError_t launch_gemm_bf16_gemv(const CUtensorMap& tmA, const CUtensorMap& tmB
   }
   const int blocks = (N + COLS - 1) / COLS;
   auto kernel = epi.act == kActGelu ? gemm_bf16_gemv_kernel<true> : gemm_bf16_gemv_kernel<false>;
-  kernel<<<blocks * ranges, THREADS, smem, stream>>>(tmA, tmB, C, N, K, ranges, ws, counters,
-                                                     status, epi);
-  e = cudaGetLastError();
+  // With split rows the ranges of a column block wait for one another, so
+  // the launch is cooperative: every block is resident at once (the grid,
+  // one block per SM, never exceeds the SM count then) or it fails.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = ranges > 1 ? 1 : 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks * ranges), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, C, N, K, ranges, ws, counters, status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -353,6 +353,12 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
       __threadfence();
       reduce_ranges<GELU>(tile_ws, split, C, ldc, M, N, m0, n0, row_a, col_b, vec_c, epi);
       if (tid == 0) counters[local_tile] = 0;  // leave the counter as found
+      // Every partial of this tile has been read: drop their lines from L2
+      // without writing them back (the next launch writes them anew).
+      __syncthreads();
+      const int lines = split * (BM * BN * 4 / 128);
+      for (int l = tid; l < lines; l += THREADS)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(tile_ws + l * 32) : "memory");
     }
     return;
   }

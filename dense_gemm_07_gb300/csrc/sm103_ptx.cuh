@@ -109,6 +109,22 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p,
                : "memory");
 }
 
+// Wait until the counter at p reaches `target` (acquire, gpu scope); gives
+// up after limit_ns and returns false.
+__device__ __forceinline__ bool wait_count_gpu(const unsigned int* p, unsigned int target,
+                                               uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "l"(reinterpret_cast<uint64_t>(p))
+                 : "memory");
+    if (v >= target) return true;
+    if ((i & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Order this thread's global-memory accesses through the generic proxy
 // with those of the copy engine (async proxy), in both directions.
 __device__ __forceinline__ void fence_proxy_async_global() {

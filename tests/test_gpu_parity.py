@@ -256,11 +256,13 @@ def test_bf16_skinny_exact(M):
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 3001), (1, 3001, 1000),
                                    (1, 127, 127), (1, 11008, 4096), (1, 4096, 11008),
                                    (1, 4096, 1), (1, 4096, 16), (1, 4096, 17), (1, 1, 64),
-                                   (1, 256, 65536), (1, 1100, 40)])
+                                   (1, 256, 65536), (1, 1100, 40), (1, 4096, 64),
+                                   (1, 1000, 100), (1, 2048, 200), (1, 3000, 4096)])
 def test_bf16_vector_times_matrix_exact(shape):
     # M = 1: B streamed in 1024-column blocks split into row ranges; ragged
     # N (a partial or wholly out-of-range box), ragged K, B copied first
-    # (N = 3001, 127), K below one 16-row stage, long K (many ranges)
+    # (N = 3001, 127), K below one 16-row stage, long K (many ranges), and
+    # 2 to 6 ranges, whose column slices are wider than a block of threads
     M, N, K = shape
     s, plan = g7.plan("bf16", M, N, K)
     assert _abi.PATHS[plan.path] == "bf16_gemv"
