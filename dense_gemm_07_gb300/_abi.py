@@ -27,7 +27,7 @@ GEMM_ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 PATHS = {0: "none", 1: "zero_fill", 2: "f32_simt", 3: "bf16_tma",
-         4: "bf16_packed", 5: "bf16_skinny", 6: "bf16_gemv"}
+         4: "bf16_packed", 5: "bf16_skinny", 6: "bf16_gemv", 7: "bf16_small"}
 
 
 class GemmPlan(ctypes.Structure):
@@ -76,6 +76,7 @@ SIGNATURES = [
                              ctypes.POINTER(GemmPlan)]),
     ("gemm_pair_units", _i64, [_i64, _i64, _i64, _i32, _i32, _i32, _vp, _i64]),
     ("gemm_set_bf16_schedule", _i32, [_i32]),
+    ("gemm_set_bf16_small_limit", _i64, [_i64]),
 ]
 
 
@@ -199,6 +200,13 @@ SCHEDULE_COLUMN_SPLIT = 2
 
 def gemm_set_bf16_schedule(schedule: int) -> int:
     return lib().gemm_set_bf16_schedule(schedule)
+
+
+def gemm_set_bf16_small_limit(max_macs: int) -> int:
+    """Largest M*N*K (M >= 2) sent to the CUDA-core small-problem path;
+    0 sends every BF16 call to the tensor-core kernels.  Returns the
+    previous limit."""
+    return lib().gemm_set_bf16_small_limit(max_macs)
 
 
 def gemm_pair_units(M, N, K, max_pairs, pair, schedule=SCHEDULE_AUTO):

@@ -19,6 +19,15 @@ std::atomic<uint64_t> g_launches{0};
 
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
+// Largest M * N * K sent to the CUDA-core small-problem kernel (M >= 2).
+std::atomic<int64_t> g_small_limit{kBf16SmallMaxMacs};
+bool bf16_small_problem(int64_t M, int64_t N, int64_t K, bool needs_copy) {
+  const int64_t lim = g_small_limit.load();
+  const int64_t max_macs =
+      needs_copy ? lim : (lim < kBf16SmallAlignedMacs ? lim : kBf16SmallAlignedMacs);
+  return M >= 2 && (M >= 64 || N * K <= (int64_t(1) << 19)) && M * N * K <= max_macs;
+}
+
 namespace {
 
 // Device status block: [0] status bits (bit 0: a bounded wait ran out),
@@ -36,7 +45,8 @@ enum ScratchUse {
   kScratchSplitK = 1,   // FP32 split-K counters (kept zero) + partial sums
   kScratchPack = 2,     // BF16 operands copied to aligned rows
   kScratchGemv = 3,     // BF16 M = 1: counters (kept zero) + partial sums
-  kScratchUses = 4
+  kScratchSmall = 4,    // BF16 small problems: counters (kept zero) + partial tiles
+  kScratchUses = 5
 };
 struct StreamScratch {
   cudaStream_t stream = nullptr;
@@ -190,7 +200,7 @@ gemm_status_t plan_f32(int64_t M, int64_t N, int64_t K, const void* A,
 
 gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
                         int64_t lda, const void* B, int64_t ldb, const void* C,
-                        int64_t ldc, gemm_plan_t* p) {
+                        int64_t ldc, gemm_plan_t* p, bool allow_small = true) {
   plan_clear(p);
   const gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (s != GEMM_OK) return s;
@@ -209,6 +219,21 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   p->pack_b = (aligned16(B) && ldb % 8 == 0) ? 0 : 1;
   p->path = (p->pack_a || p->pack_b) ? GEMM_PATH_BF16_PACKED : GEMM_PATH_BF16_TMA;
   p->workspace_bytes = pack_bytes(M, N, K, p->pack_a, p->pack_b);
+  if (allow_small && bf16_small_problem(M, N, K, p->pack_a || p->pack_b)) {
+    // Few multiply-adds: one launch on the CUDA cores, operands read in
+    // place (the K split is reported for the 152 SMs of a GB300).
+    const Bf16SmallPlan sp = bf16_small_plan(static_cast<int>(M), static_cast<int>(N),
+                                             static_cast<int>(K), 152);
+    p->path = GEMM_PATH_BF16_SMALL;
+    p->pack_a = p->pack_b = 0;
+    p->tile_m = p->tile_n = kBf16SmallTile;
+    p->tile_k = 32;
+    p->stages = 2;
+    p->split_k = sp.split;
+    p->tiles = static_cast<int64_t>(sp.tiles_m) * sp.tiles_n * sp.split;
+    p->workspace_bytes = sp.split > 1 ? kBf16SmallCounterBytes + sp.workspace_bytes : 0;
+    return GEMM_OK;
+  }
   if (M == 1) {
     // One row of A: B streamed through shared memory, products on the CUDA
     // cores (the row ranges are reported for the 152 SMs of a GB300;
@@ -637,6 +662,28 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
 
   const int m = static_cast<int>(M), n = static_cast<int>(N),
             k = static_cast<int>(K);
+  if (plan.path == GEMM_PATH_BF16_SMALL) {
+    // A fixed area of counters first, so that every call finds its counters
+    // zero whatever the size of earlier calls (zero when new; each launch's
+    // last blocks put them back), then the partial tiles.
+    const Bf16SmallPlan sp = bf16_small_plan(m, n, k, d->sms);
+    const int64_t counter_area = kBf16SmallCounterBytes;
+    void* ws = nullptr;
+    bool fresh = false, owned = false;
+    if (sp.split > 1) {
+      s = call_scratch(d, stream, kScratchSmall, counter_area + sp.workspace_bytes, &ws,
+                       &fresh, &owned);
+      if (s != GEMM_OK) return s;
+      if (fresh) s = from_cuda(cudaMemsetAsync(ws, 0, counter_area, stream));
+    }
+    if (s == GEMM_OK)
+      s = from_cuda(launch_gemm_bf16_small(
+          m, n, k, A, lda, B, ldb, C, ldc, aligned16(C) && ldc % 4 == 0, sp,
+          ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counter_area) : nullptr,
+          static_cast<unsigned int*>(ws), epi, stream));
+    if (owned) pool_free(ws, stream);
+    return s;
+  }
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
   const bool paired = !skinny && plan.path != GEMM_PATH_BF16_GEMV;
   const int max_pairs = paired ? pair_max_active(stream) : 0;
@@ -934,7 +981,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
                                const uint16_t* B, int64_t ldb, float* C,
                                int64_t ldc, cudaStream_t stream) {
   gemm_plan_t plan;
-  gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan);
+  gemm_status_t s = plan_bf16(M, N, K, A, lda, B, ldb, C, ldc, &plan, /*allow_small=*/false);
   if (s != GEMM_OK || plan.path == GEMM_PATH_NONE) return s;
   const int64_t pack_ws = pack_bytes(M, N, K, plan.pack_a, plan.pack_b);
   if (pack_ws > kNoallocScratchBytes) return GEMM_ERR_SCRATCH_TOO_SMALL;
@@ -1153,6 +1200,11 @@ void gemm_shutdown(void) {
 }
 
 int gemm_abi_version(void) { return 3; }
+
+int64_t gemm_set_bf16_small_limit(int64_t max_macs) {
+  if (max_macs < 0) return -1;
+  return g_small_limit.exchange(max_macs);
+}
 
 int gemm_set_bf16_schedule(int schedule) {
   if (schedule < GEMM_SCHEDULE_AUTO || schedule > GEMM_SCHEDULE_COLUMN_SPLIT)

@@ -50,6 +50,34 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
                             float* ws, unsigned int* counters,
                             const EpiParams& epi, cudaStream_t stream);
 
+// ---- BF16, small problems on the CUDA cores (gemm_bf16_small.cu): 64 x 64
+// tiles split along K, operands read in place at any alignment.
+constexpr int kBf16SmallTile = 64;
+constexpr int kBf16SmallMaxSplit = 16;
+struct Bf16SmallPlan {
+  int tiles_m = 0, tiles_n = 0, split = 1;
+  int64_t workspace_bytes = 0;  // partial tiles (after kBf16SmallCounterBytes of counters)
+};
+// Problems run there (measured crossovers on a GB300, CUDA events):
+//   * M >= 2 (M = 1 keeps the vector-times-matrix kernel, which streams B);
+//   * M >= 64 or B of at most 2^19 elements (for few rows and a larger B
+//     the small-M tensor-core kernel streams B much faster);
+//   * at most the set limit of multiply-adds, by default kBf16SmallMaxMacs,
+//     when an operand would have to be copied to an aligned layout for the
+//     tensor-core kernels, else at most min(limit, kBf16SmallAlignedMacs).
+constexpr int64_t kBf16SmallMaxMacs = int64_t(1) << 27;
+constexpr int64_t kBf16SmallAlignedMacs = int64_t(1) << 24;
+bool bf16_small_problem(int64_t M, int64_t N, int64_t K, bool needs_copy);
+// Fixed counter area at the start of the scratch block (one counter per
+// tile, so at most 1024 split tiles), the partial tiles after it.
+constexpr int64_t kBf16SmallCounterBytes = 4096;
+Bf16SmallPlan bf16_small_plan(int M, int N, int K, int sms);
+cudaError_t launch_gemm_bf16_small(int M, int N, int K, const uint16_t* A, int64_t lda,
+                                   const uint16_t* B, int64_t ldb, float* C, int64_t ldc,
+                                   bool vec_c, const Bf16SmallPlan& p, float* ws,
+                                   unsigned int* counters, const EpiParams& epi,
+                                   cudaStream_t stream);
+
 // ---- BF16 tensor-core path: shared tile constants.  One CTA of a pair
 // stages kTcTileM rows of A per k-slice of kTcTileK; M <= kTcTileM runs on
 // the small-M kernel, larger M on the paired-SM kernel.

@@ -301,11 +301,17 @@ typedef enum gemm_path {
     GEMM_PATH_BF16_SKINNY = 5,  /* 2 <= M <= 128: 128-column tiles, K split
                                    over a cluster, B streamed once (A/B may
                                    also be copied first: see pack_a / pack_b) */
-    GEMM_PATH_BF16_GEMV = 6     /* M == 1: B streamed through shared memory in
+    GEMM_PATH_BF16_GEMV = 6,    /* M == 1: B streamed through shared memory in
                                    1024-column blocks, FP32 products on the
                                    CUDA cores, rows split into split_k ranges
                                    added in range order (the no-allocation
                                    entry point uses GEMM_PATH_BF16_SKINNY) */
+    GEMM_PATH_BF16_SMALL = 7    /* few multiply-adds (gemm_set_bf16_small_limit):
+                                   64 x 64 tiles on the CUDA cores, operands
+                                   read in place at any alignment (no
+                                   copies), K split into split_k ranges added
+                                   in range order (not used by the
+                                   no-allocation entry point) */
 } gemm_path_t;
 
 typedef struct gemm_plan {
@@ -360,6 +366,18 @@ typedef enum gemm_schedule {
  * schedule, or -1 (nothing changed) for an unknown value.  No GPU needed.
  */
 GEMM07_API int gemm_set_bf16_schedule(int schedule);
+
+/*
+ * gemm_set_bf16_small_limit: the largest number of multiply-adds (M * N * K)
+ * of a BF16 call that takes GEMM_PATH_BF16_SMALL, for calls issued after it
+ * returns, process-wide.  That path also needs M >= 2, and M >= 64 or
+ * N * K <= 2^19; when the tensor-core kernels could read both operands in
+ * place (no copy needed) the limit is at most 2^24.  0 sends every call to
+ * the tensor-core kernels.  Default 2^27 (the measured crossovers on a
+ * GB300).  Returns the previous limit, or -1 (nothing changed) for a
+ * negative value.  No GPU needed.
+ */
+GEMM07_API int64_t gemm_set_bf16_small_limit(int64_t max_macs);
 
 /*
  * gemm_pair_units: the work units that SM pair `pair` computes in the BF16

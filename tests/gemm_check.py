@@ -11,6 +11,8 @@ where S[i][j] = sum_k |A[i][k] * B[k][j]| comes from the oracle as well.
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 import torch
 
@@ -67,3 +69,24 @@ def assert_guards_intact(buf, M, N, ldc):
     assert np.all(bits[0] == SENTINEL_BITS), "row above C written"
     assert np.all(bits[M + 1] == SENTINEL_BITS), "row below C written"
     assert np.all(bits[1:M + 1, N:] == SENTINEL_BITS), "padding columns written"
+
+
+@contextlib.contextmanager
+def small_limit(max_macs):
+    """BF16 calls inside the block take the CUDA-core small-problem path
+    only up to max_macs multiply-adds (0: always the tensor-core kernels)."""
+    from dense_gemm_07_gb300 import _abi
+    prev = _abi.gemm_set_bf16_small_limit(max_macs)
+    try:
+        yield
+    finally:
+        _abi.gemm_set_bf16_small_limit(prev)
+
+
+# Routes for BF16 shapes under the small-problem limit: the default (the
+# CUDA-core small-problem kernel) and the tensor-core kernels.
+ROUTES = ("default", "tensor_cores")
+
+
+def route_limit(route):
+    return small_limit(0) if route == "tensor_cores" else contextlib.nullcontext()

@@ -5,6 +5,8 @@ import ctypes
 import os
 import re
 
+import contextlib
+
 import pytest
 
 import dense_gemm_07_gb300 as g7
@@ -125,10 +127,11 @@ def test_plan_paths():
     # one 16-row stage: a single range, no scratch
     path, p = _path("bf16", 1, 1000, 16)
     assert path == "bf16_gemv" and p.split_k == 1 and p.workspace_bytes == 0
-    assert _path("bf16", 2, 4096, 4096)[1].tile_m == 16
     assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
     assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
-    assert _path("bf16", 16, 100, 64)[1].split_k == 1      # one k slice only
+    with _small_limit(0):                                   # tensor-core kernels only
+        assert _path("bf16", 2, 4096, 4096)[1].tile_m == 16
+        assert _path("bf16", 16, 100, 64)[1].split_k == 1  # one k slice only
     path, p = _path("f32", 4096, 4096, 4096)
     assert path == "f32_simt" and p.tiles == 32 * 32
     # small problems: 64 x 64 tiles (split along K on the device)
@@ -144,8 +147,53 @@ def test_plan_paths():
     assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
     assert p.workspace_bytes >= 127 * 3008 * 2
     # misaligned base address -> packed
-    path, p = _path("bf16", 256, 256, 256, A=16 + 2)
+    path, p = _path("bf16", 300, 1000, 3001, A=16 + 2)
     assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
+    with _small_limit(0):
+        path, p = _path("bf16", 256, 256, 256, A=16 + 2)
+        assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
+
+
+@contextlib.contextmanager
+def _small_limit(v):
+    prev = _abi.gemm_set_bf16_small_limit(v)
+    try:
+        yield
+    finally:
+        _abi.gemm_set_bf16_small_limit(prev)
+
+
+def test_plan_small_bf16_path():
+    # M >= 2, few multiply-adds: 64 x 64 tiles on the CUDA cores, operands
+    # read in place (no copies even with rows of 127 elements or a base off
+    # 16 bytes), K split so that the blocks cover about two per SM
+    path, p = _path("bf16", 127, 127, 127)
+    assert path == "bf16_small" and p.pack_a == 0 and p.pack_b == 0
+    assert (p.tile_m, p.tile_n, p.tile_k) == (64, 64, 32)
+    assert p.split_k == 4 and p.tiles == 4 * 4          # 4 slices of K, 4 tiles
+    assert p.workspace_bytes == 4096 + 4 * 4 * 64 * 64 * 4   # fixed counter area first
+    path, p = _path("bf16", 256, 256, 256, A=16 + 2)
+    assert path == "bf16_small" and p.pack_a == 0
+    path, p = _path("bf16", 3001, 127, 127)
+    assert path == "bf16_small" and p.split_k == 3 and p.tiles == 47 * 2 * 3   # 304 // 94 = 3
+    path, p = _path("bf16", 1000, 1000, 127)            # 127 M multiply-adds, A would be copied
+    assert path == "bf16_small" and p.split_k == 1 and p.workspace_bytes == 0
+    # operands the tensor-core kernels read in place: only up to 2^24
+    assert _path("bf16", 256, 256, 256)[0] == "bf16_small"        # 2^24
+    assert _path("bf16", 256, 256, 264)[0] == "bf16_tma"
+    assert _path("bf16", 127, 1000, 1000)[0] == "bf16_skinny"     # aligned rows, 1.3e8
+    assert _path("bf16", 1000, 1000, 1000)[0] == "bf16_tma"       # 10^9: tensor cores
+    # few rows and a larger B: the small-M tensor-core kernel streams B
+    assert _path("bf16", 2, 1000, 1000)[0] == "bf16_skinny"
+    assert _path("bf16", 8, 3001, 3001)[0] == "bf16_skinny"
+    assert _path("bf16", 2, 8, 8)[0] == "bf16_small"
+    assert _path("bf16", 1, 127, 127)[0] == "bf16_gemv"          # M = 1 streams B
+    # the limit is process-wide and settable; negative values are refused
+    with _small_limit(1000):
+        assert _path("bf16", 10, 10, 10)[0] == "bf16_small"      # lda = 10: A would be copied
+        assert _path("bf16", 10, 10, 11)[0] == "bf16_skinny"
+    assert _abi.gemm_set_bf16_small_limit(-1) == -1
+    assert _path("bf16", 127, 127, 127)[0] == "bf16_small"
 
 
 def test_plan_and_calls_reject_bad_arguments(lib):

@@ -11,14 +11,14 @@ import torch
 import dense_gemm_07_gb300 as g7
 from dense_gemm_07_gb300 import _abi, inputs
 import oracle
-from gemm_check import ATOL, RTOL, oracle_ref
+from gemm_check import ATOL, RTOL, oracle_ref, route_limit
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
 def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist,
-          schedule=None):
+          schedule=None, route="default"):
     dtype = torch.float32 if kind == "f32" else torch.bfloat16
     a, b = inputs.make_pair(M, N, K, seed, dist, dtype=dtype)
     g = torch.Generator().manual_seed(seed + 1000)
@@ -28,9 +28,10 @@ def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist,
     fn = g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex
     prev = _abi.gemm_set_bf16_schedule(schedule) if schedule is not None else None
     try:
-        fn(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
-           bias=bias.to(DEV) if bias is not None else None, activation=act)
-        torch.cuda.synchronize()
+        with route_limit(route):
+            fn(a.to(DEV), b.to(DEV), out=out, alpha=alpha, beta=beta,
+               bias=bias.to(DEV) if bias is not None else None, activation=act)
+            torch.cuda.synchronize()
     finally:
         if prev is not None:
             _abi.gemm_set_bf16_schedule(prev)
@@ -52,32 +53,35 @@ def _case(kind, M, N, K, seed, alpha, beta, use_bias, act, exact, dist,
         assert np.all(err <= lim), float(np.max(err - lim))
 
 
+TC = "tensor_cores"
 PATHS = [
-    ("bf16", 512, 768, 320, None),   # SM pairs, TMA-store epilogue
-    ("bf16", 300, 258, 200, None),   # SM pairs, N % 4 != 0: row stores
-    ("bf16", 2048, 2561, 320, None),  # half-width tail units, row stores
-    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + TMA stores
-    ("bf16", 2560, 2302, 512, _abi.SCHEDULE_STREAM_K),  # stream-K + row stores
-    ("bf16", 512, 1024, 8192, None),   # tiles halved along K; alpha-only: finished in C
-    ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K),  # stream-K over every tile
-    ("bf16", 48, 1000, 777, None),   # small M, cluster reduction
-    ("bf16", 1, 4096, 4096, None),   # M = 1: range sums added by the last range
-    ("bf16", 1, 1000, 40, None),     # M = 1, one range: finished in place
-    ("f32", 200, 190, 300, None),    # FP32 small problem: 64 x 64 tiles split along K
-    ("f32", 640, 520, 2000, None),   # FP32, one partial wave split along K
-    ("f32", 2560, 2048, 640, None),  # FP32, whole waves + split tail
+    ("bf16", 512, 768, 320, None, TC),   # SM pairs, TMA-store epilogue
+    ("bf16", 300, 258, 200, None, TC),   # SM pairs, N % 4 != 0: row stores
+    ("bf16", 2048, 2561, 320, None, TC),  # half-width tail units, row stores
+    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K, TC),  # stream-K + TMA stores
+    ("bf16", 2560, 2302, 512, _abi.SCHEDULE_STREAM_K, TC),  # stream-K + row stores
+    ("bf16", 512, 1024, 8192, None, TC),   # tiles halved along K; alpha-only: finished in C
+    ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K, TC),  # stream-K over every tile
+    ("bf16", 48, 1000, 777, None, TC),   # small M, cluster reduction
+    ("bf16", 1, 4096, 4096, None, TC),   # M = 1: range sums added by the row ranges
+    ("bf16", 1, 1000, 40, None, TC),     # M = 1, one range: finished in place
+    ("bf16", 300, 258, 200, None, "default"),   # small problem on the CUDA cores, split K
+    ("bf16", 2000, 1000, 60, None, "default"),  # small problem, no split: finished in place
+    ("f32", 200, 190, 300, None, "default"),    # FP32 small problem: 64 x 64 tiles split along K
+    ("f32", 640, 520, 2000, None, "default"),   # FP32, one partial wave split along K
+    ("f32", 2560, 2048, 640, None, "default"),  # FP32, whole waves + split tail
 ]
 
 
-@pytest.mark.parametrize("path", PATHS, ids=lambda p: f"{p[0]}-{p[1]}x{p[2]}x{p[3]}")
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: f"{p[0]}-{p[1]}x{p[2]}x{p[3]}-{p[5]}")
 @pytest.mark.parametrize("epi", [(2.0, -1.0, True, "none"), (1.0, 0.0, True, "relu"),
                                  (-3.0, 2.0, False, "relu"), (0.5, 0.0, False, "none")],
                          ids=["ab+c+bias", "bias+relu", "beta_relu", "alpha_only"])
 def test_epilogue_exact_integers(path, epi):
-    kind, M, N, K, schedule = path
+    kind, M, N, K, schedule, route = path
     alpha, beta, use_bias, act = epi
     _case(kind, M, N, K, 50, alpha, beta, use_bias, act, exact=True,
-          dist=inputs.INT3, schedule=schedule)
+          dist=inputs.INT3, schedule=schedule, route=route)
 
 
 @pytest.mark.parametrize("kind", ["f32", "bf16"])
@@ -118,12 +122,13 @@ def test_unknown_activation_rejected():
                             epi, st) == _abi.GEMM_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("kind,M,N,K,schedule", [
-    ("f32", 700, 900, 1000, None), ("f32", 200, 190, 300, None),
-    ("bf16", 700, 900, 1000, None), ("bf16", 300, 258, 200, None),
-    ("bf16", 48, 1000, 777, None), ("bf16", 1, 3000, 3001, None),
-    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K)])
-def test_epilogue_gelu(kind, M, N, K, schedule):
+@pytest.mark.parametrize("kind,M,N,K,schedule,route", [
+    ("f32", 700, 900, 1000, None, "default"), ("f32", 200, 190, 300, None, "default"),
+    ("bf16", 700, 900, 1000, None, "default"), ("bf16", 300, 258, 200, None, TC),
+    ("bf16", 48, 1000, 777, None, TC), ("bf16", 1, 3000, 3001, None, "default"),
+    ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K, "default"),
+    ("bf16", 300, 258, 200, None, "default"), ("bf16", 48, 500, 777, None, "default")])
+def test_epilogue_gelu(kind, M, N, K, schedule, route):
     # GELU after alpha, beta and the bias on every path.  Bound: GELU's slope
     # is at most 1.13, so the pre-activation bound grows by that factor; the
     # FP32 erff and the final products add a few units in the last place of
@@ -138,9 +143,10 @@ def test_epilogue_gelu(kind, M, N, K, schedule):
     fn = g7.gemm_f32_ex if kind == "f32" else g7.gemm_bf16_f32acc_ex
     prev = _abi.gemm_set_bf16_schedule(schedule) if schedule is not None else None
     try:
-        fn(a.to(DEV), b.to(DEV), out=out, alpha=0.5, beta=0.75, bias=bias.to(DEV),
-           activation="gelu")
-        torch.cuda.synchronize()
+        with route_limit(route):
+            fn(a.to(DEV), b.to(DEV), out=out, alpha=0.5, beta=0.75, bias=bias.to(DEV),
+               activation="gelu")
+            torch.cuda.synchronize()
     finally:
         if prev is not None:
             _abi.gemm_set_bf16_schedule(prev)

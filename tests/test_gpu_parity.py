@@ -13,8 +13,8 @@ import torch
 import dense_gemm_07_gb300 as g7
 from dense_gemm_07_gb300 import _abi
 from dense_gemm_07_gb300 import inputs
-from gemm_check import (assert_guards_intact, assert_within, guarded_output,
-                        oracle_ref)
+from gemm_check import (ROUTES, assert_guards_intact, assert_within, guarded_output,
+                        oracle_ref, route_limit)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,9 +33,10 @@ def _run(kind, a, b, out=None):
     return c
 
 
-def _check(kind, M, N, K, seed, dist, dist_b=None, exact=False, rows=None):
+def _check(kind, M, N, K, seed, dist, dist_b=None, exact=False, rows=None, route="default"):
     a, b = inputs.make_pair(M, N, K, seed, dist, dist_b, dtype=_dtype(kind))
-    c = _run(kind, a, b).cpu().numpy()
+    with route_limit(route):
+        c = _run(kind, a, b).cpu().numpy()
     if rows is not None:
         c = c[rows]
     c_ref, s_ref = oracle_ref(kind, a, b, rows=rows, with_abs=not exact)
@@ -101,18 +102,21 @@ def test_f32_ladder_rung_uniform():
 
 # --------------------------------------------------- BF16 (tensor cores)
 
-def test_bf16_256_normal():
-    _check("bf16", 256, 256, 256, 2, inputs.NORMAL)
+@pytest.mark.parametrize("route", ROUTES)
+def test_bf16_256_normal(route):
+    _check("bf16", 256, 256, 256, 2, inputs.NORMAL, route=route)
 
 
-def test_bf16_integers_exact_tiles():
-    # several 128 x 256 tiles, several 64-deep k slices and ragged tails
-    _check("bf16", 300, 600, 200, 4, inputs.INT3, exact=True)
+@pytest.mark.parametrize("route", ROUTES)
+def test_bf16_integers_exact_tiles(route):
+    # several tiles, several k slices and ragged tails on either route
+    _check("bf16", 300, 600, 200, 4, inputs.INT3, exact=True, route=route)
 
 
+@pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("K", [1, 8, 16, 63, 64, 65, 200])
-def test_bf16_small_and_ragged_k(K):
-    _check("bf16", 130, 260, K, 5, inputs.INT3, exact=True)
+def test_bf16_small_and_ragged_k(K, route):
+    _check("bf16", 130, 260, K, 5, inputs.INT3, exact=True, route=route)
 
 
 def test_bf16_full_and_split_waves_exact():
@@ -246,6 +250,11 @@ def test_bf16_every_schedule_same_bits_on_integers(shape):
 @pytest.mark.parametrize("K", [127, 1000, 3001])
 def test_bf16_boundary_sweep_exact(M, N, K):
     _check("bf16", M, N, K, 4, inputs.INT3, exact=True)
+    # shapes under the small-problem limit run on the CUDA cores by default:
+    # check the tensor-core kernels on them as well
+    s, plan = g7.plan("bf16", M, N, K)
+    if _abi.PATHS[plan.path] == "bf16_small":
+        _check("bf16", M, N, K, 4, inputs.INT3, exact=True, route="tensor_cores")
 
 
 @pytest.mark.parametrize("M", [1, 16])
@@ -286,10 +295,12 @@ def test_bf16_vector_times_matrix_general_values_and_bits():
 @pytest.mark.parametrize("shape", [(2, 300, 1000), (17, 1000, 777), (33, 257, 4096),
                                    (64, 4096, 64), (65, 999, 130), (100, 128, 3001),
                                    (128, 2048, 2048), (5, 50, 1)])
-def test_bf16_small_m_paths_exact(shape):
-    # every MMA width (16/32/64/128), ragged N and K, K below the split count
+@pytest.mark.parametrize("route", ROUTES)
+def test_bf16_small_m_paths_exact(shape, route):
+    # every MMA width (16/32/64/128), ragged N and K, K below the split
+    # count; and the same shapes on the CUDA-core small-problem path
     M, N, K = shape
-    _check("bf16", M, N, K, 18, inputs.INT3, exact=True)
+    _check("bf16", M, N, K, 18, inputs.INT3, exact=True, route=route)
 
 
 def test_bf16_small_m_normal_values():
@@ -319,26 +330,30 @@ def test_empty_m_or_n_is_noop(kind):
     assert_guards_intact(buf, 0, 5, 8)
 
 
-@pytest.mark.parametrize("kind", ["f32", "bf16"])
+@pytest.mark.parametrize("kind,route", [("f32", "default"), ("bf16", "default"),
+                                        ("bf16", "tensor_cores")])
 @pytest.mark.parametrize("shape", [(129, 257, 70), (300, 600, 200)])
-def test_guard_bands_untouched(kind, shape):
+def test_guard_bands_untouched(kind, route, shape):
     M, N, K = shape
     a, b = inputs.make_pair(M, N, K, 9, inputs.INT3, dtype=_dtype(kind))
     ldc = N + 7
     buf, c = guarded_output(M, N, ldc, DEV)
-    (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a.to(DEV), b.to(DEV), out=c)
-    torch.cuda.synchronize()
+    with route_limit(route):
+        (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a.to(DEV), b.to(DEV), out=c)
+        torch.cuda.synchronize()
     assert_guards_intact(buf, M, N, ldc)
     c_ref, s_ref = oracle_ref(kind, a, b)
     assert_within(kind, c.cpu().numpy(), c_ref, s_ref, exact=True)
 
 
-@pytest.mark.parametrize("shape,schedule", [
-    ((2048, 2561, 320), g7.abi.SCHEDULE_AUTO),       # 88 tiles: half-width tail units
-    ((2560, 2302, 640), g7.abi.SCHEDULE_STREAM_K),   # partial sums combined on the way out
-    ((300, 258, 200), g7.abi.SCHEDULE_AUTO),
-    ((1000, 127, 127), g7.abi.SCHEDULE_AUTO)])
-def test_bf16_row_store_epilogue_guarded(shape, schedule):
+@pytest.mark.parametrize("shape,schedule,route", [
+    ((2048, 2561, 320), g7.abi.SCHEDULE_AUTO, "default"),      # 88 tiles: half-width tail units
+    ((2560, 2302, 640), g7.abi.SCHEDULE_STREAM_K, "default"),  # partial sums combined on the way out
+    ((300, 258, 200), g7.abi.SCHEDULE_AUTO, "tensor_cores"),
+    ((1000, 127, 127), g7.abi.SCHEDULE_AUTO, "tensor_cores"),
+    ((300, 258, 200), g7.abi.SCHEDULE_AUTO, "default"),        # small-problem path
+    ((1000, 127, 127), g7.abi.SCHEDULE_AUTO, "default")])
+def test_bf16_row_store_epilogue_guarded(shape, schedule, route):
     # a row stride that is not a multiple of 16 bytes: C is written through
     # the staging boxes with ordinary row stores (no TMA store), and nothing
     # outside [0, M) x [0, N) may change
@@ -348,8 +363,9 @@ def test_bf16_row_store_epilogue_guarded(shape, schedule):
     buf, c = guarded_output(M, N, ldc, DEV)
     prev = g7.abi.gemm_set_bf16_schedule(schedule)
     try:
-        g7.gemm_bf16_f32acc(a.to(DEV), b.to(DEV), out=c)
-        torch.cuda.synchronize()
+        with route_limit(route):
+            g7.gemm_bf16_f32acc(a.to(DEV), b.to(DEV), out=c)
+            torch.cuda.synchronize()
     finally:
         g7.abi.gemm_set_bf16_schedule(prev)
     assert g7.gemm_get_device_status() == 0
@@ -358,8 +374,9 @@ def test_bf16_row_store_epilogue_guarded(shape, schedule):
     assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
 
 
-@pytest.mark.parametrize("kind", ["f32", "bf16"])
-def test_leading_dims_and_misaligned_bases(kind):
+@pytest.mark.parametrize("kind,route", [("f32", "default"), ("bf16", "default"),
+                                        ("bf16", "tensor_cores")])
+def test_leading_dims_and_misaligned_bases(kind, route):
     M, N, K = 150, 270, 90
     a, b = inputs.make_pair(M, N, K, 12, inputs.INT3, dtype=_dtype(kind))
     # operands placed at odd element offsets inside wider rows
@@ -369,14 +386,20 @@ def test_leading_dims_and_misaligned_bases(kind):
     b_buf[:, 3:N + 3] = b.to(DEV)
     a_v, b_v = a_buf[:, 1:K + 1], b_buf[:, 3:N + 3]
     assert a_v.stride(0) == K + 11 and b_v.stride(0) == N + 13
-    c = (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a_v, b_v)
-    torch.cuda.synchronize()
+    with route_limit(route):
+        c = (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a_v, b_v)
+        torch.cuda.synchronize()
+        if kind == "bf16":
+            # read in place by the small-problem kernel, copied first for
+            # the tensor-core kernels
+            s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
+                           b_v.data_ptr(), b_v.stride(0), c.data_ptr(), N)
+            if route == "default":
+                assert g7.abi.PATHS[p.path] == "bf16_small" and not p.pack_a and not p.pack_b
+            else:
+                assert g7.abi.PATHS[p.path] == "bf16_packed" and p.pack_a and p.pack_b
     c_ref, s_ref = oracle_ref(kind, a, b)
     assert_within(kind, c.cpu().numpy(), c_ref, s_ref, exact=True)
-    if kind == "bf16":
-        s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
-                       b_v.data_ptr(), b_v.stride(0), c.data_ptr(), N)
-        assert g7.abi.PATHS[p.path] == "bf16_packed" and p.pack_a and p.pack_b
 
 
 @pytest.mark.parametrize("a_off,b_off", [(1, 0), (0, 3), (8, 8)])
@@ -566,3 +589,55 @@ def test_capture_on_fresh_stream_then_replay(case):
         del graph
     finally:
         g7.abi.gemm_set_bf16_schedule(prev)
+
+
+# ------------------------------------------- BF16 small problems (CUDA cores)
+
+@pytest.mark.parametrize("shape", [(127, 127, 127), (2, 8, 8), (3001, 127, 127),
+                                   (127, 3001, 127), (1000, 1000, 127), (64, 64, 4001),
+                                   (65, 63, 33), (5, 50, 1), (256, 256, 256)])
+def test_bf16_small_problem_path_normal_values(shape):
+    # general values: every element within the BF16 bound, on the path that
+    # reads operands in place and splits K over the SMs
+    M, N, K = shape
+    s, plan = g7.plan("bf16", M, N, K)
+    assert _abi.PATHS[plan.path] == "bf16_small"
+    _check("bf16", M, N, K, 41, inputs.NORMAL)
+
+
+def test_bf16_small_problem_deterministic_bits():
+    # the K ranges are added in a fixed order by whichever block finishes
+    # last, so repeated calls give the same bits
+    a, b = inputs.make_pair(200, 300, 2000, 42, inputs.NORMAL, dtype=torch.bfloat16)
+    s, plan = g7.plan("bf16", 200, 300, 2000)
+    assert _abi.PATHS[plan.path] == "bf16_small" and plan.split_k > 1
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    first = g7.gemm_bf16_f32acc(a_d, b_d).clone()
+    for _ in range(5):
+        assert torch.equal(g7.gemm_bf16_f32acc(a_d, b_d).view(torch.int32),
+                           first.view(torch.int32))
+    c_ref, s_ref = oracle_ref("bf16", a, b)
+    assert_within("bf16", first.cpu().numpy(), c_ref, s_ref)
+
+
+def test_bf16_small_problem_odd_strides_and_offsets_read_in_place():
+    # rows of odd length at odd element offsets in every operand, C at an
+    # odd offset too: nothing is copied, nothing outside C changes
+    M, N, K = 77, 91, 133
+    a, b = inputs.make_pair(M, N, K, 43, inputs.INT3, dtype=torch.bfloat16)
+    a_buf = torch.zeros((M, K + 5), dtype=a.dtype, device=DEV)
+    b_buf = torch.zeros((K, N + 3), dtype=b.dtype, device=DEV)
+    a_buf[:, 1:K + 1] = a.to(DEV)
+    b_buf[:, 2:N + 2] = b.to(DEV)
+    a_v, b_v = a_buf[:, 1:K + 1], b_buf[:, 2:N + 2]
+    ldc = N + 3
+    buf, c = guarded_output(M, N, ldc, DEV)
+    s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
+                   b_v.data_ptr(), b_v.stride(0), c.data_ptr(), ldc)
+    assert _abi.PATHS[p.path] == "bf16_small" and not p.pack_a and not p.pack_b
+    g7.gemm_bf16_f32acc(a_v, b_v, out=c)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == 0
+    assert_guards_intact(buf, M, N, ldc)
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)

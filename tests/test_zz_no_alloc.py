@@ -21,7 +21,7 @@ import torch
 
 import dense_gemm_07_gb300 as g7
 from dense_gemm_07_gb300 import _abi, inputs
-from gemm_check import assert_within, oracle_ref
+from gemm_check import assert_within, oracle_ref, small_limit
 
 pytestmark = pytest.mark.gpu
 
@@ -83,8 +83,11 @@ def test_noalloc_copied_operands_two_calls_in_a_row():
             a_d, b_d = a.to(DEV), b.to(DEV)
         else:
             a_d, b_d = _misaligned(a, 9, 3), _misaligned(b, 11, 1)
-        s, plan = g7.plan("bf16", M, N, K, a_d.data_ptr(), a_d.stride(0),
-                          b_d.data_ptr(), b_d.stride(0), 16, N)
+        # this entry point never takes the small-problem path: planned with
+        # that path off, the call copies A (and B) into the fixed array
+        with small_limit(0):
+            s, plan = g7.plan("bf16", M, N, K, a_d.data_ptr(), a_d.stride(0),
+                              b_d.data_ptr(), b_d.stride(0), 16, N)
         assert s == 0 and plan.pack_a == 1, "case must exercise the scratch copies"
         _against_oracle_and_pooled(a, b, a_d, b_d, exact, f"{M}x{N}x{K}")
 
