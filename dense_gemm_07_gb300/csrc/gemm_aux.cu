@@ -6,10 +6,10 @@
 //     base is 16-byte aligned and whose row stride is a multiple of 16 bytes.
 // The fill is a grid-stride loop over rows x columns (consecutive threads,
 // consecutive columns).  The copy gives each thread one 16-byte group of a
-// destination row: eight 2-byte loads from the source (any alignment; a
-// warp's loads cover 512 contiguous bytes, so they are served by a few
-// cache lines) and one 16-byte store, zeros in the padding columns up to
-// the destination stride.
+// destination row: the source (2-byte aligned, any offset) is read as the
+// one or two aligned 16-byte chunks that hold the group and shifted into
+// place in registers, then stored with one 16-byte store; zeros in the
+// padding columns up to the destination stride.
 #include <cstdint>
 
 #include "kernels.h"
@@ -30,31 +30,71 @@ __global__ void zero_fill_f32_kernel(float* __restrict__ C, int64_t ldc, int M,
   }
 }
 
+// Bytes d .. d + 15 of the 32 bytes lo:hi (d even, 0 .. 14).
+__device__ __forceinline__ uint4 bytes_at(const uint4& lo, const uint4& hi, int d) {
+  const int sh = (d & 3) * 8;
+  uint32_t w0, w1, w2, w3, w4;
+  switch (d >> 2) {
+    case 0: w0 = lo.x; w1 = lo.y; w2 = lo.z; w3 = lo.w; w4 = hi.x; break;
+    case 1: w0 = lo.y; w1 = lo.z; w2 = lo.w; w3 = hi.x; w4 = hi.y; break;
+    case 2: w0 = lo.z; w1 = lo.w; w2 = hi.x; w3 = hi.y; w4 = hi.z; break;
+    default: w0 = lo.w; w1 = hi.x; w2 = hi.y; w3 = hi.z; w4 = hi.w; break;
+  }
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
+// One 16-byte group of a destination row: source elements c0 .. c0 + n - 1
+// (n <= 8, the rest of the group zero).  The source is read as the one or
+// two aligned 16-byte chunks that hold those elements, so every load stays
+// inside a 16-byte granule that holds data of the source row.
+__device__ __forceinline__ uint4 load_group(const uint16_t* s, int n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+  const int d = static_cast<int>(a & 15u);
+  const uint4* base = reinterpret_cast<const uint4*>(a - d);
+  const uint4 lo = __ldg(base);
+  const uint4 hi = d + 2 * n > 16 ? __ldg(base + 1) : make_uint4(0u, 0u, 0u, 0u);
+  uint4 v = d ? bytes_at(lo, hi, d) : lo;
+  if (n < 8) {
+    // clear the elements past the end of the row (word i holds elements
+    // 2i and 2i + 1)
+    auto keep = [n](int i) {
+      return (2 * i < n ? 0x0000FFFFu : 0u) | (2 * i + 1 < n ? 0xFFFF0000u : 0u);
+    };
+    v.x &= keep(0);
+    v.y &= keep(1);
+    v.z &= keep(2);
+    v.w &= keep(3);
+  }
+  return v;
+}
+
 // grid: x over 16-byte groups of a row (blockDim.x threads each), y over
-// rows (grid-stride), z over the copies; each ld_dst is a multiple of 8 and
-// each dst 16-byte aligned.
+// rows (grid-stride, four rows' loads in flight per thread), z over the
+// copies; each ld_dst is a multiple of 8 and each dst 16-byte aligned.
 __global__ void copy_rows_u16_kernel(PackJobs jobs) {
-  const PackJob& j = jobs.job[blockIdx.z];
+  // (a select, not an index: indexing the parameter array by blockIdx.z
+  // would copy it to local memory)
+  const PackJob j = blockIdx.z == 0 ? jobs.job[0] : jobs.job[1];
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   const int c0 = g * 8;
   if (c0 >= j.cols) return;
-  const bool whole = c0 + 8 <= j.cols;
-  for (int r = blockIdx.y; r < j.rows; r += gridDim.y) {
-    const uint16_t* s = j.src + static_cast<int64_t>(r) * j.ld_src + c0;
-    uint16_t v[8];
-    if (whole) {
+  const int n = j.cols - c0 < 8 ? j.cols - c0 : 8;
+  constexpr int R = 4;
+  const int step = static_cast<int>(gridDim.y);
+  for (int r0 = blockIdx.y; r0 < j.rows; r0 += R * step) {
+    uint4 v[R];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = s[e];
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = c0 + e < j.cols ? s[e] : uint16_t(0);
+    for (int i = 0; i < R; ++i) {
+      const int r = r0 + i * step;
+      if (r < j.rows) v[i] = load_group(j.src + static_cast<int64_t>(r) * j.ld_src + c0, n);
     }
-    uint4 w;
-    w.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-    w.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-    w.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-    w.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-    *reinterpret_cast<uint4*>(j.dst + static_cast<int64_t>(r) * j.ld_dst + c0) = w;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int r = r0 + i * step;
+      if (r < j.rows)
+        *reinterpret_cast<uint4*>(j.dst + static_cast<int64_t>(r) * j.ld_dst + c0) = v[i];
+    }
   }
 }
 
