@@ -272,21 +272,34 @@ def config_figures(g7, roofline, peaks, sms, reps=20):
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
         fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
         mean, best = config_table.time_call(lambda: fn(X, Y, out=C), reps, flush)
+        us = config_table.time_batched(lambda: fn(X, Y, out=C), reps, flush)
         eb = 4 if kind == "f32" else 2
         flops = roofline.gemm_flops(M, N, K)
         nbytes = roofline.min_bytes(M, N, K, eb, 4)
         peak = fp32_peak if kind == "f32" else bf16_peak
         roof_tf = min(peak, roofline.intensity(M, N, K, eb, 4) * hbm / 1e3)
         hbm_bound = roof_tf < peak
-        tf = flops / (mean * 1e-6) / 1e12
-        e = {"cfg": name, "kind": kind, "M": M, "N": N, "K": K, "us": mean,
-             "us_best": best, "tflops": tf, "gbs": nbytes / (mean * 1e-6) / 1e9,
+        tf = flops / (us * 1e-6) / 1e12
+        e = {"cfg": name, "kind": kind, "M": M, "N": N, "K": K, "us": us,
+             "us_per_call_mean": mean, "us_per_call_best": best, "tflops": tf,
+             "gbs": nbytes / (us * 1e-6) / 1e9,
              "bound": "hbm" if hbm_bound else ("alu" if kind == "f32" else "tensor"),
              "roofline_tflops": roof_tf, "frac": tf / roof_tf}
+        if hbm_bound and M <= 16:
+            # what one read of B costs on this GPU in the same protocol: a
+            # library reduction over B (context for the skinny kernels)
+            floor = config_table.time_batched(lambda: Y.sum(dtype=torch.float32), reps, flush)
+            e["read_b_reference_us"] = floor
+            e["frac_of_read_b_reference"] = floor / us
         out.append(e)
-    return {"reps": reps, "timing": "CUDA events around one call, L2 flushed "
-            "(256 MiB write) before each, queued behind a short spin; mean of "
-            "reps (us), TFLOP/s and GB/s of algorithmic bytes from the mean",
+    return {"reps": reps, "timing": "us: CUDA events around reps x (L2 flush by a "
+            "256 MiB write, call) minus events around reps flushes alone, per "
+            "call (the kernels' own time; the host queues the batch behind a "
+            "spin); us_per_call_*: events around each call after its flush "
+            "(includes launch latency, quantised to the ~2 us event step); "
+            "TFLOP/s, GB/s of algorithmic bytes and frac from us; "
+            "read_b_reference_us (skinny HBM-bound shapes): torch's sum over "
+            "B in the same protocol, a plain read of B for context",
             "entries": out}
 
 

@@ -1,9 +1,13 @@
 """Time every workload configuration of the method on one GPU and print a
-markdown table (CUDA events on the calling stream, 3 warm-up calls, then
-`--reps` timed calls with a 256 MiB L2 flush before each, queued behind a
-short spin so that host call overhead is not timed; mean and best.  CUDA
-event timestamps on this GPU advance in steps of about 2 us, so the mean
-over many calls, not the median, resolves the short ones).
+markdown table (CUDA events on the calling stream, 3 warm-up calls, a
+256 MiB L2 flush before every call).  Two measures:
+  * batched: events around `--reps` x (flush, call) minus events around
+    `--reps` flushes alone, per call -- the kernels' own time, resolved below
+    the ~2 us step of CUDA event timestamps on this GPU; the TFLOP/s, GB/s
+    and roofline columns use it;
+  * per call: events around each call, queued behind a short spin so that
+    host call overhead is not timed; mean and best of `--reps` (includes
+    the GPU's launch latency after the flush, and is quantised to ~2 us).
 
     python -m dense_gemm_07_gb300.config_table [--reps 40] [--peaks MEASURED_PEAKS.json]
 
@@ -52,6 +56,32 @@ def configs():
     return out
 
 
+def time_batched(fn, reps, flush):
+    """Per-call device time without the ~2 us granularity of CUDA event
+    timestamps on this GPU: events around `reps` x (L2 flush, call) minus
+    events around `reps` flushes alone, divided by reps.  The stream is held
+    by a spin kernel until the host has queued the whole batch, so host
+    call overhead never shows; a call's launch latency is hidden behind the
+    flush before it, so this is close to the kernels' own duration."""
+    for _ in range(3):
+        fn()
+    out = []
+    for with_call in (True, False):
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000 * reps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            flush.fill_(1.0)
+            if with_call:
+                fn()
+        e1.record()
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3)
+    return (out[0] - out[1]) / reps
+
+
 def time_call(fn, reps, flush):
     for _ in range(3):
         fn()
@@ -91,9 +121,9 @@ def main():
     flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
     print(f"peaks ({src}): FP32 {fp32_peak:.1f} TFLOP/s, BF16 {bf16_peak:.1f} TFLOP/s, "
           f"HBM {hbm:.0f} GB/s")
-    print("| cfg | kind | M x N x K | mean us | best us | TFLOP/s | GB/s (min bytes) "
-          "| roofline | % of roofline |")
-    print("|---|---|---|---|---|---|---|---|---|")
+    print("| cfg | kind | M x N x K | us (batched) | mean us (per call) | best us | TFLOP/s "
+          "| GB/s (min bytes) | roofline | % of roofline |")
+    print("|---|---|---|---|---|---|---|---|---|---|")
     for name, kind, (M, N, K), dist, dist_b, seed in configs():
         dtype = torch.float32 if kind == "f32" else torch.bfloat16
         x, y = inputs.make_pair(M, N, K, seed, dist, dist_b, dtype=dtype)
@@ -101,16 +131,17 @@ def main():
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
         fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
         mean, best = time_call(lambda: fn(X, Y, out=C), a.reps, flush)
+        batched = time_batched(lambda: fn(X, Y, out=C), a.reps, flush)
         eb = 4 if kind == "f32" else 2
         flops = roofline.gemm_flops(M, N, K)
         nbytes = roofline.min_bytes(M, N, K, eb, 4)
-        tf = flops / (mean * 1e-6) / 1e12
-        gbs = nbytes / (mean * 1e-6) / 1e9
+        tf = flops / (batched * 1e-6) / 1e12
+        gbs = nbytes / (batched * 1e-6) / 1e9
         peak = fp32_peak if kind == "f32" else bf16_peak
         roof = min(peak, roofline.intensity(M, N, K, eb, 4) * hbm / 1e3)
         bound = "compute" if roof >= peak else "HBM"
-        print(f"| {name} | {kind} | {M}x{N}x{K} | {mean:.1f} | {best:.1f} | {tf:.1f} | "
-              f"{gbs:.0f} | {roof:.0f} TF ({bound}) | {100 * tf / roof:.1f} |")
+        print(f"| {name} | {kind} | {M}x{N}x{K} | {batched:.1f} | {mean:.1f} | {best:.1f} | "
+              f"{tf:.1f} | {gbs:.0f} | {roof:.0f} TF ({bound}) | {100 * tf / roof:.1f} |")
     if g7.gemm_get_device_status() != 0:
         raise SystemExit("device status error")
 
