@@ -19,10 +19,13 @@ void note_launches(int n);
 constexpr int kF32TileM = 128;
 constexpr int kF32TileN = 128;
 constexpr int kF32TileK = 32;
-// Tile-rows per band of the grouped raster: 16 rows of 128 x 128 tiles
-// (2048 rows of A) read 8 % fewer DRAM bytes at 4096^3 than bands of 8, in
-// the same time.
-constexpr int kF32Group = 16;
+// Tile-rows per band of the grouped raster (rows of 128 x 128 tiles).
+// Measured at 4096^3 (time, DRAM bytes per launch): 8 rows 2197 us, 422.7 MB
+// (with the split-K partials written back); 12: 2186 us, 378 MB; 16: 2193 us,
+// 351.5 MB; 24: 2192 us, 408 MB; 32: 2209 us, 581 MB.  10 to 14 are equally
+// fast, also at 8192 x 8192 x 4096 and 4096 x 4096 x 8192 (0.4-0.7 % ahead
+// of 16).
+constexpr int kF32Group = 12;
 constexpr int kF32Stages = 2;
 
 // Launch plan: `full` tiles in whole waves, then `tail` tiles split into
