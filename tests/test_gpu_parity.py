@@ -554,14 +554,16 @@ def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
         assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
 
 
-@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed", "bf16_gemv"])
+@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed", "bf16_gemv",
+                                  "bf16_small"])
 def test_capture_on_fresh_stream_then_replay(case):
     # Captured on a stream the library has never seen: its scratch is then
     # allocated inside the graph (owned by it) rather than kept, and every
     # replay on new operand values is exact.
     kind = "f32" if case.startswith("f32") else "bf16"
     M, N, K = {"f32_split_k": (2560, 2048, 640), "bf16_stream_k": (2560, 2304, 1024),
-               "bf16_packed": (700, 500, 333), "bf16_gemv": (1, 4096, 4096)}[case]
+               "bf16_packed": (1000, 600, 1333), "bf16_gemv": (1, 4096, 4096),
+               "bf16_small": (300, 258, 200)}[case]
     dtype = _dtype(kind)
     fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
     a, b = inputs.make_pair(M, N, K, 35, inputs.INT3, dtype=dtype)
@@ -569,6 +571,9 @@ def test_capture_on_fresh_stream_then_replay(case):
     c = torch.empty((M, N), dtype=torch.float32, device=DEV)
     prev = g7.abi.gemm_set_bf16_schedule(
         g7.abi.SCHEDULE_STREAM_K if case == "bf16_stream_k" else g7.abi.SCHEDULE_AUTO)
+    want = {"bf16_packed": "bf16_packed", "bf16_gemv": "bf16_gemv", "bf16_small": "bf16_small",
+            "bf16_stream_k": "bf16_tma", "f32_split_k": "f32_simt"}[case]
+    assert g7.abi.PATHS[g7.plan(kind, M, N, K)[1].path] == want
     try:
         graph = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
