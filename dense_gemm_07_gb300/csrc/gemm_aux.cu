@@ -19,6 +19,8 @@ namespace {
 
 __global__ void zero_fill_f32_kernel(float* __restrict__ C, int64_t ldc, int M,
                                      int N, EpiParams epi) {
+  grid_dependency_wait();
+  grid_dependents_go();
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
        i < total; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -76,6 +78,10 @@ __global__ void copy_rows_u16_kernel(PackJobs jobs) {
   // (a select, not an index: indexing the parameter array by blockIdx.z
   // would copy it to local memory)
   const PackJob j = blockIdx.z == 0 ? jobs.job[0] : jobs.job[1];
+  // the operands may come from the kernel before this one; the GEMM after
+  // this one waits for the whole copy before it reads it
+  grid_dependency_wait();
+  grid_dependents_go();
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   const int c0 = g * 8;
   if (c0 >= j.cols) return;
@@ -112,10 +118,12 @@ int grid_for(int64_t total, int threads) {
 cudaError_t launch_zero_fill_f32(float* C, int64_t ldc, int M, int N,
                                  const EpiParams& epi, cudaStream_t stream) {
   const int threads = 256;
-  zero_fill_f32_kernel<<<grid_for(static_cast<int64_t>(M) * N, threads),
-                         threads, 0, stream>>>(C, ldc, M, N, epi);
-  note_launches(1);
-  return cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(zero_fill_f32_kernel,
+                 dim3(static_cast<unsigned>(grid_for(static_cast<int64_t>(M) * N, threads))),
+                 dim3(threads), 0, stream, C, ldc, M, N, epi);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 cudaError_t launch_pack_u16(const PackJob* jobs, int count, cudaStream_t stream) {
@@ -143,10 +151,11 @@ cudaError_t launch_pack_u16(const PackJob* jobs, int count, cudaStream_t stream)
   if (gy > max_rows) gy = max_rows;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
-  copy_rows_u16_kernel<<<dim3(gx, static_cast<unsigned>(gy), count), threads, 0,
-                         stream>>>(p);
-  note_launches(1);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(copy_rows_u16_kernel,
+                                   dim3(gx, static_cast<unsigned>(gy), count), dim3(threads),
+                                   0, stream, p);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 }  // namespace g07

@@ -99,6 +99,10 @@ gemm_bf16_gemv_kernel(const __grid_constant__ CUtensorMap tmA,
   auto* ctl = reinterpret_cast<GemvControl*>(smem + STAGES * STAGE_STRIDE);
   volatile int* abort = &ctl->abort;
 
+  // nothing global is touched before this: wait for the kernels before this
+  // one, and let the next one be scheduled as SMs free up
+  grid_dependency_wait();
+  grid_dependents_go();
   const int tid = threadIdx.x;
   const int nb = blockIdx.x / ranges;
   const int rg = blockIdx.x % ranges;
@@ -297,15 +301,16 @@ cudaError_t launch_gemm_bf16_gemv(const CUtensorMap& tmA, const CUtensorMap& tmB
   // the launch is cooperative: every block is resident at once (the grid,
   // one block per SM, never exceeds the SM count then) or it fails.
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = ranges > 1 ? 1 : 0;
+  attr[1] = pdl_attribute();
   cfg.gridDim = dim3(static_cast<unsigned>(blocks * ranges), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, C, N, K, ranges, ws, counters, status, epi);
   if (e == cudaSuccess) note_launches(1);
   return e;

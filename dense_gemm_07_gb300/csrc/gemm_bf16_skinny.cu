@@ -107,6 +107,10 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
   const int kb_begin = static_cast<int>(static_cast<int64_t>(num_kb_total) * rank / cs);
   const int kb_end = static_cast<int>(static_cast<int64_t>(num_kb_total) * (rank + 1) / cs);
   const int num_kb = kb_end - kb_begin;
+  // Nothing global has been touched yet: wait for the kernels before this
+  // one, and let the next one be scheduled as SMs free up.
+  grid_dependency_wait();
+  grid_dependents_go();
   // Test fault (gemm_debug_inject mode 1): no CTA copies its first stage,
   // so the MMA issuer's wait for it runs out; every role unwinds and the
   // cluster still meets at its final barrier.
@@ -351,17 +355,18 @@ cudaError_t launch_nm(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
   if (ea != cudaSuccess) return ea;
   const int tiles = (N + TILE_N - 1) / TILE_N;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, C, ldc, M, N, K, cs,
                                            status, epi);
   if (e == cudaSuccess) note_launches(1);

@@ -74,6 +74,8 @@ gemm_bf16_small_kernel(int M, int N, int K, const uint16_t* __restrict__ A, int6
                        EpiParams epi) {
   __shared__ __align__(16) SmallStage st[2];
   __shared__ int last_block;
+  grid_dependency_wait();  // before the first read of A, B, C or the counters
+  grid_dependents_go();
   const int tile = blockIdx.x / split;
   const int piece = blockIdx.x % split;
   const int m0 = (tile / tiles_n) * SB, n0 = (tile % tiles_n) * SB;
@@ -230,14 +232,12 @@ cudaError_t launch_gemm_bf16_small(int M, int N, int K, const uint16_t* A, int64
   if (p.split > 1 && (ws == nullptr || counters == nullptr)) return cudaErrorInvalidValue;
   const int blocks = p.tiles_m * p.tiles_n * p.split;
   const int vc = vec_c ? 1 : 0;
-  if (epi.act == kActGelu)
-    gemm_bf16_small_kernel<true><<<blocks, THREADS, 0, stream>>>(
-        M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
-  else
-    gemm_bf16_small_kernel<false><<<blocks, THREADS, 0, stream>>>(
-        M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
-  note_launches(1);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(
+      epi.act == kActGelu ? gemm_bf16_small_kernel<true> : gemm_bf16_small_kernel<false>,
+      dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, stream, M, N, K, A, lda, B, ldb, C,
+      ldc, p.tiles_n, p.split, vc, ws, counters, epi);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 }  // namespace g07

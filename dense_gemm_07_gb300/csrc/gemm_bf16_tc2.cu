@@ -543,6 +543,10 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after_sync();
+  // Set-up done (it touched no global memory): wait for the kernels before
+  // this one, and let the next one be scheduled as SMs free up.
+  grid_dependency_wait();
+  grid_dependents_go();
   const uint32_t tmem_base = ctl->tmem_base;
   const uint64_t tmo = wait_limit_ns(status);
   const unsigned int fault = status[1];
@@ -900,17 +904,18 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
       (tmW == nullptr || sk_sync == nullptr || sk_tag == 0 || (sk_tag >> 56) != 0))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.pairs), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = pair_smem_bytes();
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
   const cudaError_t e =

@@ -263,6 +263,8 @@ gemm_f32_regblock_kernel(int M, int N, int K, const float* __restrict__ A,
   extern __shared__ __align__(16) uint8_t smem_raw[];
   F32Stage<TN>* stage = reinterpret_cast<F32Stage<TN>*>(smem_raw);
   __shared__ int last_block;
+  grid_dependency_wait();  // before the first read of A, B, C or the counters
+  grid_dependents_go();
 
   // blocks [0, first): whole tiles 0 .. first - 1; then `split` blocks per
   // tile for tiles first, first + 1, ...
@@ -403,6 +405,8 @@ gemm_f32_small_kernel(int M, int N, int K, const float* __restrict__ A, int64_t 
                       EpiParams epi) {
   __shared__ __align__(16) SmallStage st[2];
   __shared__ int last_block;
+  grid_dependency_wait();  // before the first read of A, B, C or the counters
+  grid_dependents_go();
   const int tile = blockIdx.x / split;
   const int piece = blockIdx.x % split;
   const int m0 = (tile / tiles_n) * SB, n0 = (tile % tiles_n) * SB;
@@ -531,14 +535,13 @@ cudaError_t launch_part(int blocks, int M, int N, int K, const float* A,
                         int split, int vec_c, float* ws, unsigned int* counters,
                         const EpiParams& epi, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(STAGES) * sizeof(F32Stage<BN>);
-  if (epi.act == kActGelu)
-    gemm_f32_regblock_kernel<VEC_B, true><<<blocks, THREADS, smem, stream>>>(
-        M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
-        counters, epi);
-  else
-    gemm_f32_regblock_kernel<VEC_B, false><<<blocks, THREADS, smem, stream>>>(
-        M, N, K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
-        counters, epi);
+  auto kernel = epi.act == kActGelu ? gemm_f32_regblock_kernel<VEC_B, true>
+                                     : gemm_f32_regblock_kernel<VEC_B, false>;
+  const cudaError_t e =
+      launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), smem, stream, M, N,
+                 K, A, lda, B, ldb, C, ldc, tiles_m, tiles_n, first, split, vec_c, ws,
+                 counters, epi);
+  if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }
@@ -650,14 +653,11 @@ cudaError_t launch_gemm_f32(int M, int N, int K, const float* A, int64_t lda,
   cudaError_t e = cudaSuccess;
   if (p.small) {
     const int blocks = p.tiles_m * p.tiles_n * p.split;
-    if (vec_b)
-      gemm_f32_small_kernel<true><<<blocks, THREADS, 0, stream>>>(
-          M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
-    else
-      gemm_f32_small_kernel<false><<<blocks, THREADS, 0, stream>>>(
-          M, N, K, A, lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
-    note_launches(1);
-    return cudaGetLastError();
+    e = launch_pdl(vec_b ? gemm_f32_small_kernel<true> : gemm_f32_small_kernel<false>,
+                   dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, stream, M, N, K, A,
+                   lda, B, ldb, C, ldc, p.tiles_n, p.split, vc, ws, counters, epi);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
   }
   {
     const int blocks = p.full + p.tail * (p.tail > 0 ? p.split : 1);

@@ -11,6 +11,40 @@
 
 namespace g07 {
 
+// ---- programmatic dependent launch.  A kernel launched with
+// pdl_attribute() may be scheduled while the kernel before it on the stream
+// is still finishing; it calls grid_dependency_wait() before its first
+// access to global memory, which returns once every earlier kernel has
+// completed and its writes are visible (at once when there is nothing to
+// wait for).  grid_dependents_go() lets the next such kernel be scheduled
+// before this one ends; that kernel's own wait keeps it correct.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_go() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+// A plain launch (no cluster) with that attribute.
+template <typename... P, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Records `n` kernel launches by this library (defined in api.cu); the total
 // is exported through gemm_launch_count().
 void note_launches(int n);
