@@ -44,9 +44,8 @@ enum ScratchUse {
   kScratchStreamK = 0,  // BF16 stream-K partial sums + tagged sync words
   kScratchSplitK = 1,   // FP32 split-K counters (kept zero) + partial sums
   kScratchPack = 2,     // BF16 operands copied to aligned rows
-  kScratchGemv = 3,     // BF16 M = 1: counters (kept zero) + partial sums
-  kScratchSmall = 4,    // BF16 small problems: counters (kept zero) + partial tiles
-  kScratchUses = 5
+  kScratchSmall = 3,    // BF16 small problems: counters (kept zero) + partial tiles
+  kScratchUses = 4
 };
 struct StreamScratch {
   cudaStream_t stream = nullptr;
@@ -102,17 +101,6 @@ bool tma_store_ok(const void* C, int64_t N, int64_t ldc) {
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
-
-// M = 1: two counters per column block at the start of the scratch block, a
-// fixed area so that every call finds them zero whatever its size (each
-// launch's last range puts them back); partial sums after it.  Beyond 8192
-// column blocks the rows are not split.
-constexpr int64_t kGemvCounterBytes = 65536;
-int gemv_ranges_capped(int64_t N, int64_t K, int sms) {
-  const int64_t blocks = (N + kGemvCols - 1) / kGemvCols;
-  if (blocks * 8 > kGemvCounterBytes) return 1;
-  return gemv_ranges(static_cast<int>(N), static_cast<int>(K), sms);
-}
 
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
                          int64_t lda, const void* B, int64_t ldb,
@@ -234,23 +222,9 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
     p->workspace_bytes = sp.split > 1 ? kBf16SmallCounterBytes + sp.workspace_bytes : 0;
     return GEMM_OK;
   }
-  if (M == 1) {
-    // One row of A: B streamed through shared memory, products on the CUDA
-    // cores (the row ranges are reported for the 152 SMs of a GB300;
-    // launches use the device's count).
-    p->path = GEMM_PATH_BF16_GEMV;
-    p->tile_m = 1;
-    p->tile_n = kGemvCols;
-    p->tile_k = kGemvRows;
-    p->stages = kGemvStages;
-    p->split_k = gemv_ranges_capped(N, K, 152);
-    p->tiles = ((N + kGemvCols - 1) / kGemvCols) * p->split_k;
-    if (p->split_k > 1)
-      p->workspace_bytes += kGemvCounterBytes + gemv_workspace_bytes(static_cast<int>(N), p->split_k);
-    return GEMM_OK;
-  }
   if (M <= kSkinnyMaxM) {
-    // Small M: 128-column tiles of C, K split over a cluster (the split is
+    // Small M (M = 1 included): 128-column tiles of C, K split over a
+    // cluster (the split is
     // reported for the 152 SMs of a GB300; launches use the device's count
     // and lower the split until every cluster is resident at once).
     p->path = GEMM_PATH_BF16_SKINNY;
@@ -614,38 +588,6 @@ gemm_status_t run_f32(int64_t M, int64_t N, int64_t K, const float* A,
   return s;
 }
 
-// M = 1 on operands the copy engine can read in place (after any copy):
-// unswizzled maps of B (256 x 16 boxes) and of A's row (16-element boxes),
-// the counters and partial sums, the launch.
-gemm_status_t run_gemv(DeviceState* d, const uint16_t* a, int64_t lda, const uint16_t* b,
-                       int64_t ldb, float* C, int64_t N, int64_t K, const EpiParams& epi,
-                       cudaStream_t stream) {
-  const int n = static_cast<int>(N), k = static_cast<int>(K);
-  const int ranges = gemv_ranges_capped(N, K, d->sms);
-  CUtensorMap tmA, tmB;
-  gemm_status_t s = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, K, 1,
-                                   round_up(lda, 8), kGemvRows, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (s == GEMM_OK)
-    s = make_map_typed(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b, N, K, ldb, 256, kGemvRows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (s != GEMM_OK) return s;
-  void* ws = nullptr;
-  bool fresh = false, owned = false;
-  if (ranges > 1) {
-    s = call_scratch(d, stream, kScratchGemv,
-                     kGemvCounterBytes + gemv_workspace_bytes(n, ranges), &ws, &fresh, &owned);
-    if (s != GEMM_OK) return s;
-    if (fresh) s = from_cuda(cudaMemsetAsync(ws, 0, kGemvCounterBytes, stream));
-  }
-  if (s == GEMM_OK)
-    s = from_cuda(launch_gemm_bf16_gemv(
-        tmA, tmB, C, n, k, ranges,
-        ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kGemvCounterBytes) : nullptr,
-        static_cast<unsigned int*>(ws), d->status, epi, stream));
-  if (owned) pool_free(ws, stream);
-  return s;
-}
-
 gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
                        int64_t lda, const uint16_t* B, int64_t ldb, float* C,
                        int64_t ldc, cudaStream_t stream,
@@ -685,7 +627,7 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     return s;
   }
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
-  const bool paired = !skinny && plan.path != GEMM_PATH_BF16_GEMV;
+  const bool paired = !skinny;
   const int max_pairs = paired ? pair_max_active(stream) : 0;
   // The paired-SM kernel is the only kernel for M > 128: a device on which
   // no pair of its CTAs can be resident cannot run this GEMM.
@@ -722,12 +664,6 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (s == GEMM_OK)
     s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
                                 &b_op, &ldb_op, stream));
-  if (plan.path == GEMM_PATH_BF16_GEMV) {
-    if (s == GEMM_OK) s = run_gemv(d, a_op, lda_op, b_op, ldb_op, C, N, K, epi, stream);
-    if (owned) pool_free(ws, stream);
-    if (sk_owned) pool_free(sk, stream);
-    return s;
-  }
   CUtensorMap tmA, tmB;
   if (s == GEMM_OK)
     s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
@@ -1004,8 +940,7 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   CUtensorMap tmA, tmB;
   // M = 1 runs on the small-M kernel here: its cluster reduction needs no
   // counters, which the shared fixed scratch could not keep zero.
-  const bool skinny =
-      plan.path == GEMM_PATH_BF16_SKINNY || plan.path == GEMM_PATH_BF16_GEMV;
+  const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
   const int max_pairs = skinny ? 0 : pair_max_active(stream);
   if (!skinny && max_pairs <= 0) return GEMM_ERR_LAUNCH;
   if (s == GEMM_OK)
@@ -1199,7 +1134,7 @@ void gemm_shutdown(void) {
   cudaGetLastError();
 }
 
-int gemm_abi_version(void) { return 3; }
+int gemm_abi_version(void) { return 4; }
 
 int64_t gemm_set_bf16_small_limit(int64_t max_macs) {
   if (max_macs < 0) return -1;

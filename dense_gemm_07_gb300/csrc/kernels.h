@@ -153,23 +153,6 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
 // cluster, partial sums reduced through distributed shared memory.
 constexpr int kSkinnyMaxM = 128;
 constexpr int kSkinnyTileN = 128;
-// ---- BF16, M = 1 (gemm_bf16_gemv.cu): B streamed through shared memory,
-// products on the CUDA cores.  Blocks of kGemvCols columns x one of `ranges`
-// row ranges; B's map: boxes of 256 columns x kGemvRows rows, A's (one row):
-// boxes of kGemvRows elements, neither swizzled.
-constexpr int kGemvCols = 1024;
-constexpr int kGemvRows = 16;
-constexpr int kGemvStages = 6;
-// Row ranges per column block for an N x K problem on `sms` SMs (>= 1).
-int gemv_ranges(int N, int K, int sms);
-// Workspace of partial sums (0 when ranges == 1); the launch also needs two
-// zeroed counters per column block (each launch leaves them at zero).  With
-// ranges > 1 the launch is cooperative and needs blocks * ranges <= SMs.
-int64_t gemv_workspace_bytes(int N, int ranges);
-cudaError_t launch_gemm_bf16_gemv(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
-                                  int N, int K, int ranges, float* ws, unsigned int* counters,
-                                  unsigned int* status, const EpiParams& epi,
-                                  cudaStream_t stream);
 
 // MMA N used for M rows (16, 32, 64 or 128).
 int skinny_rows(int M);

@@ -252,12 +252,11 @@ GEMM07_API gemm_status_t gemm_get_device_status(void *stream);
  *   wait_ns: limit of every bounded wait inside the tensor-core kernels
  *            (0 restores the default of 2 s).
  *   mode 0:  normal operation.
- *   mode 1:  BF16 GEMMs (paired-SM path, small-M cluster path and
- *            M == 1) withhold the copy of their first k-slice (first
- *            stage), so a bounded wait runs out: the kernels unwind, return,
- *            and
- *            gemm_get_device_status() reports GEMM_ERR_TIMEOUT (C is then
- *            incomplete).  Nothing faults, traps or hangs.
+ *   mode 1:  BF16 tensor-core GEMMs (paired-SM path and small-M cluster
+ *            path, M == 1 included) withhold the copy of their first k-slice
+ *            (first stage), so a bounded wait runs out: the kernels unwind,
+ *            return, and gemm_get_device_status() reports GEMM_ERR_TIMEOUT
+ *            (C is then incomplete).  Nothing faults, traps or hangs.
  * Returns GEMM_ERR_INVALID_ARG for an unknown mode.  Not for production use.
  */
 GEMM07_API gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns);
@@ -265,9 +264,12 @@ GEMM07_API gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns);
 /* Releases per-device state held by the library (pools, status words). */
 GEMM07_API void gemm_shutdown(void);
 
-/* ABI version of this header: 3 (status codes numbered as in the boundary
- * definition: MISALIGNED = 2 reserved, UNSUPPORTED_DEVICE = 3, LAUNCH = 4,
- * TIMEOUT = 5, INTERNAL = 6; NO_MEMORY = 7 and SCRATCH_TOO_SMALL = 8 added). */
+/* ABI version of this header: 4.  Status codes are numbered as in the
+ * boundary definition (MISALIGNED = 2 reserved, UNSUPPORTED_DEVICE = 3,
+ * LAUNCH = 4, TIMEOUT = 5, INTERNAL = 6), with NO_MEMORY = 7 and
+ * SCRATCH_TOO_SMALL = 8 added (since version 3).  Since version 4, M == 1 is
+ * planned as GEMM_PATH_BF16_SKINNY and GEMM_PATH_BF16_GEMV is never
+ * returned. */
 GEMM07_API int gemm_abi_version(void);
 
 /*
@@ -298,14 +300,14 @@ typedef enum gemm_path {
     GEMM_PATH_F32_SIMT = 2,     /* gemm_f32 register-blocked kernel         */
     GEMM_PATH_BF16_TMA = 3,     /* tcgen05 kernel reading the operands      */
     GEMM_PATH_BF16_PACKED = 4,  /* operands copied to aligned workspace first */
-    GEMM_PATH_BF16_SKINNY = 5,  /* 2 <= M <= 128: 128-column tiles, K split
+    GEMM_PATH_BF16_SKINNY = 5,  /* 1 <= M <= 128: 128-column tiles, K split
                                    over a cluster, B streamed once (A/B may
                                    also be copied first: see pack_a / pack_b) */
-    GEMM_PATH_BF16_GEMV = 6,    /* M == 1: B streamed through shared memory in
-                                   1024-column blocks, FP32 products on the
-                                   CUDA cores, rows split into split_k ranges
-                                   added in range order (the no-allocation
-                                   entry point uses GEMM_PATH_BF16_SKINNY) */
+    GEMM_PATH_BF16_GEMV = 6,    /* reserved, never returned: ABI version 3's
+                                   M == 1 kernel (B streamed on the CUDA
+                                   cores); M == 1 now takes
+                                   GEMM_PATH_BF16_SKINNY, which was faster at
+                                   every shape measured */
     GEMM_PATH_BF16_SMALL = 7    /* few multiply-adds (gemm_set_bf16_small_limit):
                                    64 x 64 tiles on the CUDA cores, operands
                                    read in place at any alignment (no

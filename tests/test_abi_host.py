@@ -46,7 +46,7 @@ def test_library_is_in_tree_and_for_sm103a():
 
 
 def test_abi_version(lib):
-    assert _abi.gemm_abi_version() == 3
+    assert _abi.gemm_abi_version() == 4
 
 
 def test_status_numbering_follows_the_boundary_table():
@@ -119,14 +119,13 @@ def test_plan_paths():
     path, p = _path("bf16", 16, 4096, 4096)
     assert path == "bf16_skinny" and (p.tile_m, p.tile_n, p.split_k) == (16, 128, 4)
     assert p.tiles == 32 * 4
-    # M = 1: 1024-column blocks of B, rows split into 38 ranges (4 x 38 = 152
-    # blocks), partial sums in scratch after a fixed 64 KB of counters
+    # M = 1 takes the same small-M path (a 16-row MMA, rows 1..15 read as
+    # zeros), with no scratch for aligned operands
     path, p = _path("bf16", 1, 4096, 4096)
-    assert path == "bf16_gemv" and (p.tile_m, p.tile_n, p.tile_k, p.split_k) == (1, 1024, 16, 38)
-    assert p.tiles == 4 * 38 and p.workspace_bytes == 65536 + 4 * 38 * 1024 * 4
-    # one 16-row stage: a single range, no scratch
+    assert path == "bf16_skinny" and (p.tile_m, p.tile_n, p.split_k) == (16, 128, 4)
+    assert p.tiles == 32 * 4 and p.workspace_bytes == 0
     path, p = _path("bf16", 1, 1000, 16)
-    assert path == "bf16_gemv" and p.split_k == 1 and p.workspace_bytes == 0
+    assert path == "bf16_skinny" and p.split_k == 1 and p.workspace_bytes == 0
     assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
     assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
     with _small_limit(0):                                   # tensor-core kernels only
@@ -187,7 +186,7 @@ def test_plan_small_bf16_path():
     assert _path("bf16", 2, 1000, 1000)[0] == "bf16_skinny"
     assert _path("bf16", 8, 3001, 3001)[0] == "bf16_skinny"
     assert _path("bf16", 2, 8, 8)[0] == "bf16_small"
-    assert _path("bf16", 1, 127, 127)[0] == "bf16_gemv"          # M = 1 streams B
+    assert _path("bf16", 1, 127, 127)[0] == "bf16_skinny"        # M = 1: tensor cores
     # the limit is process-wide and settable; negative values are refused
     with _small_limit(1000):
         assert _path("bf16", 10, 10, 10)[0] == "bf16_small"      # lda = 10: A would be copied

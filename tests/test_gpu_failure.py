@@ -64,14 +64,14 @@ def test_stream_k_timeout_then_next_launch_exact():
 
 
 def test_vector_times_matrix_timeout_then_next_launch_exact():
-    # M = 1 kernel: its first stage is withheld, the consumers' bounded wait
-    # runs out; the counters of the row ranges are still put back, so the
-    # next launch is exact.
+    # M = 1 (on the small-M kernel): its first stage is withheld, the MMA
+    # issuers' bounded waits run out, every cluster unwinds; the next launch
+    # is exact.
     M, N, K = 1, 4096, 4096
     a, b = inputs.make_pair(M, N, K, 33, inputs.INT3, dtype=torch.bfloat16)
     a_d, b_d = a.cuda(), b.cuda()
     s, plan = g7.plan("bf16", M, N, K)
-    assert _abi.PATHS[plan.path] == "bf16_gemv" and plan.split_k > 1
+    assert _abi.PATHS[plan.path] == "bf16_skinny" and plan.split_k > 1
     assert g7.gemm_get_device_status() == _abi.GEMM_OK
     assert _abi.gemm_debug_inject(1, 20_000_000) == _abi.GEMM_OK
     try:

@@ -268,13 +268,13 @@ def test_bf16_skinny_exact(M):
                                    (1, 256, 65536), (1, 1100, 40), (1, 4096, 64),
                                    (1, 1000, 100), (1, 2048, 200), (1, 3000, 4096)])
 def test_bf16_vector_times_matrix_exact(shape):
-    # M = 1: B streamed in 1024-column blocks split into row ranges; ragged
-    # N (a partial or wholly out-of-range box), ragged K, B copied first
-    # (N = 3001, 127), K below one 16-row stage, long K (many ranges), and
-    # 2 to 6 ranges, whose column slices are wider than a block of threads
+    # M = 1 on the small-M kernel (one row of A in a 16-row MMA, the other
+    # rows zero-filled by the copy engine): ragged N (a partial or wholly
+    # out-of-range column tile), ragged K, B copied first (N = 3001, 127),
+    # K below one k-slice, long K (the K split over a cluster)
     M, N, K = shape
     s, plan = g7.plan("bf16", M, N, K)
-    assert _abi.PATHS[plan.path] == "bf16_gemv"
+    assert _abi.PATHS[plan.path] == "bf16_skinny"
     _check("bf16", M, N, K, 19, inputs.INT3, exact=True)
 
 
@@ -415,7 +415,7 @@ def test_bf16_vector_times_matrix_misaligned_bases(a_off, b_off):
     a_v, b_v = a_buf[:, a_off:K + a_off], b_buf[:, b_off:N + b_off]
     s, p = g7.plan("bf16", M, N, K, a_v.data_ptr(), a_v.stride(0),
                    b_v.data_ptr(), b_v.stride(0), 16, N)
-    assert g7.abi.PATHS[p.path] == "bf16_gemv"
+    assert g7.abi.PATHS[p.path] == "bf16_skinny"
     assert (p.pack_a, p.pack_b) == (a_off % 8 != 0, b_off % 8 != 0)
     c = g7.gemm_bf16_f32acc(a_v, b_v)
     torch.cuda.synchronize()
@@ -554,15 +554,15 @@ def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
         assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
 
 
-@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed", "bf16_gemv",
-                                  "bf16_small"])
+@pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed",
+                                  "bf16_m1_packed", "bf16_small"])
 def test_capture_on_fresh_stream_then_replay(case):
     # Captured on a stream the library has never seen: its scratch is then
     # allocated inside the graph (owned by it) rather than kept, and every
     # replay on new operand values is exact.
     kind = "f32" if case.startswith("f32") else "bf16"
     M, N, K = {"f32_split_k": (2560, 2048, 640), "bf16_stream_k": (2560, 2304, 1024),
-               "bf16_packed": (1000, 600, 1333), "bf16_gemv": (1, 4096, 4096),
+               "bf16_packed": (1000, 600, 1333), "bf16_m1_packed": (1, 3001, 1000),
                "bf16_small": (300, 258, 200)}[case]
     dtype = _dtype(kind)
     fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
@@ -571,7 +571,7 @@ def test_capture_on_fresh_stream_then_replay(case):
     c = torch.empty((M, N), dtype=torch.float32, device=DEV)
     prev = g7.abi.gemm_set_bf16_schedule(
         g7.abi.SCHEDULE_STREAM_K if case == "bf16_stream_k" else g7.abi.SCHEDULE_AUTO)
-    want = {"bf16_packed": "bf16_packed", "bf16_gemv": "bf16_gemv", "bf16_small": "bf16_small",
+    want = {"bf16_packed": "bf16_packed", "bf16_m1_packed": "bf16_skinny", "bf16_small": "bf16_small",
             "bf16_stream_k": "bf16_tma", "f32_split_k": "f32_simt"}[case]
     assert g7.abi.PATHS[g7.plan(kind, M, N, K)[1].path] == want
     try:
