@@ -492,6 +492,54 @@ __device__ __forceinline__ bool store_unit_rows(uint32_t taddr, float* C,
   return true;
 }
 
+// The same for a pair's last unit, whose operand ring is idle: all W / 32
+// chunks are first staged, each in a box of this warp's own in `wide` (no
+// chunk waits for another's stores), then the rows are stored chunk after
+// chunk with nothing between the stores.  Never a stream-K finish.
+template <int W, bool GELU>
+__device__ __forceinline__ void store_unit_rows_wide(uint32_t taddr, float* C, int64_t ldc,
+                                                     int row0, int n0, int M, int N,
+                                                     const EpiParams& epi, uint8_t* wide,
+                                                     int lane) {
+  const bool plain = epi.alpha == 1.0f && epi.beta == 0.0f && epi.bias == nullptr &&
+                     epi.act == 0;
+  const int rows = M - row0 < 32 ? M - row0 : 32;
+  if (rows <= 0) return;
+  int chunks = 0;  // chunks with columns inside C
+#pragma unroll 1
+  for (int c = 0; c < W / 32; ++c) {
+    if (n0 + c * 32 >= N) break;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    tmem_ld_wait();
+    uint8_t* rowp = wide + c * EPI_BOX_BYTES + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+          make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    ++chunks;
+  }
+  __syncwarp();
+  // column `lane` of a box row rr: 16-byte group lane / 4, swizzled by rr
+  const uint32_t in_group = static_cast<uint32_t>(lane & 3) * 4;
+  const uint32_t group = static_cast<uint32_t>(lane >> 2);
+#pragma unroll 1
+  for (int c = 0; c < chunks; ++c) {
+    const int gn = n0 + c * 32 + lane;
+    if (gn >= N) continue;
+    const float bias = epi.bias != nullptr ? epi.bias[gn] : 0.0f;
+    const uint8_t* box = wide + c * EPI_BOX_BYTES;
+    float* cp = C + static_cast<int64_t>(row0) * ldc + gn;
+#pragma unroll 8
+    for (int rr = 0; rr < rows; ++rr) {
+      const float v = *reinterpret_cast<const float*>(
+          box + rr * 128 + (((group ^ static_cast<uint32_t>(rr & 7)) << 4) | in_group));
+      float* dst = cp + static_cast<int64_t>(rr) * ldc;
+      *dst = plain ? v : epi_apply<GELU>(epi, v, epi.beta != 0.0f ? *dst : 0.0f, bias);
+    }
+  }
+}
+
 // GELU: whether the GELU activation is compiled in (epi_apply); the copy
 // without it serves every other epilogue.
 template <bool GELU>
@@ -799,14 +847,19 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           if (tma_c)
             store_unit_tma<BN / 2, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane,
                                    chunk, C, ldc, epi, nullptr, false, wide);
+          else if (wide)
+            store_unit_rows_wide<BN / 2, GELU>(taddr, C, ldc, row0, n0, M, N, epi, wide, lane);
           else
             store_unit_rows<BN / 2, GELU>(taddr, C, ldc, row0, n0, M, N, epi, nullptr,
                                     ebuf, lane, chunk);
+        } else if (tma_c) {
+          good = store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N, lane, chunk, C,
+                                          ldc, epi, cbp, reduce_c, wide);
+        } else if (wide) {
+          store_unit_rows_wide<BN, GELU>(taddr, C, ldc, row0, n0, M, N, epi, wide, lane);
         } else {
-          good = tma_c ? store_unit_tma<BN, GELU>(taddr, &tmC, ebuf, row0, n0, M, N,
-                                            lane, chunk, C, ldc, epi, cbp, reduce_c, wide)
-                       : store_unit_rows<BN, GELU>(taddr, C, ldc, row0, n0, M, N,
-                                             epi, cbp, ebuf, lane, chunk);
+          good = store_unit_rows<BN, GELU>(taddr, C, ldc, row0, n0, M, N, epi, cbp, ebuf,
+                                           lane, chunk);
         }
       }
       if (!good) {
