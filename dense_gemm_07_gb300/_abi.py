@@ -27,7 +27,8 @@ GEMM_ERR_SCRATCH_TOO_SMALL = 8
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 PATHS = {0: "none", 1: "zero_fill", 2: "f32_simt", 3: "bf16_tma",
-         4: "bf16_packed", 5: "bf16_skinny", 6: "bf16_gemv", 7: "bf16_small"}
+         4: "bf16_packed", 5: "bf16_skinny", 6: "bf16_gemv", 7: "bf16_small",
+         8: "bf16_narrow"}
 
 
 class GemmPlan(ctypes.Structure):

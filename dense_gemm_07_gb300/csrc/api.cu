@@ -236,6 +236,19 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
     p->tiles = ((N + kSkinnyTileN - 1) / kSkinnyTileN) * p->split_k;
     return GEMM_OK;
   }
+  if (N <= kNarrowMaxN) {
+    // Narrow N: 128-row tiles of C by all N columns, K split over a cluster
+    // (the split is reported for the 152 SMs of a GB300; launches use the
+    // device's count and lower the split until every cluster is resident).
+    p->path = GEMM_PATH_BF16_NARROW;
+    p->tile_m = kTcTileM;
+    p->tile_n = narrow_cols(static_cast<int>(N));
+    p->tile_k = kTcTileK;
+    p->stages = 0;
+    p->split_k = narrow_split(static_cast<int>(M), static_cast<int>(K), 152);
+    p->tiles = ((M + kTcTileM - 1) / kTcTileM) * p->split_k;
+    return GEMM_OK;
+  }
   // 256 x 256 tiles on SM pairs (the work sharing is reported for the 76
   // pairs of a 152-SM GB300; launches use the device's resident count).
   p->tile_m = kPairTileM;
@@ -627,7 +640,8 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     return s;
   }
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
-  const bool paired = !skinny;
+  const bool narrow = plan.path == GEMM_PATH_BF16_NARROW;
+  const bool paired = !skinny && !narrow;
   const int max_pairs = paired ? pair_max_active(stream) : 0;
   // The paired-SM kernel is the only kernel for M > 128: a device on which
   // no pair of its CTAs can be resident cannot run this GEMM.
@@ -671,6 +685,10 @@ gemm_status_t run_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A,
   if (s == GEMM_OK && skinny) {
     s = from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                           skinny_split_resident(m, n, k, d->sms), d->status,
+                                          epi, stream));
+  } else if (s == GEMM_OK && narrow) {
+    s = from_cuda(launch_gemm_bf16_narrow(tmA, tmB, C, ldc, m, n, k,
+                                          narrow_split_resident(m, n, k, d->sms), d->status,
                                           epi, stream));
   } else if (s == GEMM_OK) {
     CUtensorMap tmC;
@@ -938,11 +956,12 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   s = from_cuda(pack_operands(plan, A, lda, B, ldb, M, N, K, cursor, &a_op, &lda_op,
                               &b_op, &ldb_op, stream));
   CUtensorMap tmA, tmB;
-  // M = 1 runs on the small-M kernel here: its cluster reduction needs no
-  // counters, which the shared fixed scratch could not keep zero.
+  // The small-M and narrow-N kernels reduce through distributed shared
+  // memory: they put nothing in the array beyond the copies.
   const bool skinny = plan.path == GEMM_PATH_BF16_SKINNY;
-  const int max_pairs = skinny ? 0 : pair_max_active(stream);
-  if (!skinny && max_pairs <= 0) return GEMM_ERR_LAUNCH;
+  const bool narrow = plan.path == GEMM_PATH_BF16_NARROW;
+  const int max_pairs = skinny || narrow ? 0 : pair_max_active(stream);
+  if (!skinny && !narrow && max_pairs <= 0) return GEMM_ERR_LAUNCH;
   if (s == GEMM_OK)
     s = make_operand_maps(&tmA, &tmB, a_op, lda_op, b_op, ldb_op, M, N, K,
                           skinny ? static_cast<uint32_t>(skinny_rows(m)) : kTcTileM);
@@ -950,6 +969,10 @@ gemm_status_t run_bf16_noalloc(int64_t M, int64_t N, int64_t K,
   if (skinny)
     return from_cuda(launch_gemm_bf16_skinny(tmA, tmB, C, ldc, m, n, k,
                                              skinny_split_resident(m, n, k, d->sms),
+                                             d->status, epi_identity(), stream));
+  if (narrow)
+    return from_cuda(launch_gemm_bf16_narrow(tmA, tmB, C, ldc, m, n, k,
+                                             narrow_split_resident(m, n, k, d->sms),
                                              d->status, epi_identity(), stream));
   // Stream-K only when its scratch fits after the packed operands.
   PairSchedule ps =

@@ -149,6 +149,23 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
                                   unsigned int* status, const EpiParams& epi,
                                   cudaStream_t stream);
 
+// ---- BF16 narrow-N path (gemm_bf16_narrow.cu), N <= kNarrowMaxN and
+// M > kSkinnyMaxM: 128-row tiles of C by all N columns, split-K over a
+// cluster, partial sums reduced through distributed shared memory.
+constexpr int kNarrowMaxN = 128;
+// MMA N used for N columns (64 or 128).
+int narrow_cols(int N);
+// CTAs per cluster (k split) for an M x K problem on `sms` SMs (1..8).
+int narrow_split(int M, int K, int sms);
+// The same, lowered until every cluster of the launch fits on the current
+// device at once (host code).
+int narrow_split_resident(int M, int N, int K, int sms);
+// tmA: box {64, 128} (kTcTileM rows); tmB: the usual box {64, 64}.
+cudaError_t launch_gemm_bf16_narrow(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C,
+                                    int64_t ldc, int M, int N, int K, int cs,
+                                    unsigned int* status, const EpiParams& epi,
+                                    cudaStream_t stream);
+
 // ---- BF16 small-M path (gemm_bf16_skinny.cu): swap-AB, split-K over a
 // cluster, partial sums reduced through distributed shared memory.
 constexpr int kSkinnyMaxM = 128;

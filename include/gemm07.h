@@ -252,8 +252,8 @@ GEMM07_API gemm_status_t gemm_get_device_status(void *stream);
  *   wait_ns: limit of every bounded wait inside the tensor-core kernels
  *            (0 restores the default of 2 s).
  *   mode 0:  normal operation.
- *   mode 1:  BF16 tensor-core GEMMs (paired-SM path and small-M cluster
- *            path, M == 1 included) withhold the copy of their first k-slice
+ *   mode 1:  BF16 tensor-core GEMMs (paired-SM path, small-M and narrow-N
+ *            cluster paths, M == 1 included) withhold the copy of their first k-slice
  *            (first stage), so a bounded wait runs out: the kernels unwind,
  *            return, and gemm_get_device_status() reports GEMM_ERR_TIMEOUT
  *            (C is then incomplete).  Nothing faults, traps or hangs.
@@ -268,8 +268,8 @@ GEMM07_API void gemm_shutdown(void);
  * boundary definition (MISALIGNED = 2 reserved, UNSUPPORTED_DEVICE = 3,
  * LAUNCH = 4, TIMEOUT = 5, INTERNAL = 6), with NO_MEMORY = 7 and
  * SCRATCH_TOO_SMALL = 8 added (since version 3).  Since version 4, M == 1 is
- * planned as GEMM_PATH_BF16_SKINNY and GEMM_PATH_BF16_GEMV is never
- * returned. */
+ * planned as GEMM_PATH_BF16_SKINNY, GEMM_PATH_BF16_GEMV is never returned,
+ * and N <= 128 < M is planned as GEMM_PATH_BF16_NARROW. */
 GEMM07_API int gemm_abi_version(void);
 
 /*
@@ -308,12 +308,16 @@ typedef enum gemm_path {
                                    cores); M == 1 now takes
                                    GEMM_PATH_BF16_SKINNY, which was faster at
                                    every shape measured */
-    GEMM_PATH_BF16_SMALL = 7    /* few multiply-adds (gemm_set_bf16_small_limit):
+    GEMM_PATH_BF16_SMALL = 7,   /* few multiply-adds (gemm_set_bf16_small_limit):
                                    64 x 64 tiles on the CUDA cores, operands
                                    read in place at any alignment (no
                                    copies), K split into split_k ranges added
                                    in range order (not used by the
                                    no-allocation entry point) */
+    GEMM_PATH_BF16_NARROW = 8   /* N <= 128 < M: 128-row tiles by all N
+                                   columns, K split over a cluster, A
+                                   streamed once (A/B may also be copied
+                                   first: see pack_a / pack_b) */
 } gemm_path_t;
 
 typedef struct gemm_plan {

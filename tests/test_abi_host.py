@@ -126,6 +126,16 @@ def test_plan_paths():
     assert p.tiles == 32 * 4 and p.workspace_bytes == 0
     path, p = _path("bf16", 1, 1000, 16)
     assert path == "bf16_skinny" and p.split_k == 1 and p.workspace_bytes == 0
+    # N <= 128 < M: narrow-N path, 128-row tiles by all N columns (MMA N 64
+    # or 128), K split 4 ways over 32 row tiles
+    path, p = _path("bf16", 4096, 128, 4096)
+    assert path == "bf16_narrow" and (p.tile_m, p.tile_n, p.split_k) == (128, 128, 4)
+    assert p.tiles == 32 * 4 and p.workspace_bytes == 0
+    assert _path("bf16", 4096, 64, 4096)[1].tile_n == 64
+    assert _path("bf16", 4096, 65, 4096)[1].tile_n == 128
+    assert _path("bf16", 20000, 100, 4096)[1].split_k == 1     # 157 tiles: no split
+    assert _path("bf16", 4096, 136, 4096)[0] == "bf16_tma"     # wider: SM pairs
+    assert _path("bf16", 128, 64, 4096)[0] == "bf16_skinny"    # M <= 128 first
     assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
     assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
     with _small_limit(0):                                   # tensor-core kernels only

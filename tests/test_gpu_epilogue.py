@@ -63,8 +63,10 @@ PATHS = [
     ("bf16", 512, 1024, 8192, None, TC),   # tiles halved along K; alpha-only: finished in C
     ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K, TC),  # stream-K over every tile
     ("bf16", 48, 1000, 777, None, TC),   # small M, cluster reduction
-    ("bf16", 1, 4096, 4096, None, TC),   # M = 1: range sums added by the row ranges
-    ("bf16", 1, 1000, 40, None, TC),     # M = 1, one range: finished in place
+    ("bf16", 1, 4096, 4096, None, TC),   # M = 1 on the small-M kernel, K split
+    ("bf16", 1, 1000, 40, None, TC),     # M = 1, one k-slice: no split
+    ("bf16", 1000, 100, 777, None, TC),  # narrow N (MMA N = 128), cluster reduction
+    ("bf16", 3001, 64, 2000, None, TC),  # narrow N (MMA N = 64), rows of A copied
     ("bf16", 300, 258, 200, None, "default"),   # small problem on the CUDA cores, split K
     ("bf16", 2000, 1000, 60, None, "default"),  # small problem, no split: finished in place
     ("f32", 200, 190, 300, None, "default"),    # FP32 small problem: 64 x 64 tiles split along K

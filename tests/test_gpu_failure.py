@@ -86,6 +86,29 @@ def test_vector_times_matrix_timeout_then_next_launch_exact():
     assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
 
 
+def test_narrow_n_cluster_timeout_then_next_launch_exact():
+    # Narrow-N kernel: every CTA withholds its first k-slice, the MMA
+    # issuers' bounded waits run out, every cluster unwinds and meets at its
+    # final barrier; the next launch is exact.
+    M, N, K = 4096, 128, 4096
+    a, b = inputs.make_pair(M, N, K, 36, inputs.INT3, dtype=torch.bfloat16)
+    a_d, b_d = a.cuda(), b.cuda()
+    s, plan = g7.plan("bf16", M, N, K)
+    assert _abi.PATHS[plan.path] == "bf16_narrow" and plan.split_k > 1
+    assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    assert _abi.gemm_debug_inject(1, 20_000_000) == _abi.GEMM_OK
+    try:
+        g7.gemm_bf16_f32acc(a_d, b_d)
+        assert g7.gemm_get_device_status() == _abi.GEMM_ERR_TIMEOUT
+    finally:
+        assert _abi.gemm_debug_inject(0, 0) == _abi.GEMM_OK
+    c = g7.gemm_bf16_f32acc(a_d, b_d)
+    torch.cuda.synchronize()
+    assert g7.gemm_get_device_status() == _abi.GEMM_OK
+    c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+    assert_within("bf16", c.cpu().numpy(), c_ref, None, exact=True)
+
+
 @pytest.mark.parametrize("M", [16, 100])
 def test_small_m_cluster_timeout_then_next_launch_exact(M):
     # Small-M kernel (clusters of CTAs splitting K): every CTA withholds its

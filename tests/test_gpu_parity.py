@@ -307,6 +307,40 @@ def test_bf16_small_m_normal_values():
     _check("bf16", 24, 3000, 4096, 19, inputs.NORMAL, inputs.NORMAL_W)
 
 
+@pytest.mark.parametrize("shape", [(129, 1, 64), (300, 16, 1000), (1000, 64, 3001),
+                                   (1000, 65, 777), (3001, 127, 3001), (3001, 127, 1000),
+                                   (4096, 128, 4096), (2048, 96, 4096), (20000, 100, 200),
+                                   (257, 128, 8192), (700, 33, 1)])
+@pytest.mark.parametrize("route", ROUTES)
+def test_bf16_narrow_n_paths_exact(shape, route):
+    # N <= 128 < M on the narrow-N kernel: both MMA widths (64, 128), ragged
+    # M (a partial 128-row tile), N and K, copied operands (127, 3001), a K
+    # split of up to 8 per cluster, more tiles than SMs (no split), K below
+    # one slice; and the same shapes on the CUDA-core path where they are
+    # small
+    M, N, K = shape
+    with route_limit(route):
+        s, plan = g7.plan("bf16", M, N, K)
+    if route == "tensor_cores":
+        assert _abi.PATHS[plan.path] == "bf16_narrow"
+    _check("bf16", M, N, K, 21, inputs.INT3, exact=True, route=route)
+
+
+def test_bf16_narrow_n_normal_values_and_bits():
+    # N(0,1) inputs within the BF16 bound; the split's partial sums are added
+    # in rank order, so repeated calls give the same bits
+    a, b = inputs.make_pair(3000, 96, 4096, 22, inputs.NORMAL, inputs.NORMAL_W,
+                            dtype=torch.bfloat16)
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    first = g7.gemm_bf16_f32acc(a_d, b_d).clone()
+    for _ in range(3):
+        again = g7.gemm_bf16_f32acc(a_d, b_d)
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    c_ref, s_ref = oracle_ref("bf16", a, b)
+    assert_within("bf16", first.cpu().numpy(), c_ref, s_ref)
+    assert g7.gemm_get_device_status() == 0
+
+
 # ------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("kind", ["f32", "bf16"])

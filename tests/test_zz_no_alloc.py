@@ -134,8 +134,8 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
 
 
 def test_noalloc_single_row_exact():
-    # M = 1 runs on the small-M kernel here; A's single row of 3001 elements
-    # (not a multiple of 16 bytes) is read in place, only B is copied
+    # M = 1 runs on the small-M kernel; A's single row of 3001 elements (not
+    # a multiple of 16 bytes) is read in place, and so is B
     M, N, K = 1, 1000, 3001
     a, b = inputs.make_pair(M, N, K, 23, inputs.INT3, dtype=torch.bfloat16)
     a_d, b_d = a.to(DEV), b.to(DEV)
@@ -145,3 +145,20 @@ def test_noalloc_single_row_exact():
     assert g7.gemm_get_device_status() == 0
     c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
     assert np.array_equal(out.cpu().numpy().astype(np.float64), c_ref)
+
+
+def test_noalloc_narrow_n_exact():
+    # N <= 128 < M runs on the narrow-N kernel (cluster reduction, nothing in
+    # the array); B's rows of 100 elements are copied into it first
+    M, N, K = 3001, 100, 1000
+    a, b = inputs.make_pair(M, N, K, 24, inputs.INT3, dtype=torch.bfloat16)
+    s, plan = g7.plan("bf16", M, N, K)
+    assert _abi.PATHS[plan.path] == "bf16_narrow" and plan.pack_b == 1
+    a_d, b_d = a.to(DEV), b.to(DEV)
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    for _ in range(2):
+        assert _noalloc(a_d, b_d, out) == _abi.GEMM_OK
+        torch.cuda.synchronize()
+        assert g7.gemm_get_device_status() == 0
+        c_ref, _ = oracle_ref("bf16", a, b, with_abs=False)
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), c_ref)
