@@ -23,8 +23,9 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 std::atomic<int64_t> g_small_limit{kBf16SmallMaxMacs};
 bool bf16_small_problem(int64_t M, int64_t N, int64_t K, bool needs_copy) {
   const int64_t lim = g_small_limit.load();
-  const int64_t max_macs =
-      needs_copy ? lim : (lim < kBf16SmallAlignedMacs ? lim : kBf16SmallAlignedMacs);
+  const int64_t cap = needs_copy && K <= kBf16SmallShortK ? kBf16SmallCopyMacs
+                                                          : kBf16SmallAlignedMacs;
+  const int64_t max_macs = lim < cap ? lim : cap;
   return M >= 2 && (M >= 64 || N * K <= (int64_t(1) << 19)) && M * N * K <= max_macs;
 }
 

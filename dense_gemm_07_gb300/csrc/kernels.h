@@ -96,13 +96,21 @@ struct Bf16SmallPlan {
   int64_t workspace_bytes = 0;  // partial tiles (after kBf16SmallCounterBytes of counters)
 };
 // Problems run there (measured crossovers on a GB300, CUDA events):
-//   * M >= 2 (M = 1 keeps the vector-times-matrix kernel, which streams B);
+//   * M >= 2 (M = 1 keeps the small-M tensor-core kernel, which streams B);
 //   * M >= 64 or B of at most 2^19 elements (for few rows and a larger B
 //     the small-M tensor-core kernel streams B much faster);
-//   * at most the set limit of multiply-adds, by default kBf16SmallMaxMacs,
-//     when an operand would have to be copied to an aligned layout for the
-//     tensor-core kernels, else at most min(limit, kBf16SmallAlignedMacs).
+//   * at most the set limit of multiply-adds (by default kBf16SmallMaxMacs)
+//     and at most kBf16SmallCopyMacs when an operand would have to be
+//     copied to an aligned layout for the tensor-core kernels and K is at
+//     most kBf16SmallShortK, else at most kBf16SmallAlignedMacs: past those
+//     the tensor-core kernels (small-M, narrow-N or paired) are faster,
+//     copy included (1000 x 127 x 1000: 10.2 against 17.5 us; 1000 x 1000 x
+//     127: 9.7 against 13.4; 127 x 127 x 3001: 14.3 against 17.8), below
+//     them slower (3001 x 127 x 127: 14.0 against 10.3; 127 x 3001 x 127:
+//     14.0 against 11.8).
 constexpr int64_t kBf16SmallMaxMacs = int64_t(1) << 27;
+constexpr int64_t kBf16SmallCopyMacs = int64_t(1) << 26;
+constexpr int64_t kBf16SmallShortK = 512;
 constexpr int64_t kBf16SmallAlignedMacs = int64_t(1) << 24;
 bool bf16_small_problem(int64_t M, int64_t N, int64_t K, bool needs_copy);
 // Fixed counter area at the start of the scratch block (one counter per

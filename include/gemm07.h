@@ -377,11 +377,11 @@ GEMM07_API int gemm_set_bf16_schedule(int schedule);
  * gemm_set_bf16_small_limit: the largest number of multiply-adds (M * N * K)
  * of a BF16 call that takes GEMM_PATH_BF16_SMALL, for calls issued after it
  * returns, process-wide.  That path also needs M >= 2, and M >= 64 or
- * N * K <= 2^19; when the tensor-core kernels could read both operands in
- * place (no copy needed) the limit is at most 2^24.  0 sends every call to
- * the tensor-core kernels.  Default 2^27 (the measured crossovers on a
- * GB300).  Returns the previous limit, or -1 (nothing changed) for a
- * negative value.  No GPU needed.
+ * N * K <= 2^19, and is capped below the limit: at 2^26 when the
+ * tensor-core kernels would first copy an operand and K <= 512, else at
+ * 2^24 (the measured crossovers on a GB300).  0 sends every call to the
+ * tensor-core kernels.  Default 2^27.  Returns the previous limit, or -1
+ * (nothing changed) for a negative value.  No GPU needed.
  */
 GEMM07_API int64_t gemm_set_bf16_small_limit(int64_t max_macs);
 

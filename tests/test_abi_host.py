@@ -185,8 +185,13 @@ def test_plan_small_bf16_path():
     assert path == "bf16_small" and p.pack_a == 0
     path, p = _path("bf16", 3001, 127, 127)
     assert path == "bf16_small" and p.split_k == 3 and p.tiles == 47 * 2 * 3   # 304 // 94 = 3
-    path, p = _path("bf16", 1000, 1000, 127)            # 127 M multiply-adds, A would be copied
-    assert path == "bf16_small" and p.split_k == 1 and p.workspace_bytes == 0
+    # an operand would be copied: up to 2^26 with K <= 512, else up to 2^24
+    path, p = _path("bf16", 1000, 500, 127)             # 63.5 M, A would be copied
+    assert path == "bf16_small" and p.pack_a == 0 and p.split_k == 2   # 304 // 128 tiles
+    assert _path("bf16", 1000, 1000, 127)[0] == "bf16_packed"     # 127 M: tensor cores
+    assert _path("bf16", 127, 127, 1000)[0] == "bf16_small"       # 16.1 M, long K
+    assert _path("bf16", 127, 127, 3001)[0] == "bf16_skinny"      # 48 M, long K
+    assert _path("bf16", 1000, 127, 1000)[0] == "bf16_narrow"     # 127 M
     # operands the tensor-core kernels read in place: only up to 2^24
     assert _path("bf16", 256, 256, 256)[0] == "bf16_small"        # 2^24
     assert _path("bf16", 256, 256, 264)[0] == "bf16_tma"

@@ -68,7 +68,7 @@ PATHS = [
     ("bf16", 1000, 100, 777, None, TC),  # narrow N (MMA N = 128), cluster reduction
     ("bf16", 3001, 64, 2000, None, TC),  # narrow N (MMA N = 64), rows of A copied
     ("bf16", 300, 258, 200, None, "default"),   # small problem on the CUDA cores, split K
-    ("bf16", 2000, 1000, 60, None, "default"),  # small problem, no split: finished in place
+    ("bf16", 2000, 500, 60, None, "default"),   # small problem, no split: finished in place
     ("f32", 200, 190, 300, None, "default"),    # FP32 small problem: 64 x 64 tiles split along K
     ("f32", 640, 520, 2000, None, "default"),   # FP32, one partial wave split along K
     ("f32", 2560, 2048, 640, None, "default"),  # FP32, whole waves + split tail
