@@ -129,7 +129,8 @@ def test_unknown_activation_rejected():
     ("bf16", 700, 900, 1000, None, "default"), ("bf16", 300, 258, 200, None, TC),
     ("bf16", 48, 1000, 777, None, TC), ("bf16", 1, 3000, 3001, None, "default"),
     ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K, "default"),
-    ("bf16", 300, 258, 200, None, "default"), ("bf16", 48, 500, 777, None, "default")])
+    ("bf16", 300, 258, 200, None, "default"), ("bf16", 48, 500, 777, None, "default"),
+    ("bf16", 2000, 100, 1000, None, TC)])
 def test_epilogue_gelu(kind, M, N, K, schedule, route):
     # GELU after alpha, beta and the bias on every path.  Bound: GELU's slope
     # is at most 1.13, so the pre-activation bound grows by that factor; the
