@@ -172,9 +172,10 @@ GEMM07_API gemm_status_t gemm_bf16_f32acc_ex(int64_t M, int64_t N, int64_t K,
  *        synchronisation words (tickets, ready and cleared flags).
  *   A request whose copies (1 and 2) need more than the array returns
  *   GEMM_ERR_SCRATCH_TOO_SMALL before anything is enqueued; when 3 does not
- *   fit after them, the call runs without the K split instead.  M = 1 runs
- *   on the small-M kernel here, which reduces through shared memory and
- *   puts nothing in the array beyond 1 and 2.
+ *   fit after them, the call runs without the K split instead.  M <= 128
+ *   (M = 1 included) and N <= 128 < M run on the small-M and narrow-N
+ *   kernels, which reduce through shared memory and put nothing in the
+ *   array beyond 1 and 2.
  *   Sharing: every call on a device uses the same array and it keeps the
  *   last call's contents.  ANY two calls whose kernels may overlap on the
  *   GPU (on different streams without ordering between them) race on it,
