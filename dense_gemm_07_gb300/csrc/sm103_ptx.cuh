@@ -401,7 +401,9 @@ __device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem,
 }
 
 // Arrive once on the mbarrier at this offset in every CTA of `cta_mask` when
-// the pair MMAs issued so far have completed.
+// the pair MMAs issued so far have completed (a completion signal to both
+// CTAs of the pair; no data is copied, and no TMA load here or elsewhere
+// multicasts).
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar,
                                                 uint16_t cta_mask) {
   asm volatile(
