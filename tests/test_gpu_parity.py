@@ -589,7 +589,7 @@ def test_bf16_stream_k_in_cuda_graph_replays_exact(stream_k):
 
 
 @pytest.mark.parametrize("case", ["f32_split_k", "bf16_stream_k", "bf16_packed",
-                                  "bf16_m1_packed", "bf16_small"])
+                                  "bf16_m1_packed", "bf16_narrow", "bf16_small"])
 def test_capture_on_fresh_stream_then_replay(case):
     # Captured on a stream the library has never seen: its scratch is then
     # allocated inside the graph (owned by it) rather than kept, and every
@@ -597,6 +597,7 @@ def test_capture_on_fresh_stream_then_replay(case):
     kind = "f32" if case.startswith("f32") else "bf16"
     M, N, K = {"f32_split_k": (2560, 2048, 640), "bf16_stream_k": (2560, 2304, 1024),
                "bf16_packed": (1000, 600, 1333), "bf16_m1_packed": (1, 3001, 1000),
+               "bf16_narrow": (3001, 100, 1000),
                "bf16_small": (300, 258, 200)}[case]
     dtype = _dtype(kind)
     fn = g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc
@@ -605,7 +606,8 @@ def test_capture_on_fresh_stream_then_replay(case):
     c = torch.empty((M, N), dtype=torch.float32, device=DEV)
     prev = g7.abi.gemm_set_bf16_schedule(
         g7.abi.SCHEDULE_STREAM_K if case == "bf16_stream_k" else g7.abi.SCHEDULE_AUTO)
-    want = {"bf16_packed": "bf16_packed", "bf16_m1_packed": "bf16_skinny", "bf16_small": "bf16_small",
+    want = {"bf16_packed": "bf16_packed", "bf16_m1_packed": "bf16_skinny",
+            "bf16_narrow": "bf16_narrow", "bf16_small": "bf16_small",
             "bf16_stream_k": "bf16_tma", "f32_split_k": "f32_simt"}[case]
     assert g7.abi.PATHS[g7.plan(kind, M, N, K)[1].path] == want
     try:
