@@ -56,6 +56,7 @@
 // expiry the CTA raises its own and its peer's abort flag and the status
 // word, all roles unwind, copies and MMAs in flight are drained, and both
 // CTAs meet at a final cluster barrier before tensor memory is released.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -894,11 +895,11 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
-struct LaunchInfo {
-  int ready = 0;
-  int max_pairs = 0;
-};
-LaunchInfo g_info[64];
+// Per device: 0 until the shared-memory attribute is set and the occupancy
+// known, then the number of resident pairs + 1.  One atomic word, so that
+// a thread that finds it set also finds the attribute set (calls may come
+// from several host threads at once).
+std::atomic<int> g_pairs_plus1[64];
 
 }  // namespace
 
@@ -910,8 +911,9 @@ size_t pair_smem_bytes() {
 int pair_max_active(cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  LaunchInfo& li = g_info[dev];
-  if (!li.ready) {
+  const int known = g_pairs_plus1[dev].load(std::memory_order_acquire);
+  if (known > 0) return known - 1;
+  {
     const size_t smem = pair_smem_bytes();
     if (cudaFuncSetAttribute(gemm_bf16_pair_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -938,10 +940,9 @@ int pair_max_active(cudaStream_t stream) {
       cudaGetLastError();
       return 0;
     }
-    li.max_pairs = clusters;
-    li.ready = 1;
+    g_pairs_plus1[dev].store(clusters + 1, std::memory_order_release);
+    return clusters;
   }
-  return li.max_pairs;
 }
 
 cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,

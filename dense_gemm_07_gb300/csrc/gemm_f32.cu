@@ -29,6 +29,7 @@
 // Thread layout: 8 warps as 4 (M) x 2 (N), each warp a 32 x 64 sub-tile;
 // lane (ly = lane/8, lx = lane%8) owns rows {4ly..4ly+3, 16+4ly..16+4ly+3}
 // and columns {4lx..4lx+3, 32+4lx..32+4lx+3} of its warp's sub-tile.
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -553,8 +554,11 @@ cudaError_t set_smem_attr() {
                               static_cast<int>(STAGES * sizeof(F32Stage<BN>)));
 }
 
-int g_attr_set[64];
-int64_t g_slots[64];
+// Per device: 0 until the shared-memory attributes are set and the
+// occupancy known, then the number of resident blocks + 1.  One atomic
+// word, so that a thread that finds it set also finds the attributes set
+// (calls may come from several host threads at once).
+std::atomic<int64_t> g_slots_plus1[64];
 
 }  // namespace
 
@@ -562,7 +566,9 @@ int64_t g_slots[64];
 int64_t f32_slots() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!g_attr_set[dev]) {
+  const int64_t known = g_slots_plus1[dev].load(std::memory_order_acquire);
+  if (known > 0) return known - 1;
+  {
     if (set_smem_attr<true, false>() != cudaSuccess ||
         set_smem_attr<false, false>() != cudaSuccess ||
         set_smem_attr<true, true>() != cudaSuccess ||
@@ -576,10 +582,10 @@ int64_t f32_slots() {
       cudaGetLastError();
       return 0;
     }
-    g_slots[dev] = static_cast<int64_t>(sms) * per_sm;
-    g_attr_set[dev] = 1;
+    const int64_t slots = static_cast<int64_t>(sms) * per_sm;
+    g_slots_plus1[dev].store(slots + 1, std::memory_order_release);
+    return slots;
   }
-  return g_slots[dev];
 }
 
 F32Plan f32_plan(int M, int N, int K, int64_t slots) {
