@@ -46,6 +46,18 @@ def _check(kind, M, N, K, seed, dist, dist_b=None, exact=False, rows=None, route
 
 # ------------------------------------------------------------ FP32 (SIMT)
 
+@pytest.mark.parametrize("shape,tile", [
+    ((512, 512, 512), 64), ((513, 512, 512), 128), ((512, 512, 2049), 128),
+    ((1, 4096, 4096), 128), ((4096, 1, 4096), 128), ((1, 1, 1), 64), ((2048, 2048, 1), 128)])
+def test_f32_path_transitions_exact(shape, tile):
+    # each side of the small-problem limit (16 tiles of 128 x 128 and 2^29
+    # multiply-adds), a single row or column over a long K, and K = 1
+    M, N, K = shape
+    s, p = g7.plan("f32", M, N, K)
+    assert s == 0 and p.tile_m == tile
+    _check("f32", M, N, K, 24, inputs.INT3, exact=True)
+
+
 def test_f32_256_uniform():
     _check("f32", 256, 256, 256, 0, inputs.UNIFORM)
 
@@ -301,6 +313,24 @@ def test_bf16_small_m_paths_exact(shape, route):
     # count; and the same shapes on the CUDA-core small-problem path
     M, N, K = shape
     _check("bf16", M, N, K, 18, inputs.INT3, exact=True, route=route)
+
+
+@pytest.mark.parametrize("shape,path", [
+    ((128, 4096, 512), "bf16_skinny"), ((129, 4096, 512), "bf16_tma"),
+    ((4096, 128, 512), "bf16_narrow"), ((4096, 129, 512), "bf16_packed"),
+    ((128, 128, 512), "bf16_skinny"), ((129, 128, 512), "bf16_narrow"),
+    ((129, 129, 64), "bf16_packed"), ((1, 1, 1), "bf16_skinny"), ((129, 1, 1), "bf16_narrow"),
+    ((128, 129, 65), "bf16_skinny"), ((129, 4096, 1), "bf16_packed"),
+    ((4096, 129, 65), "bf16_packed")])
+def test_bf16_path_transitions_exact(shape, path):
+    # each side of the points where the plan changes kernel: M = 128 / 129
+    # (small-M kernel / SM pairs), N = 128 / 129 (narrow-N kernel / SM
+    # pairs), both together, and K of one element or just over one k-slice
+    M, N, K = shape
+    with route_limit("tensor_cores"):
+        s, p = g7.plan("bf16", M, N, K)
+        assert s == 0 and g7.abi.PATHS[p.path] == path
+        _check("bf16", M, N, K, 23, inputs.INT3, exact=True, route="tensor_cores")
 
 
 def test_bf16_small_m_normal_values():
