@@ -77,8 +77,10 @@ PATHS = [
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: f"{p[0]}-{p[1]}x{p[2]}x{p[3]}-{p[5]}")
 @pytest.mark.parametrize("epi", [(2.0, -1.0, True, "none"), (1.0, 0.0, True, "relu"),
-                                 (-3.0, 2.0, False, "relu"), (0.5, 0.0, False, "none")],
-                         ids=["ab+c+bias", "bias+relu", "beta_relu", "alpha_only"])
+                                 (-3.0, 2.0, False, "relu"), (0.5, 0.0, False, "none"),
+                                 (0.0, 1.0, True, "none")],
+                         ids=["ab+c+bias", "bias+relu", "beta_relu", "alpha_only",
+                              "no_product"])
 def test_epilogue_exact_integers(path, epi):
     kind, M, N, K, schedule, route = path
     alpha, beta, use_bias, act = epi

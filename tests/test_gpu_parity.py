@@ -384,6 +384,33 @@ def test_zero_k_writes_zeros(kind):
     assert_guards_intact(buf, 37, 45, 50)
 
 
+@pytest.mark.parametrize("kind,M,N,K,route", [
+    ("f32", 300, 260, 200, "default"), ("f32", 700, 900, 1000, "default"),
+    ("bf16", 520, 600, 448, "tensor_cores"), ("bf16", 16, 1200, 448, "tensor_cores"),
+    ("bf16", 1000, 100, 1200, "tensor_cores"), ("bf16", 200, 300, 150, "default")])
+def test_non_finite_inputs_propagate(kind, M, N, K, route):
+    # A NaN in A[i0, k0] and +Inf in B[k1, j1] (k1 != k0): row i0 of C is NaN
+    # (NaN times anything), column j1 is not finite (+-Inf, or NaN where
+    # A[i, k1] = 0), and every other element is finite and exact, as the
+    # two entries do not enter it
+    a, b = inputs.make_pair(M, N, K, 25, inputs.INT3, dtype=_dtype(kind))
+    i0, k0, k1, j1 = M // 2, K // 3, (2 * K) // 3, N - 1
+    a_bad, b_bad = a.clone(), b.clone()
+    a_bad[i0, k0] = float("nan")
+    b_bad[k1, j1] = float("inf")
+    with route_limit(route):
+        c = _run(kind, a_bad, b_bad).cpu().numpy()
+    assert np.all(np.isnan(c[i0])), "row of the NaN"
+    assert not np.any(np.isfinite(c[:, j1])), "column of the Inf"
+    c_ref, _ = oracle_ref(kind, a, b, with_abs=False)
+    keep = np.ones((M, N), dtype=bool)
+    keep[i0] = False
+    keep[:, j1] = False
+    assert np.all(np.isfinite(c[keep]))
+    assert np.array_equal(c[keep].astype(np.float64), c_ref[keep])
+    assert g7.gemm_get_device_status() == 0
+
+
 @pytest.mark.parametrize("kind", ["f32", "bf16"])
 def test_empty_m_or_n_is_noop(kind):
     buf, c = guarded_output(0, 5, 8, DEV)
