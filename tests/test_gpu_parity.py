@@ -602,6 +602,36 @@ def test_streams_are_respected():
     assert_within("bf16", c.cpu().numpy(), c_ref, s_ref, exact=True)
 
 
+@pytest.mark.parametrize("kind,M,N,K,route", [
+    ("bf16", 4096, 1024, 4096, "default"),        # paired SMs, operands read in place
+    ("bf16", 3001, 1000, 1001, "default"),        # operand copy kernel first
+    ("bf16", 16, 4096, 4096, "default"),          # small M
+    ("bf16", 4096, 100, 4096, "default"),         # narrow N
+    ("bf16", 300, 258, 200, "default"),           # small problem, CUDA cores
+    ("f32", 2048, 2048, 2048, "default"), ("f32", 256, 256, 256, "default")])
+def test_reads_wait_for_the_previous_kernel(kind, M, N, K, route):
+    # Every kernel is launched as a programmatic dependent of the one before
+    # it and may start early: it must not read A or B before that kernel has
+    # finished.  Here the kernels just before the GEMM overwrite A and B
+    # (zeros before), queued behind a spin so the GEMM is launched while they
+    # run; the result must be that of the new operands.
+    dtype = _dtype(kind)
+    a, b = inputs.make_pair(M, N, K, 26, inputs.INT3, dtype=dtype)
+    a_new, b_new = a.to(DEV), b.to(DEV)
+    a_d = torch.zeros_like(a_new)
+    b_d = torch.zeros_like(b_new)
+    torch.cuda.synchronize()
+    with route_limit(route):
+        torch.cuda._sleep(2_000_000)
+        a_d.copy_(a_new)
+        b_d.copy_(b_new)
+        c = (g7.gemm_f32 if kind == "f32" else g7.gemm_bf16_f32acc)(a_d, b_d)
+        torch.cuda.synchronize()
+    c_ref, _ = oracle_ref(kind, a, b, with_abs=False)
+    assert_within(kind, c.cpu().numpy(), c_ref, None, exact=True)
+    assert g7.gemm_get_device_status() == 0
+
+
 def test_invalid_arguments_rejected_before_launch():
     a = torch.ones((4, 8), dtype=torch.bfloat16, device=DEV)
     b = torch.ones((8, 4), dtype=torch.bfloat16, device=DEV)
