@@ -632,6 +632,39 @@ def test_reads_wait_for_the_previous_kernel(kind, M, N, K, route):
     assert g7.gemm_get_device_status() == 0
 
 
+def test_chained_gemms_read_the_previous_result():
+    # Back-to-back launches of the library on one stream, each reading what
+    # the one before wrote: FP32 C1 = A.B (128 x 128 blocks) feeds
+    # C2 = C1.D (small-problem tiles); BF16 C = A1.B1 on SM pairs, then
+    # C += A2.B2 (beta = 1) on SM pairs, then on the narrow-N kernel for its
+    # first 100 columns.  Integer values keep every sum exact.
+    a, b = inputs.make_pair(512, 520, 64, 27, inputs.INT3, dtype=torch.float32)
+    d = torch.randint(-3, 4, (520, 256), generator=torch.Generator().manual_seed(28)).float()
+    c1 = g7.gemm_f32(a.to(DEV), b.to(DEV))
+    c2 = g7.gemm_f32(c1, d.to(DEV))
+    torch.cuda.synchronize()
+    ab, _ = oracle_ref("f32", a, b, with_abs=False)
+    # C1's values are integers below 2^24: exact in FP32
+    want, _ = oracle_ref("f32", torch.from_numpy(ab.astype(np.float32)), d, with_abs=False)
+    assert np.array_equal(c2.cpu().numpy().astype(np.float64), want)
+
+    M, N = 1000, 1000
+    a1, b1 = inputs.make_pair(M, N, 512, 29, inputs.INT3, dtype=torch.bfloat16)
+    a2, b2 = inputs.make_pair(M, N, 256, 30, inputs.INT3, dtype=torch.bfloat16)
+    a3, b3 = inputs.make_pair(M, 100, 192, 32, inputs.INT3, dtype=torch.bfloat16)
+    c = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    with route_limit("tensor_cores"):
+        g7.gemm_bf16_f32acc(a1.to(DEV), b1.to(DEV), out=c)
+        g7.gemm_bf16_f32acc_ex(a2.to(DEV), b2.to(DEV), out=c, beta=1.0)
+        g7.gemm_bf16_f32acc_ex(a3.to(DEV), b3.to(DEV), out=c[:, :100], beta=1.0)
+        torch.cuda.synchronize()
+    want = oracle_ref("bf16", a1, b1, with_abs=False)[0] + \
+        oracle_ref("bf16", a2, b2, with_abs=False)[0]
+    want[:, :100] += oracle_ref("bf16", a3, b3, with_abs=False)[0]
+    assert np.array_equal(c.cpu().numpy().astype(np.float64), want)
+    assert g7.gemm_get_device_status() == 0
+
+
 def test_invalid_arguments_rejected_before_launch():
     a = torch.ones((4, 8), dtype=torch.bfloat16, device=DEV)
     b = torch.ones((8, 4), dtype=torch.bfloat16, device=DEV)
