@@ -1,6 +1,7 @@
 """Calls from several host threads at once, each thread on a CUDA stream of
 its own: every result exact against the oracle (integer inputs) and no
-bounded wait runs out.
+bounded wait runs out.  The host-buffer entry points, whose copies share two
+helper streams per device, run among them.
 
 The threads race on each kernel's first-call set-up (shared-memory
 attributes and occupancy queries cached per device), and their calls run
@@ -32,6 +33,8 @@ CASES = [
     ("bf16", 300, 258, 200, False),     # small problem on the CUDA cores
     ("f32", 640, 520, 2000, False),     # FP32, partial wave split along K
     ("f32", 256, 256, 256, False),      # FP32 small problem
+    ("bf16_host", 1024, 1536, 2048, False),  # host buffers: copies on shared helper streams
+    ("f32_host", 700, 900, 1000, False),
 ]
 THREADS = 4
 REPS = 3
@@ -39,6 +42,7 @@ REPS = 3
 
 def _case_inputs(i):
     kind, M, N, K, with_bias = CASES[i]
+    kind = kind.replace("_host", "")
     dtype = torch.bfloat16 if kind == "bf16" else torch.float32
     a, b = inputs.make_pair(M, N, K, 70 + i, inputs.INT3, dtype=dtype)
     bias = (torch.randint(-4, 5, (N,), generator=torch.Generator().manual_seed(170 + i))
@@ -50,8 +54,9 @@ def _case_inputs(i):
 
 def test_concurrent_calls_from_host_threads_exact():
     data = [_case_inputs(i) for i in range(len(CASES))]
-    dev_data = [(a.to(DEV), b.to(DEV), None if bias is None else bias.to(DEV))
-                for a, b, bias, _ in data]
+    dev_data = [(a.pin_memory(), b.pin_memory(), None) if CASES[i][0].endswith("_host")
+                else (a.to(DEV), b.to(DEV), None if bias is None else bias.to(DEV))
+                for i, (a, b, bias, _) in enumerate(data)]
     torch.cuda.synchronize()
     results = {}
     errors = []
@@ -68,7 +73,11 @@ def test_concurrent_calls_from_host_threads_exact():
                 for i in order:
                     kind, M, N, K, _ = CASES[i]
                     a, b, bias = dev_data[i]
-                    if bias is not None:
+                    if kind == "bf16_host":
+                        c = g7.gemm_bf16_f32acc_host(a, b)
+                    elif kind == "f32_host":
+                        c = g7.gemm_f32_host(a, b)
+                    elif bias is not None:
                         c = g7.gemm_bf16_f32acc_ex(a, b, bias=bias)
                     elif kind == "bf16":
                         c = g7.gemm_bf16_f32acc(a, b)
