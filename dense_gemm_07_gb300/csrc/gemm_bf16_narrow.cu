@@ -76,7 +76,7 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* s
 template <int NN>
 __device__ __forceinline__ void issue_stage(uint8_t* smem, uint64_t* full, int stage,
                                             const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                            int m0, int kb) {
+                                            int m0, int n0, int kb) {
   using S = NarrowShape<NN>;
   uint8_t* sa = smem + stage * S::STAGE_BYTES;
   uint8_t* sb = sa + A_STAGE_BYTES;
@@ -84,7 +84,7 @@ __device__ __forceinline__ void issue_stage(uint8_t* smem, uint64_t* full, int s
   tma_load_2d(sa, tmA, &full[stage], kb * BK, m0);
 #pragma unroll
   for (int j = 0; j < S::B_BOXES; ++j)
-    tma_load_2d(sb + j * B_BOX_BYTES, tmB, &full[stage], j * B_BOX_COLS, kb * BK);
+    tma_load_2d(sb + j * B_BOX_BYTES, tmB, &full[stage], n0 + j * B_BOX_COLS, kb * BK);
 }
 
 // GELU: whether the GELU activation is compiled in (epi_apply); the copy
@@ -107,8 +107,11 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_ctarank());
+  // tiles in column-major order: consecutive clusters share B's columns
   const int tile = blockIdx.x / cs;
-  const int m0 = tile * TILE_M;
+  const int tiles_m = (M + TILE_M - 1) / TILE_M;
+  const int m0 = (tile % tiles_m) * TILE_M;
+  const int n0 = (tile / tiles_m) * NN;
   const int num_kb_total = (K + BK - 1) / BK;
   const int kb_begin = static_cast<int>(static_cast<int64_t>(num_kb_total) * rank / cs);
   const int kb_end = static_cast<int>(static_cast<int64_t>(num_kb_total) * (rank + 1) / cs);
@@ -139,7 +142,7 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
     const int pre = num_kb < STAGES ? num_kb : STAGES;
     for (int i = 0; i < pre; ++i)
       if (!(skip_first && i == 0))
-        issue_stage<NN>(smem, ctl->full, i, &tmA, &tmB, m0, kb_begin + i);
+        issue_stage<NN>(smem, ctl->full, i, &tmA, &tmB, m0, n0, kb_begin + i);
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, S::TMEM_COLS);
@@ -165,7 +168,7 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
           raise_abort(abort, status);
           break;
         }
-        issue_stage<NN>(smem, ctl->full, stage, &tmA, &tmB, m0, kb);
+        issue_stage<NN>(smem, ctl->full, stage, &tmA, &tmB, m0, n0, kb);
         last_phase[stage] = static_cast<int>(phase);
         if (++stage == STAGES) {
           stage = 0;
@@ -254,7 +257,8 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int TPR = NN / 4;
     constexpr int PAR = TILE_M / TPR;
     const int t = (warp - 2) * 32 + lane;
-    const int n = (t % TPR) * 4;
+    const int n = (t % TPR) * 4;  // column within the tile
+    const int gn = n0 + n;        // column of C
     const int sub = t / TPR;
     const uint32_t local = smem_u32(smem);
     const int rows = M - m0 < TILE_M ? M - m0 : TILE_M;
@@ -279,7 +283,7 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
       for (int i = 0; i < RB; ++i) {
         const int m = mb + i * step;
-        if (m >= rows || n >= N) continue;
+        if (m >= rows || gn >= N) continue;
         float sum[4] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w};
 #pragma unroll
         for (int qq = 1; qq < 8; ++qq)
@@ -290,20 +294,21 @@ gemm_bf16_narrow_kernel(const __grid_constant__ CUtensorMap tmA,
             sum[3] += v[i][qq].w;
           }
         float* crow = C + static_cast<int64_t>(m0 + m) * ldc;
-        if (vec_c && n + 3 < N) {
+        if (vec_c && gn + 3 < N) {
           float4 old = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (epi.beta != 0.0f) old = *reinterpret_cast<const float4*>(crow + n);
+          if (epi.beta != 0.0f) old = *reinterpret_cast<const float4*>(crow + gn);
           const float o[4] = {old.x, old.y, old.z, old.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            sum[e] = epi_apply<GELU>(epi, sum[e], o[e], epi.bias ? epi.bias[n + e] : 0.0f);
-          *reinterpret_cast<float4*>(crow + n) = make_float4(sum[0], sum[1], sum[2], sum[3]);
+            sum[e] = epi_apply<GELU>(epi, sum[e], o[e], epi.bias ? epi.bias[gn + e] : 0.0f);
+          *reinterpret_cast<float4*>(crow + gn) = make_float4(sum[0], sum[1], sum[2], sum[3]);
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            if (n + e < N)
-              crow[n + e] = epi_apply<GELU>(epi, sum[e], epi.beta != 0.0f ? crow[n + e] : 0.0f,
-                                            epi.bias ? epi.bias[n + e] : 0.0f);
+            if (gn + e < N)
+              crow[gn + e] = epi_apply<GELU>(epi, sum[e],
+                                             epi.beta != 0.0f ? crow[gn + e] : 0.0f,
+                                             epi.bias ? epi.bias[gn + e] : 0.0f);
         }
       }
     }
@@ -386,7 +391,7 @@ cudaError_t launch_nn(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C, 
                                      : gemm_bf16_narrow_kernel<NN, false>;
   const cudaError_t ea = set_attrs_nn<NN>(dev, slot);
   if (ea != cudaSuccess) return ea;
-  const int tiles = (M + TILE_M - 1) / TILE_M;
+  const int tiles = ((M + TILE_M - 1) / TILE_M) * ((N + NN - 1) / NN);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -410,8 +415,13 @@ cudaError_t launch_nn(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C, 
 
 int narrow_cols(int N) { return N <= 64 ? 64 : 128; }
 
-int narrow_split(int M, int K, int sms) {
-  const int tiles = (M + TILE_M - 1) / TILE_M;
+int narrow_tiles(int M, int N) {
+  const int nn = narrow_cols(N);
+  return ((M + TILE_M - 1) / TILE_M) * ((N + nn - 1) / nn);
+}
+
+int narrow_split(int M, int N, int K, int sms) {
+  const int tiles = narrow_tiles(M, N);
   const int kb = (K + BK - 1) / BK;
   int cs = sms / (tiles > 0 ? tiles : 1);
   if (cs > 8) cs = 8;
@@ -420,13 +430,13 @@ int narrow_split(int M, int K, int sms) {
 }
 
 int narrow_split_resident(int M, int N, int K, int sms) {
-  int cs = narrow_split(M, K, sms);
+  int cs = narrow_split(M, N, K, sms);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
     return cs;
   }
-  const int tiles = (M + TILE_M - 1) / TILE_M;
+  const int tiles = narrow_tiles(M, N);
   // The largest split whose clusters all fit at once (a split that does not
   // leaves some clusters for a second round); with more tiles than fit at
   // once, the split is 1 anyway.
@@ -445,7 +455,8 @@ cudaError_t launch_gemm_bf16_narrow(const CUtensorMap& tmA, const CUtensorMap& t
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || cs < 1 || cs > 8 || N < 1 || N > kNarrowMaxN || M < 1)
+  if (dev < 0 || dev >= 64 || cs < 1 || cs > 8 || N < 1 || M < 1 ||
+      static_cast<int64_t>(narrow_tiles(M, N)) * cs > 0x7FFFFFFF)
     return cudaErrorInvalidValue;
   return narrow_cols(N) == 64
              ? launch_nn<64>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 0)

@@ -159,12 +159,18 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& tmA, const CUtensorMap& tmB
 
 // ---- BF16 narrow-N path (gemm_bf16_narrow.cu), N <= kNarrowMaxN and
 // M > kSkinnyMaxM: 128-row tiles of C by all N columns, split-K over a
-// cluster, partial sums reduced through distributed shared memory.
+// cluster, partial sums reduced through distributed shared memory.  The
+// kernel also takes N > kNarrowMaxN, as 128 x 128 tiles.
 constexpr int kNarrowMaxN = 128;
-// MMA N used for N columns (64 or 128).
+// Wider N also runs on this kernel when its 128 x 128 tiles number at most
+// half the SMs and K is at least this long (the automatic schedule only).
+constexpr int kNarrowTiledMinK = 1536;
+// MMA N used for N columns (64 or 128; 128 for every N > 64).
 int narrow_cols(int N);
-// CTAs per cluster (k split) for an M x K problem on `sms` SMs (1..8).
-int narrow_split(int M, int K, int sms);
+// Tiles of an M x N problem (128 rows by narrow_cols(N) columns).
+int narrow_tiles(int M, int N);
+// CTAs per cluster (k split) for an M x N x K problem on `sms` SMs (1..8).
+int narrow_split(int M, int N, int K, int sms);
 // The same, lowered until every cluster of the launch fits on the current
 // device at once (host code).
 int narrow_split_resident(int M, int N, int K, int sms);

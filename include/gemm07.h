@@ -265,12 +265,14 @@ GEMM07_API gemm_status_t gemm_debug_inject(int mode, uint64_t wait_ns);
 /* Releases per-device state held by the library (pools, status words). */
 GEMM07_API void gemm_shutdown(void);
 
-/* ABI version of this header: 4.  Status codes are numbered as in the
+/* ABI version of this header: 5.  Status codes are numbered as in the
  * boundary definition (MISALIGNED = 2 reserved, UNSUPPORTED_DEVICE = 3,
  * LAUNCH = 4, TIMEOUT = 5, INTERNAL = 6), with NO_MEMORY = 7 and
  * SCRATCH_TOO_SMALL = 8 added (since version 3).  Since version 4, M == 1 is
  * planned as GEMM_PATH_BF16_SKINNY, GEMM_PATH_BF16_GEMV is never returned,
- * and N <= 128 < M is planned as GEMM_PATH_BF16_NARROW. */
+ * and N <= 128 < M is planned as GEMM_PATH_BF16_NARROW.  Since version 5,
+ * M > 128 and N > 128 with at most 76 tiles of 128 x 128 and K >= 1536 are
+ * planned as GEMM_PATH_BF16_NARROW too, under GEMM_SCHEDULE_AUTO. */
 GEMM07_API int gemm_abi_version(void);
 
 /*
@@ -318,7 +320,11 @@ typedef enum gemm_path {
     GEMM_PATH_BF16_NARROW = 8   /* N <= 128 < M: 128-row tiles by all N
                                    columns, K split over a cluster, A
                                    streamed once (A/B may also be copied
-                                   first: see pack_a / pack_b) */
+                                   first: see pack_a / pack_b).  Also
+                                   M, N > 128 with few tiles and a long K
+                                   (at most 76 tiles of 128 x 128, K >= 1536,
+                                   under GEMM_SCHEDULE_AUTO): 128 x 128 tiles,
+                                   K split over clusters of 2 to 8 CTAs */
 } gemm_path_t;
 
 typedef struct gemm_plan {
@@ -344,7 +350,9 @@ typedef struct gemm_plan {
 /*
  * How the BF16 paired-SM kernel (M > 128) shares out a partial last wave of
  * 256 x 256 tiles ("GEMM Optimization", section "L2 Cache and Wave Analysis":
- * a partial last wave leaves SMs idle).
+ * a partial last wave leaves SMs idle).  Under GEMM_SCHEDULE_AUTO, calls
+ * with few tiles and a long K run on the narrow-N kernel instead (see
+ * GEMM_PATH_BF16_NARROW); the other two schedules keep them on SM pairs.
  *   GEMM_SCHEDULE_AUTO: the estimated fastest of running the last wave as
  *       it is, as 256 x 128 units (when it fills at most half of the SM
  *       pairs), with each of its tiles halved along K over two pairs, or

@@ -46,7 +46,7 @@ def test_library_is_in_tree_and_for_sm103a():
 
 
 def test_abi_version(lib):
-    assert _abi.gemm_abi_version() == 4
+    assert _abi.gemm_abi_version() == 5
 
 
 def test_status_numbering_follows_the_boundary_table():
@@ -113,8 +113,24 @@ def test_plan_paths():
     assert p.workspace_bytes == 56 * 4 * 128 * 1024 + (28 * 8 + 56 * 16) * 8
     assert (p.dp_tiles, p.sk_tiles, p.sk_pairs, p.pairs) == (228, 28, 56, 76)
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
-    path, p = _path("bf16", 129, 4096, 4096)
+    path, p = _path("bf16", 129, 4096, 1024)
     assert path == "bf16_tma" and (p.tile_m, p.tile_n, p.stages) == (256, 256, 6)
+    # few 128 x 128 tiles (at most half the SMs) and K >= 1536: the narrow-N
+    # kernel with 128 x 128 tiles, K split over clusters; not for a short K,
+    # more tiles, or a schedule other than the automatic one
+    path, p = _path("bf16", 129, 4096, 4096)
+    assert path == "bf16_narrow" and (p.tile_m, p.tile_n, p.split_k) == (128, 128, 2)
+    assert p.tiles == 64 * 2 and p.workspace_bytes == 0
+    path, p = _path("bf16", 512, 1024, 8192)
+    assert path == "bf16_narrow" and p.split_k == 4 and p.tiles == 32 * 4
+    assert _path("bf16", 512, 512, 4096)[1].split_k == 8
+    assert _path("bf16", 1024, 1024, 1528)[0] == "bf16_tma"
+    assert _path("bf16", 1280, 1024, 4096)[0] == "bf16_tma"   # 80 tiles
+    prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)
+    try:
+        assert _path("bf16", 512, 1024, 8192)[0] == "bf16_tma"
+    finally:
+        _abi.gemm_set_bf16_schedule(prev)
     # M <= 128: small-M path, 128-column tiles, K split 4 ways over 32 tiles
     path, p = _path("bf16", 16, 4096, 4096)
     assert path == "bf16_skinny" and (p.tile_m, p.tile_n, p.split_k) == (16, 128, 4)
@@ -134,7 +150,9 @@ def test_plan_paths():
     assert _path("bf16", 4096, 64, 4096)[1].tile_n == 64
     assert _path("bf16", 4096, 65, 4096)[1].tile_n == 128
     assert _path("bf16", 20000, 100, 4096)[1].split_k == 1     # 157 tiles: no split
-    assert _path("bf16", 4096, 136, 4096)[0] == "bf16_tma"     # wider: SM pairs
+    assert _path("bf16", 4096, 136, 1024)[0] == "bf16_tma"     # wider, short K: SM pairs
+    assert _path("bf16", 4096, 136, 4096)[0] == "bf16_narrow"  # 64 tiles, long K
+    assert _path("bf16", 8192, 136, 4096)[0] == "bf16_tma"     # 128 tiles: SM pairs
     assert _path("bf16", 128, 64, 4096)[0] == "bf16_skinny"    # M <= 128 first
     assert _path("bf16", 33, 4096, 4096)[1].tile_m == 64
     assert _path("bf16", 128, 4096, 4096)[1].tile_m == 128
@@ -152,11 +170,15 @@ def test_plan_paths():
     # K = 3001: A rows are not a multiple of 16 bytes -> A is packed
     path, p = _path("bf16", 127, 1000, 3001)
     assert path == "bf16_skinny" and p.pack_a == 1 and p.pack_b == 0
-    path, p = _path("bf16", 300, 1000, 3001)
+    path, p = _path("bf16", 3001, 1000, 3001)
     assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
-    assert p.workspace_bytes >= 127 * 3008 * 2
+    assert p.workspace_bytes >= 3001 * 3008 * 2
+    # few tiles and a long K: the narrow-N kernel, A still copied first
+    path, p = _path("bf16", 300, 1000, 3001)
+    assert path == "bf16_narrow" and p.pack_a == 1 and p.pack_b == 0
+    assert p.workspace_bytes >= 300 * 3008 * 2
     # misaligned base address -> packed
-    path, p = _path("bf16", 300, 1000, 3001, A=16 + 2)
+    path, p = _path("bf16", 3001, 1000, 3001, A=16 + 2)
     assert path == "bf16_packed" and p.pack_a == 1 and p.pack_b == 0
     with _small_limit(0):
         path, p = _path("bf16", 256, 256, 256, A=16 + 2)

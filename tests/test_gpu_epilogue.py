@@ -60,7 +60,8 @@ PATHS = [
     ("bf16", 2048, 2561, 320, None, TC),  # half-width tail units, row stores
     ("bf16", 2560, 2304, 512, _abi.SCHEDULE_STREAM_K, TC),  # stream-K + TMA stores
     ("bf16", 2560, 2302, 512, _abi.SCHEDULE_STREAM_K, TC),  # stream-K + row stores
-    ("bf16", 512, 1024, 8192, None, TC),   # tiles halved along K; alpha-only: finished in C
+    ("bf16", 1280, 1024, 4096, None, TC),  # tiles halved along K; alpha-only: finished in C
+    ("bf16", 512, 1024, 8192, None, TC),   # few tiles, long K: 128 x 128 tiles, K split
     ("bf16", 2560, 2048, 4096, _abi.SCHEDULE_STREAM_K, TC),  # stream-K over every tile
     ("bf16", 48, 1000, 777, None, TC),   # small M, cluster reduction
     ("bf16", 1, 4096, 4096, None, TC),   # M = 1 on the small-M kernel, K split

@@ -173,10 +173,11 @@ def test_bf16_stream_k_exact(stream_k, shape):
 
 
 def test_bf16_stream_k_chosen_automatically_for_long_k():
-    # few tiles and a long K: the automatic schedule halves each tile along K
-    M, N, K = 512, 1024, 8192
+    # 20 tiles of 256 x 256 (80 of 128 x 128, too many for the narrow-N
+    # kernel) and a long K: the automatic schedule halves each tile along K
+    M, N, K = 1280, 1024, 4096
     s, p = g7.plan("bf16", M, N, K)
-    assert (p.sk_tiles, p.sk_pairs) == (8, 16)
+    assert g7.abi.PATHS[p.path] == "bf16_tma" and (p.sk_tiles, p.sk_pairs) == (20, 40)
     _check("bf16", M, N, K, 27, inputs.NORMAL)
 
 
@@ -354,6 +355,23 @@ def test_bf16_narrow_n_paths_exact(shape, route):
     if route == "tensor_cores":
         assert _abi.PATHS[plan.path] == "bf16_narrow"
     _check("bf16", M, N, K, 21, inputs.INT3, exact=True, route=route)
+
+
+@pytest.mark.parametrize("shape", [(512, 1024, 8192), (512, 512, 4096), (256, 1024, 4096),
+                                   (1000, 1000, 3001), (129, 4096, 4096), (4096, 136, 4096),
+                                   (300, 1000, 3001), (1023, 1025, 1536), (700, 1300, 6200)])
+def test_bf16_few_tiles_long_k_exact(shape):
+    # M, N > 128 with at most half as many 128 x 128 tiles as SMs and a long
+    # K run on the narrow-N kernel as 128 x 128 tiles, K split over clusters
+    # (ragged M, N and K, copied A, a last column tile of 8 columns)
+    M, N, K = shape
+    s, p = g7.plan("bf16", M, N, K)
+    assert s == 0 and g7.abi.PATHS[p.path] == "bf16_narrow" and p.tile_n == 128
+    _check("bf16", M, N, K, 34, inputs.INT3, exact=True)
+
+
+def test_bf16_few_tiles_normal_values():
+    _check("bf16", 700, 900, 4000, 35, inputs.NORMAL)
 
 
 def test_bf16_narrow_n_normal_values_and_bits():

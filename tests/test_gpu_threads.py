@@ -25,8 +25,9 @@ DEV = "cuda"
 # (kind, M, N, K, with a bias): one shape per path
 CASES = [
     ("bf16", 3001, 1000, 1000, False),  # operands copied to aligned rows, paired kernel
-    ("bf16", 512, 1024, 8192, False),   # tiles halved along K, finished in C
-    ("bf16", 512, 1024, 8192, True),    # halved tiles meeting in the partial-sum workspace
+    ("bf16", 1280, 1024, 4096, False),  # tiles halved along K, finished in C
+    ("bf16", 1280, 1024, 4096, True),   # halved tiles meeting in the partial-sum workspace
+    ("bf16", 512, 1024, 8192, False),   # few tiles, long K: 128 x 128 tiles, K split
     ("bf16", 1000, 3001, 777, False),   # row-store epilogue
     ("bf16", 16, 4096, 4096, False),    # small-M kernel, cluster reduction
     ("bf16", 1000, 100, 1200, False),   # narrow-N kernel

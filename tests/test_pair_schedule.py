@@ -142,9 +142,12 @@ def test_schedule_setting_and_plans(lib):
         # workspace, which costs more than the column split saves
         assert _plan(4096, 4096, 4096, c_addr=260) == ((256, 0, 0, 76), 0)
         assert _plan(2560, 2560, 4096, c_addr=260) == ((100, 0, 0, 76), 0)
-        # few tiles and long K: each of the 8 tiles halved along K
-        sched, ws = _plan(512, 1024, 8192)
-        assert sched == (0, 8, 16, 16) and ws >= 16 * 4 * 128 * 1024
+        # few tiles and long K: on SM pairs each of the 20 tiles would be
+        # halved along K; the automatic schedule runs 80 tiles of 128 x 128
+        # there, and fewer (512 x 1024 x 8192: 32) on the narrow-N kernel
+        sched, ws = _plan(1280, 1024, 4096)
+        assert sched == (0, 20, 40, 40) and ws >= 40 * 4 * 128 * 1024
+        assert _plan(512, 1024, 8192) == ((0, 0, 0, 0), 0)
         assert _plan(4096, 4096, 8192) == ((228, 28, 56, 76), ws_4096)
         assert _plan(5120, 5120, 4096)[0] == (380, 20, 40, 76)
         assert _plan(2560, 2560, 4096)[0] == (76, 24, 48, 76)

@@ -147,13 +147,15 @@ def test_noalloc_single_row_exact():
     assert np.array_equal(out.cpu().numpy().astype(np.float64), c_ref)
 
 
-def test_noalloc_narrow_n_exact():
+@pytest.mark.parametrize("M,N,K,packed", [(3001, 100, 1000, "b"), (300, 1000, 3001, "a")])
+def test_noalloc_narrow_n_exact(M, N, K, packed):
     # N <= 128 < M runs on the narrow-N kernel (cluster reduction, nothing in
-    # the array); B's rows of 100 elements are copied into it first
-    M, N, K = 3001, 100, 1000
+    # the array); B's rows of 100 elements are copied into it first.  So do
+    # few 128 x 128 tiles with a long K, here with A's rows copied.
     a, b = inputs.make_pair(M, N, K, 24, inputs.INT3, dtype=torch.bfloat16)
     s, plan = g7.plan("bf16", M, N, K)
-    assert _abi.PATHS[plan.path] == "bf16_narrow" and plan.pack_b == 1
+    assert _abi.PATHS[plan.path] == "bf16_narrow"
+    assert (plan.pack_a, plan.pack_b) == ((1, 0) if packed == "a" else (0, 1))
     a_d, b_d = a.to(DEV), b.to(DEV)
     out = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
     for _ in range(2):
