@@ -26,7 +26,9 @@ bool bf16_small_problem(int64_t M, int64_t N, int64_t K, bool needs_copy) {
   const int64_t cap = needs_copy && K <= kBf16SmallShortK ? kBf16SmallCopyMacs
                                                           : kBf16SmallAlignedMacs;
   const int64_t max_macs = lim < cap ? lim : cap;
-  return M >= 2 && (M >= 64 || N * K <= (int64_t(1) << 19)) && M * N * K <= max_macs;
+  // M, N, K < 2^31: M * N and N * K fit 64 bits, M * N * K need not
+  return M >= 2 && K > 0 && (M >= 64 || N * K <= (int64_t(1) << 19)) &&
+         M * N <= max_macs / K;
 }
 
 namespace {
@@ -243,7 +245,7 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
   // SM pairs (512x512x4096 11.8 against 20.0 us, 512x1024x8192 16.0
   // against 28.3, 1024x1024x4096 17.2 against 20.1, 1000x1000x3001 19.8
   // against 21.8).
-  const bool few_tiles = narrow_tiles(static_cast<int>(M), static_cast<int>(N)) * 2 <= 152 &&
+  const bool few_tiles = narrow_tiles(M, N) * 2 <= 152 &&
                          K >= kNarrowTiledMinK && g_schedule.load() == GEMM_SCHEDULE_AUTO;
   if (N <= kNarrowMaxN || few_tiles) {
     // Narrow N: 128-row tiles of C by all N columns (128 x 128 tiles when N
@@ -256,7 +258,7 @@ gemm_status_t plan_bf16(int64_t M, int64_t N, int64_t K, const void* A,
     p->tile_k = kTcTileK;
     p->stages = 0;
     p->split_k = narrow_split(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), 152);
-    p->tiles = narrow_tiles(static_cast<int>(M), static_cast<int>(N)) * p->split_k;
+    p->tiles = narrow_tiles(M, N) * p->split_k;
     return GEMM_OK;
   }
   // 256 x 256 tiles on SM pairs (the work sharing is reported for the 76

@@ -415,15 +415,15 @@ cudaError_t launch_nn(const CUtensorMap& tmA, const CUtensorMap& tmB, float* C, 
 
 int narrow_cols(int N) { return N <= 64 ? 64 : 128; }
 
-int narrow_tiles(int M, int N) {
-  const int nn = narrow_cols(N);
+int64_t narrow_tiles(int64_t M, int64_t N) {
+  const int64_t nn = N <= 64 ? 64 : 128;
   return ((M + TILE_M - 1) / TILE_M) * ((N + nn - 1) / nn);
 }
 
 int narrow_split(int M, int N, int K, int sms) {
-  const int tiles = narrow_tiles(M, N);
+  const int64_t tiles = narrow_tiles(M, N);
   const int kb = (K + BK - 1) / BK;
-  int cs = sms / (tiles > 0 ? tiles : 1);
+  int cs = static_cast<int>(sms / (tiles > 0 ? tiles : 1));
   if (cs > 8) cs = 8;
   if (cs > kb) cs = kb;
   return cs < 1 ? 1 : cs;
@@ -436,7 +436,7 @@ int narrow_split_resident(int M, int N, int K, int sms) {
     cudaGetLastError();
     return cs;
   }
-  const int tiles = narrow_tiles(M, N);
+  const int64_t tiles = narrow_tiles(M, N);
   // The largest split whose clusters all fit at once (a split that does not
   // leaves some clusters for a second round); with more tiles than fit at
   // once, the split is 1 anyway.
@@ -456,7 +456,7 @@ cudaError_t launch_gemm_bf16_narrow(const CUtensorMap& tmA, const CUtensorMap& t
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || cs < 1 || cs > 8 || N < 1 || M < 1 ||
-      static_cast<int64_t>(narrow_tiles(M, N)) * cs > 0x7FFFFFFF)
+      narrow_tiles(M, N) * cs > 0x7FFFFFFF)
     return cudaErrorInvalidValue;
   return narrow_cols(N) == 64
              ? launch_nn<64>(tmA, tmB, C, ldc, M, N, K, cs, status, epi, stream, dev, 0)

@@ -168,7 +168,7 @@ constexpr int kNarrowTiledMinK = 1536;
 // MMA N used for N columns (64 or 128; 128 for every N > 64).
 int narrow_cols(int N);
 // Tiles of an M x N problem (128 rows by narrow_cols(N) columns).
-int narrow_tiles(int M, int N);
+int64_t narrow_tiles(int64_t M, int64_t N);
 // CTAs per cluster (k split) for an M x N x K problem on `sms` SMs (1..8).
 int narrow_split(int M, int N, int K, int sms);
 // The same, lowered until every cluster of the launch fits on the current

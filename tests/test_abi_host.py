@@ -151,6 +151,11 @@ def test_plan_paths():
     assert _path("bf16", 4096, 65, 4096)[1].tile_n == 128
     assert _path("bf16", 20000, 100, 4096)[1].split_k == 1     # 157 tiles: no split
     assert _path("bf16", 4096, 136, 1024)[0] == "bf16_tma"     # wider, short K: SM pairs
+    # sizes whose M * N * K overflows 64 bits are not mistaken for small
+    # problems: their tile count is refused
+    huge = 1 << 30
+    assert _abi.gemm_plan_bf16(huge, huge, 4096, 16, 4096, 16, huge, 16, huge)[0] == \
+        _abi.GEMM_ERR_INVALID_ARG
     assert _path("bf16", 4096, 136, 4096)[0] == "bf16_narrow"  # 64 tiles, long K
     assert _path("bf16", 8192, 136, 4096)[0] == "bf16_tma"     # 128 tiles: SM pairs
     assert _path("bf16", 128, 64, 4096)[0] == "bf16_skinny"    # M <= 128 first
