@@ -105,6 +105,12 @@ bool tma_store_ok(const void* C, int64_t N, int64_t ldc) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// The elements a matrix spans (rows x leading dimension) stay at most
+// 2^60, so that byte offsets and workspace sizes fit 64 bits.
+bool span_ok(int64_t rows, int64_t ld) {
+  return rows == 0 || ld <= (int64_t(1) << 60) / rows;
+}
+
 gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
                          int64_t lda, const void* B, int64_t ldb,
                          const void* C, int64_t ldc) {
@@ -112,6 +118,7 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A,
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
   if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
     return GEMM_ERR_INVALID_ARG;
+  if (!span_ok(M, lda) || !span_ok(K, ldb) || !span_ok(M, ldc)) return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
   if (C == nullptr) return GEMM_ERR_INVALID_ARG;
   if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;

@@ -19,7 +19,8 @@
  * Conventions shared by every entry point:
  *   - Sizes and leading dimensions are element counts (int64_t).  Required:
  *     M, N, K >= 0, lda >= max(K, 1), ldb >= max(N, 1), ldc >= max(N, 1),
- *     and M, N, K < 2^31.
+ *     M, N, K < 2^31, and each matrix's rows x leading dimension (M x lda,
+ *     K x ldb, M x ldc) at most 2^60 elements.
  *   - Pointers are DEVICE pointers on the calling thread's current device,
  *     owned by the caller; the library keeps none of them after the call
  *     returns, and never frees caller memory.  A null pointer is allowed only

@@ -156,6 +156,14 @@ def test_plan_paths():
     huge = 1 << 30
     assert _abi.gemm_plan_bf16(huge, huge, 4096, 16, 4096, 16, huge, 16, huge)[0] == \
         _abi.GEMM_ERR_INVALID_ARG
+    # a matrix spanning more than 2^60 elements (rows x leading dimension)
+    # is refused, whatever M, N and K are
+    for fn in (_abi.gemm_plan_bf16, _abi.gemm_plan_f32):
+        assert fn(1 << 20, 64, 64, 16, 1 << 41, 16, 64, 16, 64)[0] == _abi.GEMM_ERR_INVALID_ARG
+        assert fn(64, 64, 1 << 20, 16, 1 << 20, 16, 1 << 41, 16, 64)[0] == \
+            _abi.GEMM_ERR_INVALID_ARG
+        assert fn(1 << 20, 64, 64, 16, 64, 16, 64, 16, 1 << 41)[0] == _abi.GEMM_ERR_INVALID_ARG
+        assert fn(1 << 20, 64, 64, 16, 1 << 40, 16, 64, 16, 64)[0] == _abi.GEMM_OK
     assert _path("bf16", 4096, 136, 4096)[0] == "bf16_narrow"  # 64 tiles, long K
     assert _path("bf16", 8192, 136, 4096)[0] == "bf16_tma"     # 128 tiles: SM pairs
     assert _path("bf16", 128, 64, 4096)[0] == "bf16_skinny"    # M <= 128 first
