@@ -42,10 +42,13 @@ def _torch():
 
 
 def _ld(t, rows_name: str) -> int:
-    """Row stride of a 2-D tensor whose rows are contiguous."""
+    """Row stride of a 2-D tensor whose rows are contiguous and do not
+    overlap (a broadcast row, stride 0, would be read past its storage)."""
     rows, cols = t.shape
     if cols > 1 and t.stride(1) != 1:
         raise ValueError(f"{rows_name}: rows must be contiguous (stride(1) == 1)")
+    if rows > 1 and cols > 0 and t.stride(0) < cols:
+        raise ValueError(f"{rows_name}: rows must not overlap (stride(0) >= columns)")
     return max(t.stride(0) if rows > 1 else cols, cols, 1)
 
 

@@ -264,6 +264,22 @@ def test_plan_and_calls_reject_bad_arguments(lib):
     assert _abi.gemm_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == _abi.GEMM_OK
 
 
+def test_binding_row_strides():
+    # the binding passes a tensor's row stride as the leading dimension: rows
+    # must be contiguous and must not overlap (a broadcast row has stride 0)
+    torch = pytest.importorskip("torch")
+    assert g7._ld(torch.zeros(4, 3), "A") == 3
+    assert g7._ld(torch.zeros(4, 8)[:, 2:5], "A") == 8     # a column slice
+    assert g7._ld(torch.zeros(1, 5), "A") == 5
+    assert g7._ld(torch.zeros(4, 1).t(), "A") == 4          # one row
+    with pytest.raises(ValueError):
+        g7._ld(torch.zeros(4, 3).t(), "A")                  # transposed
+    with pytest.raises(ValueError):
+        g7._ld(torch.zeros(1, 3).expand(4, 3), "A")         # broadcast rows
+    with pytest.raises(ValueError):
+        g7._ld(torch.zeros(12).as_strided((4, 6), (2, 1)), "A")  # overlapping rows
+
+
 def test_epilogue_entry_points_validate_on_host(lib):
     epi = _abi.GemmEpilogue(1.0, 0.0, None, 9)
     assert _abi.gemm_bf16_f32acc_ex(4, 4, 4, 16, 4, 16, 4, 16, 4, epi, None) == \
