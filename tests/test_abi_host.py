@@ -125,6 +125,10 @@ def test_plan_paths():
     assert path == "bf16_narrow" and p.split_k == 4 and p.tiles == 32 * 4
     assert _path("bf16", 512, 512, 4096)[1].split_k == 8
     assert _path("bf16", 1024, 1024, 1528)[0] == "bf16_tma"
+    # the limits exactly: 4 x 19 = 76 tiles, K 1536 / 1528
+    assert _path("bf16", 512, 2432, 1536)[0] == "bf16_narrow"
+    assert _path("bf16", 512, 2433, 1536)[0] == "bf16_packed"   # 4 x 20 tiles (B copied)
+    assert _path("bf16", 512, 2432, 1528)[0] == "bf16_tma"
     assert _path("bf16", 1280, 1024, 4096)[0] == "bf16_tma"   # 80 tiles
     prev = _abi.gemm_set_bf16_schedule(_abi.SCHEDULE_STREAM_K)
     try:
