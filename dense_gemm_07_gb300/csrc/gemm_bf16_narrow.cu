@@ -1,5 +1,5 @@
 // gemm_bf16_narrow.cu -- BF16 x BF16 -> FP32 GEMM for narrow N (N <= 128)
-// and M > 128.
+// and M > 128; also for wider N when there are few tiles and a long K.
 //
 // With few columns the product does few FLOPs per byte of A and is bound by
 // reading A, as a small-M product is bound by reading B ("How a Matrix
@@ -11,7 +11,10 @@
 //   * a tile is 128 rows of C by all N columns: D (128 x NN) = A_tile
 //     (128 x K, A read K-major as stored) x B (K x NN, B read N-major as
 //     stored), NN = 64 or 128 (tcgen05.mma M=128, N=NN; columns of B past
-//     N read as zeros);
+//     N read as zeros).  Wider N is cut into tiles of 128 columns; with at
+//     most half as many such tiles as SMs, K still splits over clusters of
+//     two or more and every SM streams its own operands, where 256 x 256
+//     tiles on SM pairs would leave most pairs idle;
 //   * one cluster of CS CTAs per tile splits K into CS contiguous ranges;
 //     each CTA runs a TMA -> mbarrier ring -> tcgen05.mma pipeline over its
 //     range;
